@@ -1,0 +1,342 @@
+#!/usr/bin/env python3
+"""Benchmark of the sm_103a attention forward (one JSON line on rank 0).
+
+A step is one attention forward over the headline workload (B=1, H=32, Nq=Nk=4096, D=128,
+bf16, non-causal, Q/K/V ~ N(0,1), scale 1/sqrt(128)). FLOPs per step are 4*B*H*Nq*Nk*D
+(halved when causal).
+
+  value     TFLOP/s of the whole job: inputs resident in device memory, W warm-up steps, then
+            exactly K timed steps between barrier + synchronize, timed with CUDA events on the
+            launching stream, max over ranks. Consecutive steps cycle through several input
+            sets whose total exceeds the 129 MB L2, so no step starts on inputs left in L2 by
+            the step before.
+  e2e       the same metric through fa_fwd_host (host buffers): each step copies Q, K, V from
+            pinned host memory, runs the kernel and copies O back.
+  roofline  the kernel against the measured dense bf16 peak (MEASURED_PEAKS.json).
+  cpu_baseline  the fp64 oracle on the host cores over a bounded sample of the workload.
+
+--impl reference times the oracle itself as the reference arm (the method's pages ship no
+runnable implementation). With torchrun (N > 1) each rank runs its own replica of the workload
+on its own GPU (the forward pass has no exchange step); value sums the work of all ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import csv
+import hashlib
+import io
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+from pathlib import Path
+
+ROOT = Path(__file__).resolve().parent
+sys.path.insert(0, str(ROOT))
+
+METRIC = "attention fwd TFLOP/s and % of GB300 dense tensor peak (B=1,H=32,L=4096,D=128)"
+KERNEL_SOURCES = ["tiled_online_softmax_gb300/csrc/fa_fwd_kernel.cuh",
+                  "tiled_online_softmax_gb300/csrc/sm103_ptx.cuh"]
+L2_BYTES = 129 * 1000 * 1000
+DATASHEET_DENSE_BF16_TFLOPS = 2250.0  # nominal, context only
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def env_rank():
+    return (int(os.environ.get("RANK", 0)), int(os.environ.get("LOCAL_RANK", 0)),
+            int(os.environ.get("WORLD_SIZE", 1)))
+
+
+def workload_desc(w):
+    return (f"{w.name}: B={w.B} H={w.H} Nq={w.Nq} Nk={w.Nk} D={w.D} {w.dtype} "
+            f"{'causal' if w.causal else 'non-causal'}")
+
+
+def load_peaks():
+    p = ROOT / "MEASURED_PEAKS.json"
+    if p.exists():
+        d = json.loads(p.read_text())
+        return d, "measured"
+    return FALLBACK_PEAKS, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for s in KERNEL_SOURCES:
+        h.update((ROOT / s).read_bytes())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload_name: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel."""
+    f = ROOT / "profiles" / f"fa_fwd_kernel_{workload_name}.md"
+    if not f.exists():
+        return None
+    kv = {}
+    for line in f.read_text().splitlines():
+        if line.startswith("- ") and ":" in line:
+            k, _, v = line[2:].partition(":")
+            kv[k.strip()] = v.strip().strip("`")
+    if kv.get("kernel_source_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the GPU works."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for row in csv.reader(io.StringIO(out)):
+            if len(row) < 9:
+                continue
+            try:
+                sm.append(float(row[1]))
+                smax.append(float(row[2]))
+                power.append(float(row[3]))
+            except ValueError:
+                continue
+            for name, val in zip(names, row[5:9]):
+                if val.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "power_w_max": max(power) if power else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+def cpu_oracle_sample(w, target_s: float = 12.0):
+    """Time the fp64 oracle over whole (b, h) slices of the workload: one slice to calibrate,
+    then as many slices as fit about `target_s` seconds. Returns (TFLOP/s, seconds, desc)."""
+    import numpy as np
+
+    import oracle
+    from tiled_online_softmax_gb300 import inputs
+
+    sub = w.with_(B=1, H=1)
+    per_slice_flops = sub.flops
+    orc = oracle.default()
+
+    def run(n_slices):
+        ws = w.with_(B=1, H=n_slices)
+        bits = inputs.draw(ws)
+        q, k, v = (inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv")
+        t0 = time.perf_counter()
+        orc.attention(q, k, v, w.scale, w.causal)
+        return time.perf_counter() - t0
+
+    t1 = run(1)
+    n = max(1, min(w.B * w.H, int(target_s / max(t1, 1e-3))))
+    t = run(n) if n > 1 else t1
+    desc = (f"{n} of {w.B * w.H} (b,h) slices of the {w.name} workload "
+            f"({n * per_slice_flops / 1e9:.1f} GFLOP), fp64 two-pass oracle, OpenMP")
+    return n * per_slice_flops / t / 1e12, t, desc, orc.num_threads()
+
+
+def run_reference(args, w):
+    """The reference arm: the fp64 oracle on the host cores (rank 0 only)."""
+    rank, _, world = env_rank()
+    if rank != 0:
+        return 0
+    tflops_runs, cores, desc = [], None, ""
+    for i in range(args.warmup + args.steps):
+        tf, _, desc, cores = cpu_oracle_sample(w, target_s=args.ref_seconds)
+        if i >= args.warmup:
+            tflops_runs.append(tf)
+    value = statistics.median(tflops_runs)
+    ms = w.flops / (value * 1e12) * 1e3
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": workload_desc(w), "global_batch": w.B, "seq_len": w.Nq,
+                   "parallelism": "cpu"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default="headline")
+    ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--ref-seconds", type=float, default=12.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+
+    from tiled_online_softmax_gb300 import inputs
+
+    w = inputs.WORKLOADS[args.workload]
+    if args.impl == "reference":
+        return run_reference(args, w)
+
+    import torch
+    import torch.distributed as dist
+
+    from tiled_online_softmax_gb300 import fa
+
+    rank, local_rank, world = env_rank()
+    if world > 1:
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl")
+    dev = torch.device("cuda", local_rank if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    fa.lib()
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+
+    # Input sets: cycle through enough of them that consecutive steps never share L2 contents.
+    bits = inputs.draw(w)
+    base = {n: inputs.to_torch(bits[n], w.dtype).to(dev) for n in "qkv"}
+    set_bytes = sum(t.numel() * 2 for t in base.values()) + base["q"].numel() * 2
+    n_sets = max(2, math.ceil(2 * L2_BYTES / set_bytes) + 1)
+    sets = []
+    for i in range(n_sets):
+        q, k, v = (base[n] if i == 0 else base[n].clone() for n in "qkv")
+        sets.append((q, k, v, torch.empty_like(q)))
+    stream = torch.cuda.current_stream(dev)
+
+    def step(i):
+        q, k, v, o = sets[i % n_sets]
+        fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=o, stream=stream)
+
+    # Warm-up, then about a second of the same work with the clock sampler already running,
+    # so its samples describe the GPU under this load.
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize(dev)
+    sampler = ClockSampler(dev.index) if rank == 0 or world > 1 else None
+    t_end = time.perf_counter() + 1.0
+    i = 0
+    while time.perf_counter() < t_end:
+        for _ in range(8):
+            step(i)
+            i += 1
+        torch.cuda.synchronize(dev)
+
+    # Timed region: exactly K steps.
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier()
+    torch.cuda.synchronize(dev)
+    ev0.record(stream)
+    for i in range(args.steps):
+        step(i)
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier()
+    ms_total = ev0.elapsed_time(ev1)
+    clocks = sampler.stop() if sampler else None
+    st, site = fa.last_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"kernel error word set during the bench (site {site})")
+
+    if world > 1:
+        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms_total = float(t.item())
+    ms_per_step = ms_total / args.steps
+    value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+
+    # e2e: host buffers through fa_fwd_host, copies inside the timed region.
+    qh, kh, vh = (inputs.to_torch(bits[n], w.dtype).pin_memory() for n in "qkv")
+    oh = torch.empty_like(qh).pin_memory()
+    fa.forward_host(qh, kh, vh, oh, causal=w.causal, scale=w.scale, stream=stream,
+                    device=dev.index)
+    barrier()
+    t0 = time.perf_counter()
+    for _ in range(args.e2e_steps):
+        fa.forward_host(qh, kh, vh, oh, causal=w.causal, scale=w.scale, stream=stream,
+                        device=dev.index)
+    e2e_s = (time.perf_counter() - t0) / args.e2e_steps
+    if world > 1:
+        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_s = float(t.item())
+    h2d = sum(t.numel() * 2 for t in (qh, kh, vh))
+    d2h = oh.numel() * 2
+
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return 0
+
+    peaks, peaks_kind = load_peaks()
+    peak = float(peaks["bf16_tflops"])
+    achieved = w.flops / (ms_per_step * 1e-3) / 1e12  # one launch per step
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "frac": achieved / peak, "traffic": profiled_traffic(w.name),
+                "peak_kind": f"{peaks_kind} bf16 dense (burst)",
+                "frac_of_datasheet": achieved / DATASHEET_DENSE_BF16_TFLOPS}
+
+    cpu = None
+    if not args.no_cpu_baseline and world >= 1:
+        tf, secs, desc, cores = cpu_oracle_sample(w, target_s=args.ref_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+               "sample": desc, "seconds": secs}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": workload_desc(w), "global_batch": w.B * world, "seq_len": w.Nq,
+                   "parallelism": f"replicas{world}",
+                   "l2": f"{n_sets} rotating input sets of {set_bytes / 2**20:.0f} MiB "
+                         f"(> L2 between consecutive steps)",
+                   "pct_of_measured_peak": 100 * achieved / peak},
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": {"value": world * w.flops / e2e_s / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": e2e_s * 1e3},
+        "clocks": clocks,
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())

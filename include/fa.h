@@ -1,0 +1,115 @@
+/*
+ * fa.h -- C interface of libfa, the sm_103a attention forward pass.
+ *
+ * The operation (sources named by page title and section):
+ *   O = softmax(scale * Q K^T) V, row by row, computed as a tiled online softmax: a tile of
+ *   128 query rows stays on chip while tiles of 128 keys stream past it, each row carrying a
+ *   running maximum m, denominator l and unnormalised accumulator o that are rescaled by
+ *   exp(m_old - m_new) when the maximum moves; o is divided by l once, at write-back.
+ *   - definition of S, P, O: "11. Fusion, recompute, and flash attention", section 11.2;
+ *   - the running (m, l, o) recurrence: same chapter, section 11.6 "Online softmax", and
+ *     "Flash Attention 2" (linearalgebraforprogrammers.com), "Overview of the algorithm";
+ *   - one tile of queries per thread block, keys streamed, division at write-back:
+ *     same chapter, section 11.9 "How FlashAttention tiles on a GPU";
+ *   - a masked, partial last key block: "Attention" (phobos stdlib docs), `attention`;
+ *   - causal masking that stops the key loop at the tile's last query: same page,
+ *     "Causal attention".
+ *
+ * Layout: Q and O are contiguous [B, H, Nq, D]; K and V are contiguous [B, H, Nk, D]; D is the
+ * innermost (fastest) index and rows of one (b, h) slice are adjacent. All four tensors have
+ * the same 16-bit element type `dtype`; accumulation is fp32 inside the kernel. O is written
+ * by rounding the fp32 result to nearest (ties to even).
+ *
+ * Causal masking (causal = 1): query i sees key j iff j <= i, counting both from 0 within
+ * their slice (top-left alignment, also when Nq != Nk). Key 0 is always visible, so no row
+ * is ever empty.
+ *
+ * Ownership: every pointer is owned by the caller. libfa keeps no reference to them after a
+ * call returns (for fa_fwd: after the launched work has finished on `stream`).
+ *
+ * Errors: every entry point returns a fa_status. Argument checks happen before any CUDA call;
+ * a rejected call has no side effect. fa_last_error_message() gives a one-line reason for the
+ * last non-FA_OK status returned on the calling host thread.
+ */
+#ifndef TILED_ONLINE_SOFTMAX_FA_H
+#define TILED_ONLINE_SOFTMAX_FA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fa_dtype {
+    FA_F16 = 0,  /* IEEE binary16 */
+    FA_BF16 = 1  /* bfloat16 */
+} fa_dtype;
+
+typedef enum fa_status {
+    FA_OK = 0,
+    FA_ERR_INVALID_ARGUMENT = 1, /* null pointer, size < 1, non-finite scale, causal not 0/1,
+                                    overlapping output, unknown dtype */
+    FA_ERR_UNSUPPORTED = 2,      /* a valid request this build has no kernel for (D not 64/128,
+                                    no sm_103a device) */
+    FA_ERR_MISALIGNED = 3,       /* a tensor pointer not 16-byte aligned */
+    FA_ERR_CUDA = 4,             /* a CUDA runtime or driver call failed */
+    FA_ERR_TIMEOUT = 5           /* a kernel's bounded wait ran out (see fa_last_device_error) */
+} fa_status;
+
+/*
+ * fa_fwd -- attention forward on device memory, asynchronous on `stream`.
+ *
+ *   Q  device pointer, [B, H, Nq, D] of `dtype`, read only.
+ *   K  device pointer, [B, H, Nk, D] of `dtype`, read only.
+ *   V  device pointer, [B, H, Nk, D] of `dtype`, read only.
+ *   O  device pointer, [B, H, Nq, D] of `dtype`, written; must not overlap Q, K or V.
+ *   B, H, Nq, Nk >= 1; B*H*max(Nq, Nk)*D must fit the tensor-map limits (2^31 rows per slice).
+ *   D      head dimension: 64 or 128 (others return FA_ERR_UNSUPPORTED).
+ *   scale  finite softmax temperature multiplying Q K^T (usually 1/sqrt(D)).
+ *   causal 0 = every key visible, 1 = causal mask as above.
+ *   stream a cudaStream_t (NULL = the legacy default stream).
+ *
+ * All four pointers must be 16-byte aligned (the tensor-memory-access unit requires it).
+ * FA_OK means validated and launched; the result is ready once `stream` reaches this point.
+ * The first call on a device allocates one 16-byte device word for kernel error reports
+ * (kept until process exit); make that first call outside any stream capture.
+ */
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H,
+                 int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, fa_dtype dtype,
+                 void* stream);
+
+/*
+ * fa_fwd_host -- the same operation on HOST buffers, synchronous.
+ *
+ * Q, K, V, O are host pointers with the layout above (pinned memory gives full copy speed).
+ * The call copies Q, K, V to device memory owned by libfa, runs fa_fwd on `stream`, copies O
+ * back and waits for the stream. The device staging buffers grow to the largest request seen
+ * and are kept until process exit (or fa_release_host_buffers). Not thread-safe: concurrent
+ * calls from several host threads must be serialised by the caller.
+ */
+fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int64_t B,
+                      int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,
+                      fa_dtype dtype, void* stream);
+
+/* Free the staging buffers of fa_fwd_host on the current device. */
+fa_status fa_release_host_buffers(void);
+
+/*
+ * fa_last_device_error -- synchronise `stream`, then read and clear the current device's
+ * kernel error word. Returns FA_ERR_TIMEOUT if a kernel launched by libfa on this device gave
+ * up a bounded wait since the last check (its output is then incomplete), FA_ERR_CUDA if the
+ * synchronisation failed, FA_OK otherwise. `site` (may be NULL) receives the wait site code.
+ */
+fa_status fa_last_device_error(void* stream, int* site);
+
+/* A static, human-readable name for a status code. */
+const char* fa_status_string(fa_status status);
+
+/* One line on why the last non-FA_OK status on this host thread was returned. */
+const char* fa_last_error_message(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TILED_ONLINE_SOFTMAX_FA_H */

@@ -1,0 +1,82 @@
+"""The C interface without a GPU: libfa.so loads, exports every function include/fa.h declares,
+and rejects bad arguments before touching CUDA. CPU only (no compute call is made)."""
+import ctypes
+import re
+from pathlib import Path
+
+import pytest
+
+ROOT = Path(__file__).resolve().parent.parent
+HEADER = (ROOT / "include" / "fa.h").read_text()
+
+
+@pytest.fixture(scope="module")
+def fa():
+    from tiled_online_softmax_gb300 import build, fa
+
+    if not fa.LIB_PATH.exists():
+        build.build()
+    fa.lib()
+    return fa
+
+
+def declared_functions():
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(fa_\w+)\s*\(", HEADER, re.M)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    assert "fa_fwd" in names and "fa_fwd_host" in names and "fa_last_device_error" in names
+
+
+def test_every_declared_symbol_is_exported(fa):
+    lib = ctypes.CDLL(str(fa.LIB_PATH))
+    missing = [n for n in declared_functions() if not hasattr(lib, n)]
+    assert not missing, missing
+    assert set(fa.EXPORTS) <= set(declared_functions())
+
+
+def test_status_strings(fa):
+    for code, name in fa.STATUS.items():
+        assert fa.status_string(code) == name
+
+
+A = 1 << 20  # a fake, 16-byte aligned address: never dereferenced (validation fails first)
+
+
+def call(fa, **kw):
+    args = dict(q=A, k=2 * A, v=3 * A, o=4 * A, B=1, H=1, Nq=128, Nk=128, D=64, scale=0.125,
+                causal=0, dtype=0)
+    args.update(kw)
+    return fa.fa_fwd(args["q"], args["k"], args["v"], args["o"], args["B"], args["H"], args["Nq"],
+                     args["Nk"], args["D"], args["scale"], args["causal"], args["dtype"], 0)
+
+
+@pytest.mark.parametrize("kw,status", [
+    (dict(q=0), 1), (dict(k=0), 1), (dict(v=0), 1), (dict(o=0), 1),
+    (dict(B=0), 1), (dict(H=-1), 1), (dict(Nq=0), 1), (dict(Nk=0), 1), (dict(D=0), 1),
+    (dict(D=96), 2), (dict(D=256), 2), (dict(D=32), 2),
+    (dict(causal=2), 1), (dict(dtype=7), 1),
+    (dict(scale=float("nan")), 1), (dict(scale=float("inf")), 1),
+    (dict(q=A + 2), 3), (dict(o=4 * A + 8), 3),
+    (dict(o=A), 1),  # output overlaps Q
+    (dict(o=2 * A + 64), 1),  # output overlaps K
+])
+def test_rejects_bad_arguments(fa, kw, status):
+    assert call(fa, **kw) == status
+    assert fa.lib().fa_last_error_message().decode()
+
+
+def test_host_entry_rejects_bad_arguments(fa):
+    assert fa.fa_fwd_host(0, A, A, A, 1, 1, 8, 8, 64, 0.1, 0, 0, 0) == 1
+    assert fa.fa_fwd_host(A, A, A, 4 * A, 1, 1, 8, 8, 80, 0.1, 0, 0, 0) == 2
+
+
+def test_binding_refuses_cpu_tensors(fa):
+    import torch
+
+    q = torch.zeros(1, 1, 8, 64, dtype=torch.float16)
+    with pytest.raises(ValueError):
+        fa.forward(q, q, q)
+    with pytest.raises(TypeError):
+        fa.forward(q.float(), q.float(), q.float())

@@ -1,0 +1,211 @@
+"""Parity of the CUDA path (called through the C interface) with the fp64 oracle.
+
+Small and medium problems are compared element by element on every output. The large
+workloads run at full size in the same launch configuration the bench times and are checked on
+sampled rows the oracle computes one by one, plus properties that hold at any size.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle
+from tests import parity
+from tiled_online_softmax_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tiled_online_softmax_gb300 import fa as fa_mod
+
+    fa_mod.lib()
+    return fa_mod
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return oracle.default()
+
+
+def run_gpu(fa, bits, w: inputs.Workload, out=None):
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    o = fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=out)
+    torch.cuda.synchronize()
+    st, site = fa.last_device_error()
+    assert st == 0, f"device error word set (site {site})"
+    return o
+
+
+def full_check(fa, orc, w: inputs.Workload, literal=True):
+    bits = inputs.draw(w)
+    o = run_gpu(fa, bits, w)
+    ref = orc.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"), w.scale, w.causal)
+    stats = parity.compare(inputs.from_torch(o), ref, w.dtype)
+    parity.assert_parity(stats, literal, w.name)
+    return stats
+
+
+def sampled_check(fa, orc, w: inputs.Workload, slices, rows_per_slice, literal=True, seed=0):
+    """Full-size run; oracle on `rows_per_slice` rows of each sampled (b, h) slice, always
+    including the first and last rows (the ragged / diagonal tiles)."""
+    bits = inputs.draw(w)
+    o = inputs.from_torch(run_gpu(fa, bits, w))
+    rng = np.random.default_rng(seed)
+    stats_all = []
+    for b, h in slices:
+        rows = np.unique(np.concatenate([[0, w.Nq - 1, w.Nq // 2],
+                                         rng.choice(w.Nq, rows_per_slice, replace=False)]))
+        q = inputs.bits_to_f64(bits["q"][b, h, rows], w.dtype)
+        k = inputs.bits_to_f64(bits["k"][b, h], w.dtype)
+        v = inputs.bits_to_f64(bits["v"][b, h], w.dtype)
+        ref = orc.attention_rows(q, rows, k, v, w.scale, w.causal)
+        stats = parity.compare(o[b, h, rows], ref, w.dtype)
+        parity.assert_parity(stats, literal, f"{w.name} slice ({b},{h})")
+        stats_all.append(stats)
+    # Any-size properties: finite, and each output is a convex combination of V rows, so it
+    # lies within [min V, max V] per column (up to output rounding).
+    of = inputs.bits_to_f64(o, w.dtype)
+    assert np.all(np.isfinite(of))
+    vf = inputs.bits_to_f64(bits["v"], w.dtype)
+    vmin, vmax = vf.min(axis=2, keepdims=True), vf.max(axis=2, keepdims=True)
+    tol = 0.5 * parity.ulp(np.maximum(np.abs(vmin), np.abs(vmax)), w.dtype) + 1e-6
+    assert np.all(of >= vmin - tol) and np.all(of <= vmax + tol)
+    return stats_all
+
+
+# --- the workloads ---------------------------------------------------------------------------
+
+def test_single_head(fa, orc):
+    full_check(fa, orc, inputs.WORKLOADS["single_head"])
+
+
+def test_ragged(fa, orc):
+    full_check(fa, orc, inputs.WORKLOADS["ragged"])
+
+
+def test_causal_prefill(fa, orc):
+    full_check(fa, orc, inputs.WORKLOADS["causal_prefill"])
+
+
+def test_rescale_stress_reduced_full_compare(fa, orc):
+    """The large-magnitude workload's distribution and sequence length on 2 heads, all outputs."""
+    w = inputs.WORKLOADS["rescale_stress"].with_(B=1, H=2)
+    full_check(fa, orc, w, literal=False)
+
+
+def test_rescale_stress_full_size(fa, orc):
+    w = inputs.WORKLOADS["rescale_stress"]
+    sampled_check(fa, orc, w, [(0, 0), (3, 31), (2, 17)], 96, literal=False)
+
+
+def test_long_causal_full_size(fa, orc):
+    w = inputs.WORKLOADS["long_causal"]
+    sampled_check(fa, orc, w, [(0, 0), (0, 15)], 64)
+
+
+def test_headline_full_size(fa, orc):
+    w = inputs.WORKLOADS["headline"]
+    sampled_check(fa, orc, w, [(0, 0), (0, 31)], 128)
+
+
+# --- edge cases ------------------------------------------------------------------------------
+
+EDGE_SIZES = [1, 2, 63, 64, 65, 127, 128, 129, 255, 257]
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("causal", [False, True])
+def test_edge_shapes(fa, orc, D, dtype, causal):
+    """Ragged query and key counts around the 128-row tile, including Nq != Nk under causal."""
+    seed = 100 + D + (dtype == "bf16") * 7 + causal * 13
+    for i, nq in enumerate(EDGE_SIZES):
+        nk = EDGE_SIZES[(i * 3 + 1) % len(EDGE_SIZES)]
+        for nq_, nk_ in ((nq, nq), (nq, nk)):
+            w = inputs.Workload(f"edge_{nq_}x{nk_}", 1, 2, nq_, nk_, D, dtype, causal,
+                                seed=seed + nq_ * 1000 + nk_)
+            full_check(fa, orc, w)
+
+
+def test_late_maximum(fa, orc):
+    """Scores that grow along the row (the running max moves at every key tile): a kernel that
+    forgets to rescale O fails here."""
+    D, n = 64, 1024
+    q = np.zeros((1, 1, n, D), np.float32)
+    k = np.zeros((1, 1, n, D), np.float32)
+    q[..., 0] = 1.0
+    k[0, 0, :, 0] = np.linspace(0, 24, n)  # score rises with the key index
+    v = np.random.default_rng(7).standard_normal((1, 1, n, D)).astype(np.float32)
+    w = inputs.Workload("late_max", 1, 1, n, n, D, "f16", False, seed=0, scale=1.0)
+    bits = {"q": inputs.round_to_bits(q, "f16"), "k": inputs.round_to_bits(k, "f16"),
+            "v": inputs.round_to_bits(v, "f16")}
+    o = run_gpu(fa, bits, w)
+    ref = orc.attention(*(inputs.bits_to_f64(bits[x], "f16") for x in "qkv"), 1.0)
+    parity.assert_parity(parity.compare(inputs.from_torch(o), ref, "f16"), True, "late max")
+
+
+def test_all_equal_scores_give_mean(fa):
+    """Q = 0: every visible key weighs the same, O is the (prefix) mean of V."""
+    for causal in (False, True):
+        w = inputs.Workload("zero_q", 1, 2, 200, 300, 128, "bf16", causal, seed=9)
+        bits = inputs.draw(w)
+        bits["q"][:] = 0
+        o = inputs.bits_to_f64(inputs.from_torch(run_gpu(fa, bits, w)), "bf16")
+        v = inputs.bits_to_f64(bits["v"], "bf16")
+        if causal:
+            want = np.cumsum(v, axis=2)[:, :, :200] / np.arange(1, 201)[None, None, :, None]
+        else:
+            want = np.broadcast_to(v.mean(axis=2, keepdims=True), o.shape)
+        assert np.max(np.abs(o - want)) < 1e-2
+
+
+def test_single_key_gives_v(fa):
+    w = inputs.Workload("one_key", 2, 3, 130, 1, 64, "f16", False, seed=10)
+    bits = inputs.draw(w)
+    o = inputs.from_torch(run_gpu(fa, bits, w))
+    assert np.array_equal(o, np.broadcast_to(bits["v"], o.shape))
+
+
+def test_deterministic_and_no_stray_writes(fa):
+    """Two runs give identical bits; bytes around O stay untouched."""
+    w = inputs.Workload("canary", 1, 3, 300, 400, 128, "bf16", True, seed=11)
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    n = q.numel()
+    pad = 4096
+    buf = torch.full((n + 2 * pad,), -7.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[pad:pad + n].view(q.shape)
+    fa.forward(q, k, v, causal=True, scale=w.scale, out=out)
+    first = out.clone()
+    fa.forward(q, k, v, causal=True, scale=w.scale, out=out)
+    torch.cuda.synchronize()
+    assert torch.equal(first.view(torch.int16), out.view(torch.int16))
+    assert bool((buf[:pad] == -7.0).all()) and bool((buf[pad + n:] == -7.0).all())
+
+
+def test_rejections_on_device(fa):
+    q = torch.zeros(1, 1, 128, 64, dtype=torch.float16, device="cuda")
+    flat = torch.zeros(128 * 64 + 8, dtype=torch.float16, device="cuda")
+    mis = flat[1:1 + 128 * 64]  # 2-byte offset
+    assert fa.fa_fwd(mis.data_ptr(), q.data_ptr(), q.data_ptr(), torch.empty_like(q).data_ptr(),
+                     1, 1, 128, 128, 64, 0.125, 0, 0, 0) == 3
+    q96 = torch.zeros(1, 1, 128, 96, dtype=torch.float16, device="cuda")
+    with pytest.raises(fa.FaError):
+        fa.forward(q96, q96, q96)
+    assert fa.last_device_error()[0] == 0
+
+
+def test_host_buffer_entry_matches_device_entry(fa):
+    w = inputs.Workload("host", 1, 4, 257, 300, 128, "bf16", False, seed=12)
+    bits = inputs.draw(w)
+    dev = inputs.from_torch(run_gpu(fa, bits, w))
+    qh, kh, vh = (inputs.to_torch(bits[n], w.dtype).pin_memory() for n in "qkv")
+    oh = torch.empty_like(qh).pin_memory()
+    fa.forward_host(qh, kh, vh, oh, causal=False, scale=w.scale)
+    assert np.array_equal(inputs.from_torch(oh), dev)

@@ -1,0 +1,308 @@
+// fa_api.cu -- the C interface of libfa (declared in include/fa.h): argument checks, TMA tensor
+// maps, launch of the sm_103a kernel, the device error word and the host-buffer entry point.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+
+#include "fa.h"
+#include "fa_fwd_kernel.cuh"
+
+namespace {
+
+constexpr int MAX_DEVICES = 64;
+constexpr int STAGES = 2;
+
+thread_local char g_msg[512] = "";
+
+fa_status fail(fa_status s, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_msg, sizeof(g_msg), fmt, ap);
+    va_end(ap);
+    return s;
+}
+
+fa_status cuda_fail(cudaError_t e, const char* what) {
+    return fail(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+std::mutex g_mutex;
+int* g_err_word[MAX_DEVICES] = {};         // device error word per device (16 bytes)
+int g_arch_ok[MAX_DEVICES] = {};           // 0 unknown, 1 sm_103, -1 other
+unsigned g_attr_set[MAX_DEVICES] = {};     // bit per kernel instance: smem attribute applied
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+unsigned long long wait_timeout_ns() {
+    static unsigned long long t = [] {
+        const char* e = getenv("FA_WAIT_TIMEOUT_NS");
+        unsigned long long v = e ? strtoull(e, nullptr, 10) : 0ull;
+        return v ? v : 1000000000ull;  // 1 s
+    }();
+    return t;
+}
+
+bool overlaps(const void* a, size_t na, const void* b, size_t nb) {
+    auto pa = reinterpret_cast<uintptr_t>(a), pb = reinterpret_cast<uintptr_t>(b);
+    return pa < pb + nb && pb < pa + na;
+}
+
+fa_status validate(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H,
+                   int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, int dtype,
+                   bool device_ptrs) {
+    if (!Q || !K || !V || !O) return fail(FA_ERR_INVALID_ARGUMENT, "null tensor pointer");
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || D < 1)
+        return fail(FA_ERR_INVALID_ARGUMENT, "sizes must be >= 1 (B=%lld H=%lld Nq=%lld Nk=%lld D=%lld)",
+                    (long long)B, (long long)H, (long long)Nq, (long long)Nk, (long long)D);
+    if (dtype != FA_F16 && dtype != FA_BF16)
+        return fail(FA_ERR_INVALID_ARGUMENT, "unknown dtype code %d", dtype);
+    if (causal != 0 && causal != 1)
+        return fail(FA_ERR_INVALID_ARGUMENT, "causal must be 0 or 1 (got %d)", causal);
+    if (!std::isfinite(scale)) return fail(FA_ERR_INVALID_ARGUMENT, "scale is not finite");
+    if (D != 64 && D != 128)
+        return fail(FA_ERR_UNSUPPORTED, "head dimension %lld not supported (64 or 128)", (long long)D);
+    // Limits of the launch (grid.x) and of the tensor maps (32-bit dims).
+    const int64_t bh = B * H;
+    if (B > (1ll << 31) || H > (1ll << 31) || bh > (1ll << 31) - 1 || Nq > (1ll << 31) - 1 ||
+        Nk > (1ll << 31) - 1)
+        return fail(FA_ERR_UNSUPPORTED, "problem too large for one launch");
+    const int64_t q_tiles = (Nq + fa::BM - 1) / fa::BM;
+    if (q_tiles > ((1ll << 31) - 1) / bh) return fail(FA_ERR_UNSUPPORTED, "too many tiles");
+    const size_t q_bytes = size_t(bh) * size_t(Nq) * size_t(D) * 2;
+    const size_t kv_bytes = size_t(bh) * size_t(Nk) * size_t(D) * 2;
+    if (device_ptrs) {
+        for (const void* p : {static_cast<const void*>(Q), static_cast<const void*>(K),
+                              static_cast<const void*>(V), static_cast<const void*>(O)})
+            if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+                return fail(FA_ERR_MISALIGNED, "tensor pointer %p is not 16-byte aligned", p);
+    }
+    if (overlaps(O, q_bytes, Q, q_bytes) || overlaps(O, q_bytes, K, kv_bytes) ||
+        overlaps(O, q_bytes, V, kv_bytes))
+        return fail(FA_ERR_INVALID_ARGUMENT, "output overlaps an input");
+    return FA_OK;
+}
+
+fa_status encode_map(CUtensorMap* map, const void* base, int64_t bh, int64_t n, int64_t D,
+                     int dtype) {
+    auto fn = encode_fn();
+    if (!fn) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(n), cuuint64_t(bh)};
+    const cuuint64_t strides[2] = {cuuint64_t(D) * 2, cuuint64_t(n) * cuuint64_t(D) * 2};
+    const cuuint32_t box[3] = {64, 128, 1};  // 128-byte rows, 128 rows (one BM or BN tile)
+    const cuuint32_t estr[3] = {1, 1, 1};
+    CUresult r = fn(map,
+                    dtype == FA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                     : CU_TENSOR_MAP_DATA_TYPE_FLOAT16,
+                    3, const_cast<void*>(base), dims, strides, box, estr,
+                    CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", int(r));
+    return FA_OK;
+}
+
+// Per-device state: architecture check and the error word. Called with no lock held.
+fa_status device_state(int* dev_out, int** err_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= MAX_DEVICES) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_arch_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (g_arch_ok[dev] != 1)
+        return fail(FA_ERR_UNSUPPORTED, "device %d is not an sm_103 GPU; libfa is built for sm_103a", dev);
+    if (!g_err_word[dev]) {
+        int* w = nullptr;
+        if ((e = cudaMalloc(&w, 16)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
+        if ((e = cudaMemset(w, 0, 16)) != cudaSuccess) {
+            cudaFree(w);
+            return cuda_fail(e, "cudaMemset(error word)");
+        }
+        g_err_word[dev] = w;
+    }
+    *dev_out = dev;
+    *err_out = g_err_word[dev];
+    return FA_OK;
+}
+
+template <int D, bool BF16, bool CAUSAL>
+fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtensorMap& mk,
+                          const CUtensorMap& mv, const fa::Params& p, cudaStream_t stream) {
+    auto kernel = fa::fa_fwd_kernel<D, BF16, CAUSAL, STAGES>;
+    constexpr int smem = fa::Smem<D, STAGES>::ALLOC_BYTES;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!(g_attr_set[dev] & (1u << inst))) {
+            cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
+            g_attr_set[dev] |= 1u << inst;
+        }
+    }
+    const unsigned grid = static_cast<unsigned>(p.num_q_tiles) * static_cast<unsigned>(p.bh);
+    kernel<<<grid, fa::NUM_THREADS, smem, stream>>>(mq, mk, mv, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
+    return FA_OK;
+}
+
+fa_status launch(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H,
+                 int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, int dtype,
+                 cudaStream_t stream) {
+    int dev = 0;
+    int* err = nullptr;
+    fa_status s = device_state(&dev, &err);
+    if (s != FA_OK) return s;
+    const int64_t bh = B * H;
+    CUtensorMap mq, mk, mv;
+    if ((s = encode_map(&mq, Q, bh, Nq, D, dtype)) != FA_OK) return s;
+    if ((s = encode_map(&mk, K, bh, Nk, D, dtype)) != FA_OK) return s;
+    if ((s = encode_map(&mv, V, bh, Nk, D, dtype)) != FA_OK) return s;
+    fa::Params p{};
+    p.o = O;
+    p.err = err;
+    p.bh = static_cast<int>(bh);
+    p.nq = static_cast<int>(Nq);
+    p.nk = static_cast<int>(Nk);
+    p.num_q_tiles = static_cast<int>((Nq + fa::BM - 1) / fa::BM);
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.timeout_ns = wait_timeout_ns();
+    const bool bf16 = dtype == FA_BF16;
+    const int inst = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
+    switch (inst) {
+        case 0: return launch_instance<64, false, false>(dev, inst, mq, mk, mv, p, stream);
+        case 1: return launch_instance<64, false, true>(dev, inst, mq, mk, mv, p, stream);
+        case 2: return launch_instance<64, true, false>(dev, inst, mq, mk, mv, p, stream);
+        case 3: return launch_instance<64, true, true>(dev, inst, mq, mk, mv, p, stream);
+        case 4: return launch_instance<128, false, false>(dev, inst, mq, mk, mv, p, stream);
+        case 5: return launch_instance<128, false, true>(dev, inst, mq, mk, mv, p, stream);
+        case 6: return launch_instance<128, true, false>(dev, inst, mq, mk, mv, p, stream);
+        default: return launch_instance<128, true, true>(dev, inst, mq, mk, mv, p, stream);
+    }
+}
+
+// Staging buffers of fa_fwd_host on each device.
+struct Staging {
+    void* buf = nullptr;
+    size_t bytes = 0;
+};
+Staging g_staging[MAX_DEVICES];
+
+}  // namespace
+
+extern "C" {
+
+fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H,
+                 int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, fa_dtype dtype,
+                 void* stream) {
+    fa_status s = validate(Q, K, V, O, B, H, Nq, Nk, D, scale, causal, int(dtype), true);
+    if (s != FA_OK) return s;
+    return launch(Q, K, V, O, B, H, Nq, Nk, D, scale, causal, int(dtype),
+                  static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int64_t B,
+                      int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,
+                      fa_dtype dtype, void* stream) {
+    fa_status s = validate(Q, K, V, O, B, H, Nq, Nk, D, scale, causal, int(dtype), false);
+    if (s != FA_OK) return s;
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= MAX_DEVICES) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
+    const size_t q_bytes = size_t(B * H) * size_t(Nq) * size_t(D) * 2;
+    const size_t kv_bytes = size_t(B * H) * size_t(Nk) * size_t(D) * 2;
+    auto round_up = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const size_t need = 2 * round_up(q_bytes) + 2 * round_up(kv_bytes);
+    Staging& st = g_staging[dev];
+    if (st.bytes < need) {
+        if (st.buf) cudaFree(st.buf);
+        st.buf = nullptr;
+        st.bytes = 0;
+        if ((e = cudaMalloc(&st.buf, need)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(staging)");
+        st.bytes = need;
+    }
+    auto* base = static_cast<uint8_t*>(st.buf);
+    void* dq = base;
+    void* dk = base + round_up(q_bytes);
+    void* dv = base + round_up(q_bytes) + round_up(kv_bytes);
+    void* dout = base + round_up(q_bytes) + 2 * round_up(kv_bytes);
+    auto strm = static_cast<cudaStream_t>(stream);
+    if ((e = cudaMemcpyAsync(dq, Q, q_bytes, cudaMemcpyHostToDevice, strm)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dk, K, kv_bytes, cudaMemcpyHostToDevice, strm)) != cudaSuccess ||
+        (e = cudaMemcpyAsync(dv, V, kv_bytes, cudaMemcpyHostToDevice, strm)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync(host to device)");
+    s = launch(dq, dk, dv, dout, B, H, Nq, Nk, D, scale, causal, int(dtype), strm);
+    if (s != FA_OK) return s;
+    if ((e = cudaMemcpyAsync(O, dout, q_bytes, cudaMemcpyDeviceToHost, strm)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpyAsync(device to host)");
+    if ((e = cudaStreamSynchronize(strm)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    return FA_OK;
+}
+
+fa_status fa_release_host_buffers(void) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev >= 0 && dev < MAX_DEVICES && g_staging[dev].buf) {
+        e = cudaFree(g_staging[dev].buf);
+        g_staging[dev] = Staging{};
+        if (e != cudaSuccess) return cuda_fail(e, "cudaFree(staging)");
+    }
+    return FA_OK;
+}
+
+fa_status fa_last_device_error(void* stream, int* site) {
+    if (site) *site = 0;
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= MAX_DEVICES || !g_err_word[dev]) return FA_OK;
+    int word = 0;
+    if ((e = cudaMemcpy(&word, g_err_word[dev], sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+        return cuda_fail(e, "cudaMemcpy(error word)");
+    if (word == 0) return FA_OK;
+    if (site) *site = word;
+    if ((e = cudaMemset(g_err_word[dev], 0, 16)) != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+    return fail(FA_ERR_TIMEOUT, "a kernel gave up waiting at site %d", word);
+}
+
+const char* fa_status_string(fa_status status) {
+    switch (status) {
+        case FA_OK: return "FA_OK";
+        case FA_ERR_INVALID_ARGUMENT: return "FA_ERR_INVALID_ARGUMENT";
+        case FA_ERR_UNSUPPORTED: return "FA_ERR_UNSUPPORTED";
+        case FA_ERR_MISALIGNED: return "FA_ERR_MISALIGNED";
+        case FA_ERR_CUDA: return "FA_ERR_CUDA";
+        case FA_ERR_TIMEOUT: return "FA_ERR_TIMEOUT";
+    }
+    return "FA_ERR_UNKNOWN";
+}
+
+const char* fa_last_error_message(void) { return g_msg; }
+
+}  // extern "C"

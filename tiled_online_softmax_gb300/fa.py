@@ -1,0 +1,152 @@
+"""ctypes binding of libfa (include/fa.h). Argument marshalling only: every step of the attention
+forward runs in the library's CUDA kernels. There is no fallback: without a built libfa.so or a
+GPU, every call raises."""
+from __future__ import annotations
+
+import ctypes
+import math
+from pathlib import Path
+
+LIB_PATH = Path(__file__).resolve().with_name("libfa.so")
+
+FA_F16, FA_BF16 = 0, 1
+STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED",
+          3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
+EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_error",
+           "fa_status_string", "fa_last_error_message")
+
+
+class FaError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS.get(status, status)}: {message}")
+        self.status = status
+
+
+_lib: ctypes.CDLL | None = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libfa.so with its signatures declared."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not LIB_PATH.exists():
+        raise RuntimeError(f"{LIB_PATH} is not built: run tiled_online_softmax_gb300.build.build()")
+    L = ctypes.CDLL(str(LIB_PATH))
+    i64, vp = ctypes.c_int64, ctypes.c_void_p
+    sig = [vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
+    L.fa_fwd.argtypes = sig
+    L.fa_fwd.restype = ctypes.c_int
+    L.fa_fwd_host.argtypes = sig
+    L.fa_fwd_host.restype = ctypes.c_int
+    L.fa_release_host_buffers.argtypes = []
+    L.fa_release_host_buffers.restype = ctypes.c_int
+    L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
+    L.fa_last_device_error.restype = ctypes.c_int
+    L.fa_status_string.argtypes = [ctypes.c_int]
+    L.fa_status_string.restype = ctypes.c_char_p
+    L.fa_last_error_message.argtypes = []
+    L.fa_last_error_message.restype = ctypes.c_char_p
+    _lib = L
+    return L
+
+
+def _raise_if(status: int) -> None:
+    if status != 0:
+        raise FaError(status, lib().fa_last_error_message().decode())
+
+
+def fa_fwd(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, B: int, H: int, Nq: int, Nk: int,
+           D: int, scale: float, causal: int, dtype: int, stream: int = 0) -> int:
+    """The raw C call on device pointers; returns the fa_status code."""
+    return lib().fa_fwd(q_ptr, k_ptr, v_ptr, o_ptr, B, H, Nq, Nk, D, scale, causal, dtype, stream)
+
+
+def fa_fwd_host(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, B: int, H: int, Nq: int,
+                Nk: int, D: int, scale: float, causal: int, dtype: int, stream: int = 0) -> int:
+    """The raw C call on host pointers (synchronous); returns the fa_status code."""
+    return lib().fa_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, B, H, Nq, Nk, D, scale, causal, dtype,
+                             stream)
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float16:
+        return FA_F16
+    if t.dtype == torch.bfloat16:
+        return FA_BF16
+    raise TypeError(f"attention inputs must be float16 or bfloat16, got {t.dtype}")
+
+
+def _shape(q, k, v):
+    if q.dim() != 4 or k.dim() != 4 or v.dim() != 4:
+        raise ValueError("q, k, v must be [B, H, N, D]")
+    B, H, Nq, D = q.shape
+    if k.shape[:2] != (B, H) or k.shape[3] != D or v.shape != k.shape:
+        raise ValueError(f"shape mismatch: q {tuple(q.shape)}, k {tuple(k.shape)}, v {tuple(v.shape)}")
+    if not (q.dtype == k.dtype == v.dtype):
+        raise TypeError("q, k, v must share one dtype")
+    for t in (q, k, v):
+        if not t.is_contiguous():
+            raise ValueError("q, k, v must be contiguous")
+    return B, H, Nq, k.shape[2], D
+
+
+def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None, stream=None):
+    """O = softmax(scale * q k^T) v for CUDA tensors q [B,H,Nq,D], k, v [B,H,Nk,D].
+
+    Launches on `stream` (default: torch's current stream) and returns `out` without waiting.
+    """
+    import torch
+
+    B, H, Nq, Nk, D = _shape(q, k, v)
+    code = _dtype_code(q)
+    if not q.is_cuda:
+        raise ValueError("forward() takes CUDA tensors; use forward_host() for host buffers")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        _raise_if(fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, Nq, Nk,
+                         D, float(scale), int(bool(causal)), code, stream.cuda_stream))
+    return out
+
+
+def forward_host(q, k, v, out, causal: bool = False, scale: float | None = None, stream=None,
+                 device: int = 0):
+    """The same on host (CPU, ideally pinned) tensors: copies in, runs, copies out, waits."""
+    import torch
+
+    B, H, Nq, Nk, D = _shape(q, k, v)
+    if q.is_cuda or out.is_cuda:
+        raise ValueError("forward_host() takes host tensors")
+    if out.shape != q.shape or out.dtype != q.dtype or not out.is_contiguous():
+        raise ValueError("out must be a contiguous tensor shaped and typed like q")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    with torch.cuda.device(device):
+        if stream is None:
+            stream = torch.cuda.current_stream(device)
+        _raise_if(fa_fwd_host(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H,
+                              Nq, Nk, D, float(scale), int(bool(causal)), _dtype_code(q),
+                              stream.cuda_stream))
+    return out
+
+
+def last_device_error(stream=None) -> tuple[int, int]:
+    """Synchronise `stream` and return (status, wait-site code) of the device error word."""
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    site = ctypes.c_int(0)
+    st = lib().fa_last_device_error(stream.cuda_stream, ctypes.byref(site))
+    return st, site.value
+
+
+def status_string(status: int) -> str:
+    return lib().fa_status_string(status).decode()
