@@ -134,42 +134,49 @@ class ClockSampler:
                 "samples": len(sm), "reasons": sorted(reasons)}
 
 
-def cpu_oracle_sample(w, target_s: float = 12.0):
-    """Time the fp64 oracle over whole (b, h) slices of the workload: one slice to calibrate,
-    then as many slices as fit about `target_s` seconds. Returns (TFLOP/s, seconds, desc)."""
-    import numpy as np
+class OracleSample:
+    """The fp64 oracle over whole (b, h) slices of the workload, timed on the host cores.
 
-    import oracle
-    from tiled_online_softmax_gb300 import inputs
+    One slice calibrates the per-slice time; a run then covers as many slices as fit the
+    requested seconds (at least one, at most all B*H). Inputs are drawn once, outside timing."""
 
-    sub = w.with_(B=1, H=1)
-    per_slice_flops = sub.flops
-    orc = oracle.default()
+    def __init__(self, w):
+        import oracle
+        from tiled_online_softmax_gb300 import inputs
 
-    def run(n_slices):
-        ws = w.with_(B=1, H=n_slices)
-        bits = inputs.draw(ws)
-        q, k, v = (inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv")
+        self.w = w
+        self.orc = oracle.default()
+        self.cores = self.orc.num_threads()
+        n_all = w.B * w.H
+        bits = inputs.draw(w.with_(B=1, H=n_all))
+        self.q, self.k, self.v = (inputs.bits_to_f64(bits[n][0], w.dtype) for n in "qkv")
+        self.slice_flops = w.with_(B=1, H=1).flops
+        self.t_slice = self._time(1)
+
+    def _time(self, n):
         t0 = time.perf_counter()
-        orc.attention(q, k, v, w.scale, w.causal)
+        self.orc.attention(self.q[:n], self.k[:n], self.v[:n], self.w.scale, self.w.causal)
         return time.perf_counter() - t0
 
-    t1 = run(1)
-    n = max(1, min(w.B * w.H, int(target_s / max(t1, 1e-3))))
-    t = run(n) if n > 1 else t1
-    desc = (f"{n} of {w.B * w.H} (b,h) slices of the {w.name} workload "
-            f"({n * per_slice_flops / 1e9:.1f} GFLOP), fp64 two-pass oracle, OpenMP")
-    return n * per_slice_flops / t / 1e12, t, desc, orc.num_threads()
+    def run(self, seconds: float):
+        n = max(1, min(len(self.q), int(seconds / max(self.t_slice, 1e-4))))
+        t = self._time(n)
+        desc = (f"{n} of {len(self.q)} (b,h) slices of the {self.w.name} workload "
+                f"({n * self.slice_flops / 1e9:.1f} GFLOP), fp64 two-pass oracle, OpenMP")
+        return n * self.slice_flops / t / 1e12, t, desc
 
 
 def run_reference(args, w):
-    """The reference arm: the fp64 oracle on the host cores (rank 0 only)."""
+    """The reference arm: the fp64 oracle on the host cores (rank 0 only), each step a bounded
+    sample of the workload sized so that the whole run takes about two minutes."""
     rank, _, world = env_rank()
     if rank != 0:
         return 0
-    tflops_runs, cores, desc = [], None, ""
+    sample = OracleSample(w)
+    per_step = min(args.ref_seconds, 120.0 / (args.warmup + args.steps))
+    tflops_runs, desc = [], ""
     for i in range(args.warmup + args.steps):
-        tf, _, desc, cores = cpu_oracle_sample(w, target_s=args.ref_seconds)
+        tf, _, desc = sample.run(per_step)
         if i >= args.warmup:
             tflops_runs.append(tf)
     value = statistics.median(tflops_runs)
@@ -181,8 +188,8 @@ def run_reference(args, w):
         "data": "synthetic",
         "config": {"workload": workload_desc(w), "global_batch": w.B, "seq_len": w.Nq,
                    "parallelism": "cpu"},
-        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": desc},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": sample.cores,
+                         "kind": "oracle", "sample": desc},
         "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -200,6 +207,9 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=10)
     ap.add_argument("--ref-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="profiler runs: only the warm-up and timed launches (no clock pre-heat, "
+                         "e2e or CPU leg); the printed numbers are not bench values")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
 
@@ -246,8 +256,8 @@ def main():
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(dev.index) if rank == 0 or world > 1 else None
-    t_end = time.perf_counter() + 1.0
+    sampler = ClockSampler(dev.index) if not args.profile else None
+    t_end = time.perf_counter() + (0.0 if args.profile else 1.0)
     i = 0
     while time.perf_counter() < t_end:
         for _ in range(8):
@@ -277,6 +287,11 @@ def main():
         ms_total = float(t.item())
     ms_per_step = ms_total / args.steps
     value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+
+    if args.profile:
+        if rank == 0:
+            print(json.dumps({"profile_run": True, "ms_per_step": ms_per_step}), flush=True)
+        return 0
 
     # e2e: host buffers through fa_fwd_host, copies inside the timed region.
     qh, kh, vh = (inputs.to_torch(bits[n], w.dtype).pin_memory() for n in "qkv")
@@ -310,9 +325,10 @@ def main():
                 "frac_of_datasheet": achieved / DATASHEET_DENSE_BF16_TFLOPS}
 
     cpu = None
-    if not args.no_cpu_baseline and world >= 1:
-        tf, secs, desc, cores = cpu_oracle_sample(w, target_s=args.ref_seconds)
-        cpu = {"value": tf, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+    if not args.no_cpu_baseline:
+        sample = OracleSample(w)
+        tf, secs, desc = sample.run(args.ref_seconds)
+        cpu = {"value": tf, "unit": "TFLOP/s", "cores": sample.cores, "kind": "oracle",
                "sample": desc, "seconds": secs}
 
     line = {

@@ -4,9 +4,13 @@ Tolerance (the attention forward's stated bar): max |err| <= 1e-2 and mean |err|
 the exact result, for fp32 accumulation with fp16/bf16 inputs and output. Rounding the exact
 result to the 16-bit output type already costs up to half an ulp of |O|; on inputs where |O|
 exceeds 2 (the large-magnitude workload, Q and K ~ N(0, 9)), half a bf16 ulp is 0.0156 > 1e-2,
-so no 16-bit output can meet the literal bound there. For those elements the bound reads
-|err| <= 1e-2 + ulp(O_ref)/2, and the report always gives the literal max, the mean and the
-rounding floor max |round(O_ref) - O_ref|.
+so no 16-bit output can meet the literal bound there. Likewise, on tiny problems (a row or two,
+few keys) |O| is about 1 and bf16 output rounding alone averages about 1e-3. The relaxed
+reading therefore charges the kernel only for error beyond the unavoidable output rounding:
+elementwise |err| <= 1e-2 + ulp(O_ref)/2 and mean |err| <= 1e-3 + mean |round(O_ref) - O_ref|.
+The literal bound is asserted on every named N(0,1) workload; the relaxed one on the
+large-magnitude workload and on the small edge-shape cases. The report always gives the literal
+max and mean and the rounding floor.
 """
 import numpy as np
 
@@ -30,14 +34,15 @@ def compare(out_bits: np.ndarray, ref: np.ndarray, dtype: str) -> dict:
     bound = MAX_ERR + 0.5 * ulp(ref, dtype)
     return dict(
         max_err=float(err.max()), mean_err=float(err.mean()), rounding_floor=float(floor.max()),
-        n=int(err.size), finite=bool(np.all(np.isfinite(got))),
+        mean_floor=float(floor.mean()), n=int(err.size), finite=bool(np.all(np.isfinite(got))),
         worst_excess=float((err - bound).max()),
     )
 
 
 def assert_parity(stats: dict, literal: bool = True, what: str = "") -> None:
     assert stats["finite"], f"{what}: non-finite output"
-    assert stats["mean_err"] <= MEAN_ERR, f"{what}: mean |err| {stats['mean_err']:.3g} > {MEAN_ERR}"
+    mean_bound = MEAN_ERR if literal else MEAN_ERR + stats["mean_floor"]
+    assert stats["mean_err"] <= mean_bound, f"{what}: mean |err| {stats['mean_err']:.3g} > {mean_bound:.3g}"
     if literal:
         assert stats["max_err"] <= MAX_ERR, f"{what}: max |err| {stats['max_err']:.3g} > {MAX_ERR}"
     else:

@@ -155,6 +155,15 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+    if constexpr (BF16) {
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    } else {
+        return __half22float2(*reinterpret_cast<const __half2*>(&u));
+    }
+}
+
 // ---------------------------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------------------------
@@ -363,26 +372,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int n_vis = k_end - k0;  // may be <= 0 only for padding rows past Nq
             const bool full_tile = (n_vis >= BN);
 
-            // Tile maximum of the scaled scores over visible keys.
+            // Tile maximum of the scaled scores over visible keys. Scaling by c >= 0 is monotone
+            // in floating point, so the maximum is taken on the raw scores and scaled once
+            // (for c < 0 the minimum plays that role).
+            const bool neg = c < 0.f;
             float mx[8];
 #pragma unroll
             for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-            if (full_tile) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q)
+            for (int q = 0; q < 4; ++q)
 #pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sr[q][i]) * c);
-            } else {
-#pragma unroll
-                for (int q = 0; q < 4; ++q)
-#pragma unroll
-                    for (int i = 0; i < 32; ++i)
-                        if (q * 32 + i < n_vis)
-                            mx[i & 7] = fmaxf(mx[i & 7], __uint_as_float(sr[q][i]) * c);
-            }
-            const float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                       fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+                for (int i = 0; i < 32; ++i) {
+                    const float sv = neg ? -__uint_as_float(sr[q][i]) : __uint_as_float(sr[q][i]);
+                    if (full_tile || q * 32 + i < n_vis) mx[i & 7] = fmaxf(mx[i & 7], sv);
+                }
+            float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
+                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
+            m_tile = (m_tile == -INFINITY) ? -INFINITY : (neg ? -m_tile : m_tile) * c;
             const float m_new = fmaxf(m, m_tile);
             // An empty state (m = -inf) has nothing to rescale; an all-hidden row keeps m = -inf
             // and is given weight 0 below.
@@ -403,9 +409,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         if (q * 32 + i >= n_vis) p0 = 0.f;
                         if (q * 32 + i + 1 >= n_vis) p1 = 0.f;
                     }
-                    sum[i & 7] += p0;
-                    sum[(i + 1) & 7] += p1;
-                    pk[q >> 1][(q & 1) * 16 + i / 2] = pack2<BF16>(p0, p1);
+                    // l sums the same 16-bit-rounded weights the PV product uses, so the
+                    // final O / l is an exact weighted average of V under those weights.
+                    const uint32_t u = pack2<BF16>(p0, p1);
+                    const float2 r = unpack2<BF16>(u);
+                    sum[i & 7] += r.x;
+                    sum[(i + 1) & 7] += r.y;
+                    pk[q >> 1][(q & 1) * 16 + i / 2] = u;
                 }
             }
             const float rowsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) +
