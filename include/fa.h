@@ -95,6 +95,38 @@ fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int6
 fa_status fa_release_host_buffers(void);
 
 /*
+ * fa_fwd_noalloc -- fa_fwd for callers that must not allocate device memory.
+ * (The attention pages have no counterpart to this entry point: it only changes where the
+ * kernel's scratch lives.)
+ *
+ * Who needs it: code that runs where cudaMalloc is off limits -- inside a custom allocator or
+ * memory-pool callback, in a process whose device memory was reserved up front by a framework
+ * pool, or in code that must not allocate after start-up (fixed-footprint serving, real-time
+ * paths). fa_fwd allocates a small device error record on its first call on each device; this
+ * entry point never calls cudaMalloc, cudaFree or any allocating routine.
+ *
+ * Scratch: the kernel's only scratch is its error record (one int, site code of a timed-out
+ * wait). Here it lives in a file-scope device array of FA_NOALLOC_SCRATCH_BYTES bytes, which
+ * every GPU that loads libfa holds until process exit. A request whose scratch would exceed
+ * that array is rejected with FA_ERR_UNSUPPORTED (the record does not grow with B, H, Nq, Nk or
+ * D, so no valid problem reaches that limit today).
+ *
+ * Arguments, layouts, ownership and validation are those of fa_fwd (device pointers, async
+ * on `stream`). Each call clears the record with cudaMemsetAsync on `stream` before its launch.
+ * All calls share the one array and it keeps the last call's contents, so calls that overlap on
+ * the GPU (different streams with no ordering between them) race on it. The record is not read
+ * back by any entry point; a timeout there means the output of that call is incomplete.
+ *
+ * The first call on each device, with that device current, looks up the array's device address
+ * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that first call before
+ * any stream capture.
+ */
+#define FA_NOALLOC_SCRATCH_BYTES 256
+fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, int64_t B,
+                         int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,
+                         fa_dtype dtype, void* stream);
+
+/*
  * fa_last_device_error -- synchronise `stream`, then read and clear the current device's
  * kernel error word. Returns FA_ERR_TIMEOUT if a kernel launched by libfa on this device gave
  * up a bounded wait since the last check (its output is then incomplete), FA_ERR_CUDA if the

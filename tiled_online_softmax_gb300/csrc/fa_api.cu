@@ -211,9 +211,86 @@ struct Staging {
 };
 Staging g_staging[MAX_DEVICES];
 
+// ---------------------------------------------------------------------------------------------
+// Allocation-free variant (fa_fwd_noalloc): the kernel's error record lives in this file-scope
+// device array instead of device memory from cudaMalloc. Host code must not pass the symbol
+// itself to a kernel (on the host it names a stand-in, not a device address): its device address
+// comes from cudaGetSymbolAddress, once per device, with that device current.
+// ---------------------------------------------------------------------------------------------
+static __device__ __align__(256) int g_noalloc_scratch[FA_NOALLOC_SCRATCH_BYTES / sizeof(int)];
+constexpr size_t NOALLOC_RECORD_BYTES = 16;  // what the kernel needs: one error word, padded
+int* g_noalloc_addr[MAX_DEVICES] = {};
+
+fa_status noalloc_device_state(int* dev_out, int** scratch_out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= MAX_DEVICES) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_arch_ok[dev] == 0) {
+        int major = 0, minor = 0;
+        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
+    }
+    if (g_arch_ok[dev] != 1)
+        return fail(FA_ERR_UNSUPPORTED, "device %d is not an sm_103 GPU; libfa is built for sm_103a", dev);
+    if (!g_noalloc_addr[dev]) {
+        void* addr = nullptr;
+        if ((e = cudaGetSymbolAddress(&addr, g_noalloc_scratch)) != cudaSuccess)
+            return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+        g_noalloc_addr[dev] = static_cast<int*>(addr);
+    }
+    *dev_out = dev;
+    *scratch_out = g_noalloc_addr[dev];
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
+
+fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, int64_t B,
+                         int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,
+                         fa_dtype dtype, void* stream) {
+    fa_status s = validate(Q, K, V, O, B, H, Nq, Nk, D, scale, causal, int(dtype), true);
+    if (s != FA_OK) return s;
+    if (NOALLOC_RECORD_BYTES > FA_NOALLOC_SCRATCH_BYTES)
+        return fail(FA_ERR_UNSUPPORTED, "request needs %zu bytes of scratch; the static array holds %d",
+                    NOALLOC_RECORD_BYTES, FA_NOALLOC_SCRATCH_BYTES);
+    int dev = 0;
+    int* scratch = nullptr;
+    if ((s = noalloc_device_state(&dev, &scratch)) != FA_OK) return s;
+    auto strm = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(scratch, 0, NOALLOC_RECORD_BYTES, strm);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch)");
+    const int64_t bh = B * H;
+    CUtensorMap mq, mk, mv;
+    if ((s = encode_map(&mq, Q, bh, Nq, D, int(dtype))) != FA_OK) return s;
+    if ((s = encode_map(&mk, K, bh, Nk, D, int(dtype))) != FA_OK) return s;
+    if ((s = encode_map(&mv, V, bh, Nk, D, int(dtype))) != FA_OK) return s;
+    fa::Params p{};
+    p.o = O;
+    p.err = scratch;
+    p.bh = static_cast<int>(bh);
+    p.nq = static_cast<int>(Nq);
+    p.nk = static_cast<int>(Nk);
+    p.num_q_tiles = static_cast<int>((Nq + fa::BM - 1) / fa::BM);
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.timeout_ns = wait_timeout_ns();
+    const int inst = (D == 128 ? 4 : 0) + (dtype == FA_BF16 ? 2 : 0) + (causal ? 1 : 0);
+    switch (inst) {
+        case 0: return launch_instance<64, false, false>(dev, inst, mq, mk, mv, p, strm);
+        case 1: return launch_instance<64, false, true>(dev, inst, mq, mk, mv, p, strm);
+        case 2: return launch_instance<64, true, false>(dev, inst, mq, mk, mv, p, strm);
+        case 3: return launch_instance<64, true, true>(dev, inst, mq, mk, mv, p, strm);
+        case 4: return launch_instance<128, false, false>(dev, inst, mq, mk, mv, p, strm);
+        case 5: return launch_instance<128, false, true>(dev, inst, mq, mk, mv, p, strm);
+        case 6: return launch_instance<128, true, false>(dev, inst, mq, mk, mv, p, strm);
+        default: return launch_instance<128, true, true>(dev, inst, mq, mk, mv, p, strm);
+    }
+}
 
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H,
                  int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, fa_dtype dtype,

@@ -13,7 +13,7 @@ FA_F16, FA_BF16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED",
           3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_error",
-           "fa_status_string", "fa_last_error_message")
+           "fa_status_string", "fa_last_error_message", "fa_fwd_noalloc")
 
 
 class FaError(RuntimeError):
@@ -39,6 +39,8 @@ def lib() -> ctypes.CDLL:
     L.fa_fwd.restype = ctypes.c_int
     L.fa_fwd_host.argtypes = sig
     L.fa_fwd_host.restype = ctypes.c_int
+    L.fa_fwd_noalloc.argtypes = sig
+    L.fa_fwd_noalloc.restype = ctypes.c_int
     L.fa_release_host_buffers.argtypes = []
     L.fa_release_host_buffers.restype = ctypes.c_int
     L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
@@ -67,6 +69,13 @@ def fa_fwd_host(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, B: int, H: int, 
     """The raw C call on host pointers (synchronous); returns the fa_status code."""
     return lib().fa_fwd_host(q_ptr, k_ptr, v_ptr, o_ptr, B, H, Nq, Nk, D, scale, causal, dtype,
                              stream)
+
+
+def fa_fwd_noalloc(q_ptr: int, k_ptr: int, v_ptr: int, o_ptr: int, B: int, H: int, Nq: int,
+                   Nk: int, D: int, scale: float, causal: int, dtype: int, stream: int = 0) -> int:
+    """The raw allocation-free C call on device pointers; returns the fa_status code."""
+    return lib().fa_fwd_noalloc(q_ptr, k_ptr, v_ptr, o_ptr, B, H, Nq, Nk, D, scale, causal, dtype,
+                                stream)
 
 
 def _dtype_code(t) -> int:
