@@ -134,6 +134,17 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, i
  */
 fa_status fa_last_device_error(void* stream, int* site);
 
+/*
+ * Lazy (conditional) rescaling threshold, process-wide, in log2 units of the scaled scores.
+ * A row keeps its reference maximum, and so skips rescaling its accumulator, while the new
+ * maximum exceeds the reference by at most this much (the conditional rescaling paragraph of
+ * ithelp article 10405336, "FlashAttention 保留三個狀態"). O / l is unchanged by the choice;
+ * the 16-bit weights P stay <= 2^threshold. 0 rescales on every rise of the maximum. Range
+ * [0, 15] (fp16 P must stay finite); default 8. Affects launches made after the call.
+ */
+fa_status fa_set_rescale_threshold(float log2_threshold);
+float fa_get_rescale_threshold(void);
+
 /* A static, human-readable name for a status code. */
 const char* fa_status_string(fa_status status);
 

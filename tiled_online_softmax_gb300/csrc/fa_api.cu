@@ -17,7 +17,6 @@
 namespace {
 
 constexpr int MAX_DEVICES = 64;
-constexpr int STAGES = 2;
 
 thread_local char g_msg[512] = "";
 
@@ -37,6 +36,7 @@ std::mutex g_mutex;
 int* g_err_word[MAX_DEVICES] = {};         // device error word per device (16 bytes)
 int g_arch_ok[MAX_DEVICES] = {};           // 0 unknown, 1 sm_103, -1 other
 unsigned g_attr_set[MAX_DEVICES] = {};     // bit per kernel instance: smem attribute applied
+float g_rescale_threshold = 8.0f;          // lazy-rescale threshold (log2 units)
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -85,8 +85,8 @@ fa_status validate(const void* Q, const void* K, const void* V, void* O, int64_t
     if (B > (1ll << 31) || H > (1ll << 31) || bh > (1ll << 31) - 1 || Nq > (1ll << 31) - 1 ||
         Nk > (1ll << 31) - 1)
         return fail(FA_ERR_UNSUPPORTED, "problem too large for one launch");
-    const int64_t q_tiles = (Nq + fa::BM - 1) / fa::BM;
-    if (q_tiles > ((1ll << 31) - 1) / bh) return fail(FA_ERR_UNSUPPORTED, "too many tiles");
+    const int64_t units = (Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS;
+    if (units > ((1ll << 31) - 1) / bh) return fail(FA_ERR_UNSUPPORTED, "too many tiles");
     const size_t q_bytes = size_t(bh) * size_t(Nq) * size_t(D) * 2;
     const size_t kv_bytes = size_t(bh) * size_t(Nk) * size_t(D) * 2;
     if (device_ptrs) {
@@ -152,8 +152,8 @@ fa_status device_state(int* dev_out, int** err_out) {
 template <int D, bool BF16, bool CAUSAL>
 fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const fa::Params& p, cudaStream_t stream) {
-    auto kernel = fa::fa_fwd_kernel<D, BF16, CAUSAL, STAGES>;
-    constexpr int smem = fa::Smem<D, STAGES>::ALLOC_BYTES;
+    auto kernel = fa::fa_fwd_kernel<D, BF16, CAUSAL>;
+    constexpr int smem = fa::Smem<D>::ALLOC_BYTES;
     {
         std::lock_guard<std::mutex> lock(g_mutex);
         if (!(g_attr_set[dev] & (1u << inst))) {
@@ -162,7 +162,7 @@ fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtens
             g_attr_set[dev] |= 1u << inst;
         }
     }
-    const unsigned grid = static_cast<unsigned>(p.num_q_tiles) * static_cast<unsigned>(p.bh);
+    const unsigned grid = static_cast<unsigned>(p.num_units) * static_cast<unsigned>(p.bh);
     kernel<<<grid, fa::NUM_THREADS, smem, stream>>>(mq, mk, mv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -187,8 +187,9 @@ fa_status launch(const void* Q, const void* K, const void* V, void* O, int64_t B
     p.bh = static_cast<int>(bh);
     p.nq = static_cast<int>(Nq);
     p.nk = static_cast<int>(Nk);
-    p.num_q_tiles = static_cast<int>((Nq + fa::BM - 1) / fa::BM);
+    p.num_units = static_cast<int>((Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.rescale_threshold = g_rescale_threshold;
     p.timeout_ns = wait_timeout_ns();
     const bool bf16 = dtype == FA_BF16;
     const int inst = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
@@ -276,8 +277,9 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, i
     p.bh = static_cast<int>(bh);
     p.nq = static_cast<int>(Nq);
     p.nk = static_cast<int>(Nk);
-    p.num_q_tiles = static_cast<int>((Nq + fa::BM - 1) / fa::BM);
+    p.num_units = static_cast<int>((Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.rescale_threshold = g_rescale_threshold;
     p.timeout_ns = wait_timeout_ns();
     const int inst = (D == 128 ? 4 : 0) + (dtype == FA_BF16 ? 2 : 0) + (causal ? 1 : 0);
     switch (inst) {
@@ -381,5 +383,15 @@ const char* fa_status_string(fa_status status) {
 }
 
 const char* fa_last_error_message(void) { return g_msg; }
+
+fa_status fa_set_rescale_threshold(float log2_threshold) {
+    if (!std::isfinite(log2_threshold) || log2_threshold < 0.f || log2_threshold > 15.f)
+        return fail(FA_ERR_INVALID_ARGUMENT, "rescale threshold must be in [0, 15], got %g",
+                    double(log2_threshold));
+    g_rescale_threshold = log2_threshold;
+    return FA_OK;
+}
+
+float fa_get_rescale_threshold(void) { return g_rescale_threshold; }
 
 }  // extern "C"

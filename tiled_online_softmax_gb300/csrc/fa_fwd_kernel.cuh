@@ -1,38 +1,45 @@
 // fa_fwd_kernel.cuh -- the sm_103a attention forward kernel (tiled online softmax).
 //
-// One CTA owns one tile of BM = 128 query rows of one (batch, head) slice and streams the
-// slice's keys past it in tiles of BN = 128 ("11. Fusion, recompute, and flash attention",
-// section 11.9: one thread block per block of query rows, the query block loaded once, key
-// blocks looped over). Per key tile j:
+// Work unit: 256 query rows of one (batch, head) slice, as two tiles of BM = 128 rows that share
+// every K/V tile the CTA loads; keys stream past in tiles of BN = 128 ("11. Fusion, recompute,
+// and flash attention", section 11.9: one thread block per block of query rows, the query block
+// loaded once, key blocks looped over). For query tile t and key tile j:
 //
-//   S_j = Q K_j^T                       tcgen05 MMA, fp32 accumulator in tensor memory (TMEM)
-//   m_new = max(m, rowmax S_j * c)      c = scale * log2(e); every exponential is then a bare
-//   corr  = 2^(m - m_new)               exp2 (same chapter, section 11.7: base 2 with log2 e
-//   P_j   = 2^(S_j * c - m_new)         folded into the scale)
-//   l     = l * corr + rowsum P_j
-//   O     = O * corr + P_j V_j          the rescale runs on O in TMEM, then a second MMA adds
-//                                       P_j V_j with P_j read from TMEM
+//   S_t = Q_t K_j^T                     tcgen05 MMA, fp32 accumulator in tensor memory (TMEM)
+//   m_new = max(m, rowmax S_t * c)      c = scale * log2(e): every exponential is a bare exp2
+//   corr  = 2^(m - m_new)               (same chapter, section 11.7, base 2 with log2 e folded
+//   P_t   = 2^(S_t * c - m_new)          into the scale)
+//   l     = l * corr + rowsum P_t
+//   O_t   = O_t * corr + P_t V_j        rescale of O_t in TMEM, then an MMA with P_t from TMEM
 //
-// and after the last tile O / l is written once ("Flash Attention 2", "Write the data back to
-// HBM": the division happens once at write-back). The recurrence is the one of section 11.6
-// "Online softmax" taken one key block at a time ("Flash Attention 2", "Overview of the
-// algorithm"; phobos "Attention", `online_softmax`).
+// and after the last key tile O_t / l is written once ("Flash Attention 2", "Write the data back
+// to HBM"). The recurrence is section 11.6 "Online softmax" one key block at a time ("Flash
+// Attention 2", "Overview of the algorithm"; phobos "Attention", `online_softmax`). The maximum
+// is updated lazily: while a row's new maximum exceeds its reference maximum by at most a
+// threshold (8 in log2 units), the reference is kept and nothing is rescaled (the conditional
+// rescaling of ithelp article 10405336, FlashAttention 保留三個狀態); l and O share the
+// reference, so O / l is unchanged and P stays <= 2^threshold.
 //
-// Warp roles (192 threads):
-//   warps 0-3  softmax: thread t owns query row t of the tile (TMEM lane t), so row max and
-//              row sum need no shuffles; it also rescales its O row and writes the output.
-//   warp 4     MMA issuer (one lane) and TMEM owner.
-//   warp 5     TMA producer (one lane): Q once, then K and V tiles through a ring of stages.
+// Warp roles (512 threads, registers rebalanced with setmaxnreg):
+//   warpgroup 0 (warps 0-3)  softmax of query tile 0: thread r owns row r (TMEM lane r), so row
+//                            max and sum need no shuffles.
+//   warpgroup 1 (warps 4-7)  softmax of query tile 1.
+//   warpgroup 2 (warps 8-11) correction: rescales O_0 / O_1 in TMEM when a row's reference max
+//                            moved, then divides by l and writes O.
+//   warp 12                  MMA issuer (one lane) and TMEM owner.
+//   warp 13                  TMA producer (one lane): Q_0 and Q_1 once, then K and V tiles
+//                            through rings of stages.
+//   warps 14-15              idle.
+// The MMA warp issues, per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). While the softmax
+// of one tile runs, the tensor cores work on the other tile's two products.
 //
 // Tensor memory (512 columns x 128 lanes of 32 bit):
-//   [0,128)    S buffer 0 (fp32); its first 64 columns take P (16-bit pairs) once S is read
-//   [128,256)  S buffer 1, same
-//   [256,256+D) O accumulator (fp32)
-// Two S buffers let the MMA warp compute S_{j+1} while the softmax warps work on S_j.
+//   [0,128) S_0 (fp32), its first 64 columns take P_0 (16-bit pairs) once S_0 is read
+//   [128,256) S_1 / P_1;  [256,256+D) O_0;  [384,384+D) O_1.
 //
 // Masking: a key j >= Nk (partial last tile, phobos "Attention", `attention`) or, under causal
-// masking, a key after the query (phobos "Causal attention") gets weight 0 and is left out of
-// the row maximum; key tiles entirely after the tile's last query are never loaded.
+// masking, a key after the query (phobos "Causal attention") is left out of the row max and gets
+// weight 0; key tiles entirely after a query tile's last row are never computed for that tile.
 //
 // Every wait is bounded: past the time limit the waiting thread records a site code in the
 // device error word, raises the CTA's abort flag, and every role winds down (waiting, bounded
@@ -49,14 +56,21 @@
 
 namespace fa {
 
-constexpr int BM = 128;               // query rows per tile = TMEM lanes
-constexpr int BN = 128;               // keys per tile
-constexpr int NUM_THREADS = 192;
-constexpr int SOFTMAX_THREADS = 128;  // warps 0-3
-constexpr int MMA_WARP = 4;
-constexpr int LOAD_WARP = 5;
+constexpr int BM = 128;              // query rows per tile = TMEM lanes
+constexpr int BN = 128;              // keys per tile
+constexpr int Q_TILES = 2;           // query tiles per CTA (one work unit = 256 rows)
+constexpr int UNIT_ROWS = BM * Q_TILES;
+constexpr int NUM_THREADS = 512;
+constexpr int MMA_WARP = 12;
+constexpr int LOAD_WARP = 13;
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t TMEM_S0 = 0, TMEM_S1 = 128, TMEM_O = 256;
+__host__ __device__ constexpr uint32_t tmem_s(int t) { return t ? 128u : 0u; }
+__host__ __device__ constexpr uint32_t tmem_o(int t) { return t ? 384u : 256u; }
+
+// Registers per thread after rebalancing; the launch gives 512 x 128.
+constexpr uint32_t REG_SOFTMAX = 184, REG_CORRECTION = 80, REG_MISC = 64;
+static_assert(8 * 32 * REG_SOFTMAX + 4 * 32 * REG_CORRECTION + 4 * 32 * REG_MISC <= 512 * 128,
+              "setmaxnreg split exceeds the launch's register file");
 
 // Wait-site codes written to the device error word (first timeout wins).
 enum WaitSite : int {
@@ -67,8 +81,9 @@ enum WaitSite : int {
     SITE_MMA_P_FULL = 5,
     SITE_MMA_V_FULL = 6,
     SITE_SOFTMAX_S_FULL = 7,
-    SITE_SOFTMAX_O_READY = 8,
-    SITE_DRAIN = 9,
+    SITE_CORR_SCALE = 8,
+    SITE_CORR_O_READY = 9,
+    SITE_DRAIN = 10,
 };
 
 struct Params {
@@ -76,37 +91,43 @@ struct Params {
     int* err;                  // device error word (site code of the first timeout)
     int bh;                    // B * H
     int nq, nk;
-    int num_q_tiles;
+    int num_units;             // ceil(nq / 256)
     float scale_log2;          // scale * log2(e)
+    float rescale_threshold;   // lazy-rescale threshold, log2 units (0 = rescale on every rise)
     unsigned long long timeout_ns;
 };
 
-template <int D, int STAGES>
+template <int D>
 struct Smem {
+    static constexpr int STAGES = (D == 64) ? 4 : 2;
     static constexpr int COL_BLOCKS = D / 64;            // 128-byte (64-element) column blocks
-    static constexpr int Q_BYTES = BM * D * 2;
+    static constexpr int Q_TILE_BYTES = BM * D * 2;
     static constexpr int KV_BYTES = BN * D * 2;          // one K or V tile
     static constexpr int Q_OFF = 0;
-    static constexpr int K_OFF = Q_OFF + Q_BYTES;
+    static constexpr int K_OFF = Q_OFF + Q_TILES * Q_TILE_BYTES;
     static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
-    static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
+    static constexpr int ROW_OFF = V_OFF + STAGES * KV_BYTES;   // float [3][2][128]
+    static constexpr int BAR_OFF = ROW_OFF + 3 * Q_TILES * BM * 4;
     // barrier indices
-    static constexpr int B_Q_FULL = 0;
-    static constexpr int B_K_FULL = 1;
+    static constexpr int B_Q_FULL = 0;                          // [2]
+    static constexpr int B_K_FULL = B_Q_FULL + Q_TILES;         // [STAGES]
     static constexpr int B_K_EMPTY = B_K_FULL + STAGES;
     static constexpr int B_V_FULL = B_K_EMPTY + STAGES;
     static constexpr int B_V_EMPTY = B_V_FULL + STAGES;
-    static constexpr int B_S_FULL = B_V_EMPTY + STAGES;  // 2
-    static constexpr int B_P_FULL = B_S_FULL + 2;        // 2
-    static constexpr int B_O_READY = B_P_FULL + 2;
-    static constexpr int B_DRAIN = B_O_READY + 1;
+    static constexpr int B_S_FULL = B_V_EMPTY + STAGES;         // [2] MMA -> softmax
+    static constexpr int B_SCALE = B_S_FULL + Q_TILES;          // [2] softmax -> correction
+    static constexpr int B_P_FULL = B_SCALE + Q_TILES;          // [2] softmax+correction -> MMA
+    static constexpr int B_O_READY = B_P_FULL + Q_TILES;        // [2] MMA -> correction
+    static constexpr int B_DRAIN = B_O_READY + Q_TILES;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
     static constexpr int BYTES = ABORT_OFF + 4;
-    // +1024 slack for 1024-byte alignment; at least 116 KB so that two CTAs never share an SM
-    // (each holds all 512 TMEM columns; a second one would stall in tcgen05.alloc).
-    static constexpr int ALLOC_BYTES = (BYTES + 1024 > 116 * 1024) ? BYTES + 1024 : 116 * 1024;
+    static constexpr int ALLOC_BYTES = BYTES + 1024;            // slack for 1024-byte alignment
+    static_assert(ALLOC_BYTES <= 232448, "shared memory budget");
+    // More than half an SM's shared memory, so two CTAs never share an SM: each holds all 512
+    // TMEM columns, and a second one would stall in tcgen05.alloc.
+    static_assert(ALLOC_BYTES > 116 * 1024, "one CTA per SM");
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -155,23 +176,215 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
-template <bool BF16>
-__device__ __forceinline__ float2 unpack2(uint32_t u) {
-    if constexpr (BF16) {
-        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
-    } else {
-        return __half22float2(*reinterpret_cast<const __half2*>(&u));
+// ---------------------------------------------------------------------------------------------
+// softmax of one query tile (warpgroup t)
+// ---------------------------------------------------------------------------------------------
+template <int D, bool BF16, bool CAUSAL>
+__device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbase, float* rows,
+                                             const Params& p, const Ctl& ctl, int q_tile0,
+                                             int n_tiles) {
+    using L = Smem<D>;
+    auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
+    const int r = threadIdx.x & 127;          // row within the tile = TMEM lane
+    const int warp = threadIdx.x >> 5;
+    const int row = q_tile0 + r;
+    const uint32_t s_cols = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + tmem_s(t);
+    const float c = p.scale_log2;
+    const bool neg = c < 0.f;
+    const float tau = p.rescale_threshold;
+    float* row_scale = rows + (0 * Q_TILES + t) * BM;
+    float* row_l = rows + (1 * Q_TILES + t) * BM;
+    float* row_m = rows + (2 * Q_TILES + t) * BM;
+    float m_ref = -INFINITY;  // reference max of the scaled scores (log2 units)
+    float l = 0.f;            // running denominator relative to m_ref
+
+    for (int j = 0; j < n_tiles; ++j) {
+        if (!wait_bar_warp(bar(L::B_S_FULL + t), j & 1, ctl, SITE_SOFTMAX_S_FULL)) return;
+        ptx::tc_fence_after();
+        uint32_t sr[4][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ptx::tmem_ld32(s_cols + q * 32, sr[q]);
+        ptx::tmem_wait_ld();
+#pragma unroll
+        for (int q = 0; q < 4; ++q) ptx::reg_fence(sr[q]);
+
+        // Keys of this tile the row may see: [k0, k0 + lim).
+        const int k0 = j * BN;
+        const bool need_mask = (k0 + BN > p.nk) || (CAUSAL && k0 + BN - 1 > q_tile0);
+        int lim = p.nk - k0;
+        if constexpr (CAUSAL) lim = min(lim, row + 1 - k0);
+        if (need_mask) {
+            const uint32_t hidden = neg ? 0x7f800000u : 0xff800000u;  // +inf / -inf
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int i = 0; i < 32; ++i)
+                    if (q * 32 + i >= lim) sr[q][i] = hidden;
+        }
+
+        // Tile maximum on the raw scores (scaling by c >= 0 is monotone; c < 0 uses the min).
+        float mx[4];
+        if (!neg) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float a = __uint_as_float(sr[q][0]);
+#pragma unroll
+                for (int i = 1; i < 31; i += 2)
+                    a = ptx::fmax3(a, __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]));
+                mx[q] = fmaxf(a, __uint_as_float(sr[q][31]));
+            }
+        } else {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                float a = __uint_as_float(sr[q][0]);
+#pragma unroll
+                for (int i = 1; i < 31; i += 2)
+                    a = ptx::fmin3(a, __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]));
+                mx[q] = fminf(a, __uint_as_float(sr[q][31]));
+            }
+        }
+        const float mraw = neg ? fminf(fminf(mx[0], mx[1]), fminf(mx[2], mx[3]))
+                               : fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        const float m_tile = (mraw == INFINITY || mraw == -INFINITY) ? -INFINITY : mraw * c;
+
+        // Lazy reference update: move m_ref only when the row max rose by more than tau.
+        float corr = 1.f;
+        if (m_tile > m_ref + tau || m_ref == -INFINITY) {
+            const float m_new = fmaxf(m_ref, m_tile);
+            corr = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - m_new);
+            m_ref = m_new;
+        }
+        row_scale[r] = corr;
+        ptx::mbar_arrive(bar(L::B_SCALE + t));
+        const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
+
+        // P = 2^(s*c - m_ref), rounded to 16 bits; l sums the rounded values, so O / l is an
+        // exact weighted average of V under the weights the PV product uses.
+        float acc[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+        uint32_t pk[2][32];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+#pragma unroll
+            for (int i = 0; i < 32; i += 2) {
+                float x0, x1;
+                ptx::ffma2(x0, x1, __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]), c,
+                           neg_m);
+                float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                if (need_mask) {
+                    if (q * 32 + i >= lim) p0 = 0.f;
+                    if (q * 32 + i + 1 >= lim) p1 = 0.f;
+                }
+                const uint32_t u = pack2<BF16>(p0, p1);
+                ptx::add_halves<BF16>(acc[(i >> 1) & 3], acc[4 + ((i >> 1) & 3)], u);
+                pk[q >> 1][(q & 1) * 16 + i / 2] = u;
+            }
+        }
+        const float rowsum =
+            ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
+        l = l * corr + rowsum;
+        ptx::tmem_st32(s_cols + 0, pk[0]);
+        ptx::tmem_st32(s_cols + 32, pk[1]);
+        ptx::tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(bar(L::B_P_FULL + t));
+    }
+    row_l[r] = l;
+    row_m[r] = m_ref;
+    ptx::mbar_arrive(bar(L::B_SCALE + t));
+}
+
+// ---------------------------------------------------------------------------------------------
+// correction and epilogue (warpgroup 2)
+// ---------------------------------------------------------------------------------------------
+template <int D, bool BF16>
+__device__ __forceinline__ void correction_role(uint32_t tmem, uint32_t sbase, const float* rows,
+                                                const Params& p, const Ctl& ctl, int bh, int q0,
+                                                const int (&n_tiles)[Q_TILES]) {
+    using L = Smem<D>;
+    auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
+    const int r = threadIdx.x & 127;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const int n_max = n_tiles[Q_TILES - 1];
+
+    for (int j = 0; j < n_max; ++j) {
+#pragma unroll
+        for (int t = 0; t < Q_TILES; ++t) {
+            if (j >= n_tiles[t]) continue;
+            if (!wait_bar_warp(bar(L::B_SCALE + t), j & 1, ctl, SITE_CORR_SCALE)) return;
+            if (j > 0) {
+                const float corr = rows[(0 * Q_TILES + t) * BM + r];
+                // O_t holds sum_{i<j} P_i V_i relative to the old reference once PV(j-1) is done.
+                if (!wait_bar_warp(bar(L::B_O_READY + t), (j - 1) & 1, ctl, SITE_CORR_O_READY))
+                    return;
+                ptx::tc_fence_after();
+                if (__any_sync(0xffffffffu, corr != 1.f)) {
+                    const uint32_t o_cols = tmem + lane_base + tmem_o(t);
+#pragma unroll
+                    for (int q = 0; q < D / 32; ++q) {
+                        uint32_t o[32];
+                        ptx::tmem_ld32(o_cols + q * 32, o);
+                        ptx::tmem_wait_ld();
+                        ptx::reg_fence(o);
+#pragma unroll
+                        for (int i = 0; i < 32; ++i)
+                            o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                        ptx::tmem_st32(o_cols + q * 32, o);
+                    }
+                    ptx::tmem_wait_st();
+                }
+            }
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(L::B_P_FULL + t));
+        }
+    }
+
+    // Epilogue: O_t / l, rounded to the 16-bit type, one row per thread.
+#pragma unroll
+    for (int t = 0; t < Q_TILES; ++t) {
+        const int n = n_tiles[t];
+        if (!wait_bar_warp(bar(L::B_SCALE + t), n & 1, ctl, SITE_CORR_SCALE)) return;
+        const float l = rows[(1 * Q_TILES + t) * BM + r];
+        if (!wait_bar_warp(bar(L::B_O_READY + t), (n - 1) & 1, ctl, SITE_CORR_O_READY)) return;
+        ptx::tc_fence_after();
+        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+        const int row = q0 + t * BM + r;
+        const uint32_t o_cols = tmem + lane_base + tmem_o(t);
+        uint8_t* out_row =
+            static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.nq + row) * (D * 2);
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            ptx::tmem_ld32(o_cols + q * 32, o);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(o);
+            uint32_t packed[16];
+#pragma unroll
+            for (int i = 0; i < 16; ++i)
+                packed[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
+                                        __uint_as_float(o[2 * i + 1]) * inv_l);
+            if (row < p.nq) {
+                uint4* dst = reinterpret_cast<uint4*>(out_row + q * 64);
+#pragma unroll
+                for (int v = 0; v < 4; ++v)
+                    dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                        packed[4 * v + 3]);
+            }
+        }
     }
 }
 
 // ---------------------------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------------------------
-template <int D, bool BF16, bool CAUSAL, int STAGES>
+template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                   const __grid_constant__ CUtensorMap tm_v, const Params p) {
-    using L = Smem<D, STAGES>;
+    using L = Smem<D>;
+    constexpr int STAGES = L::STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw_addr = ptx::smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw_addr + 1023u) & ~1023u) - raw_addr);
@@ -179,38 +392,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::ABORT_OFF);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
+    float* rows = reinterpret_cast<float*>(smem + L::ROW_OFF);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int wg = warp >> 2;
 
-    // Tile schedule. Causal: the longest rows first, spread over all slices; otherwise the tiles
-    // of one slice are adjacent so its K/V stay hot in L2.
-    int bh, qt;
+    // Work unit. Causal: the longest units first, spread over all slices; otherwise the units of
+    // one slice are adjacent so its K/V stay hot in L2.
+    int bh, u;
     if constexpr (CAUSAL) {
         bh = blockIdx.x % p.bh;
-        qt = p.num_q_tiles - 1 - static_cast<int>(blockIdx.x / p.bh);
+        u = p.num_units - 1 - static_cast<int>(blockIdx.x / p.bh);
     } else {
-        qt = blockIdx.x % p.num_q_tiles;
-        bh = blockIdx.x / p.num_q_tiles;
+        u = blockIdx.x % p.num_units;
+        bh = blockIdx.x / p.num_units;
     }
-    const int q0 = qt * BM;
-    int n_tiles = (p.nk + BN - 1) / BN;
-    if constexpr (CAUSAL) n_tiles = min(n_tiles, (q0 + BM - 1) / BN + 1);
+    const int q0 = u * UNIT_ROWS;
+    const int nkt = (p.nk + BN - 1) / BN;
+    int n_tiles[Q_TILES];
+#pragma unroll
+    for (int t = 0; t < Q_TILES; ++t)
+        n_tiles[t] = CAUSAL ? min(nkt, (q0 + t * BM + BM - 1) / BN + 1) : nkt;
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
-        ptx::mbar_init(bar(L::B_Q_FULL), 1);
+        for (int t = 0; t < Q_TILES; ++t) {
+            ptx::mbar_init(bar(L::B_Q_FULL + t), 1);
+            ptx::mbar_init(bar(L::B_S_FULL + t), 1);
+            ptx::mbar_init(bar(L::B_SCALE + t), BM);
+            ptx::mbar_init(bar(L::B_P_FULL + t), 2 * BM);  // softmax rows + correction rows
+            ptx::mbar_init(bar(L::B_O_READY + t), 1);
+        }
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar(L::B_K_FULL + s), 1);
             ptx::mbar_init(bar(L::B_K_EMPTY + s), 1);
             ptx::mbar_init(bar(L::B_V_FULL + s), 1);
             ptx::mbar_init(bar(L::B_V_EMPTY + s), 1);
         }
-        for (int b = 0; b < 2; ++b) {
-            ptx::mbar_init(bar(L::B_S_FULL + b), 1);
-            ptx::mbar_init(bar(L::B_P_FULL + b), SOFTMAX_THREADS);
-        }
-        ptx::mbar_init(bar(L::B_O_READY), 1);
         ptx::mbar_init(bar(L::B_DRAIN), 1);
         ptx::fence_barrier_init();
         ptx::fence_proxy_async_smem();
@@ -230,257 +449,147 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const Ctl ctl{abort_flag, p.err, p.timeout_ns};
 
-    if (warp == LOAD_WARP) {
-        // ------------------------------------------------------------------ TMA producer
-        if (lane == 0) {
-            const uint32_t sq = sbase + L::Q_OFF, sk = sbase + L::K_OFF, sv = sbase + L::V_OFF;
-            ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL), L::Q_BYTES);
-            for (int c = 0; c < L::COL_BLOCKS; ++c)
-                ptx::tma_load_3d(sq + c * (BM * 128), &tm_q, c * 64, q0, bh, bar(L::B_Q_FULL));
-            int issued = 0;
-            for (int j = 0; j < n_tiles; ++j) {
-                const int st = j % STAGES;
-                const uint32_t ph = (j / STAGES) & 1;
-                if (!wait_bar(bar(L::B_K_EMPTY + st), ph ^ 1, ctl, SITE_LOAD_K_EMPTY)) break;
-                ptx::mbar_arrive_expect_tx(bar(L::B_K_FULL + st), L::KV_BYTES);
-                for (int c = 0; c < L::COL_BLOCKS; ++c)
-                    ptx::tma_load_3d(sk + st * L::KV_BYTES + c * (BN * 128), &tm_k, c * 64,
-                                     j * BN, bh, bar(L::B_K_FULL + st));
-                if (!wait_bar(bar(L::B_V_EMPTY + st), ph ^ 1, ctl, SITE_LOAD_V_EMPTY)) {
-                    issued = 2 * j + 1;
-                    break;
+    if (wg == 3) {
+        ptx::regs_dec<REG_MISC>();
+        if (warp == LOAD_WARP) {
+            // -------------------------------------------------------------- TMA producer
+            if (lane == 0) {
+                const uint32_t sq = sbase + L::Q_OFF, sk = sbase + L::K_OFF, sv = sbase + L::V_OFF;
+                for (int t = 0; t < Q_TILES; ++t) {
+                    ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL + t), L::Q_TILE_BYTES);
+                    for (int c = 0; c < L::COL_BLOCKS; ++c)
+                        ptx::tma_load_3d(sq + t * L::Q_TILE_BYTES + c * (BM * 128), &tm_q, c * 64,
+                                         q0 + t * BM, bh, bar(L::B_Q_FULL + t));
                 }
-                ptx::mbar_arrive_expect_tx(bar(L::B_V_FULL + st), L::KV_BYTES);
-                for (int c = 0; c < L::COL_BLOCKS; ++c)
-                    ptx::tma_load_3d(sv + st * L::KV_BYTES + c * (BN * 128), &tm_v, c * 64,
-                                     j * BN, bh, bar(L::B_V_FULL + st));
-                issued = 2 * j + 2;
-            }
-            if (*abort_flag) {
-                // Drain: every copy this thread started must land before the CTA's shared
-                // memory can be released. The last copy into each stage is the newest phase.
-                wait_bar(bar(L::B_Q_FULL), 0, ctl, SITE_DRAIN, false);
-                for (int t = (issued > 2 * STAGES ? issued - 2 * STAGES : 0); t < issued; ++t) {
-                    const int j = t / 2, st = j % STAGES;
+                const int n = n_tiles[Q_TILES - 1];
+                int issued = 0;
+                for (int j = 0; j < n; ++j) {
+                    const int st = j % STAGES;
                     const uint32_t ph = (j / STAGES) & 1;
-                    const int b = (t & 1) ? L::B_V_FULL + st : L::B_K_FULL + st;
-                    wait_bar(bar(b), ph, ctl, SITE_DRAIN, false);
+                    if (!wait_bar(bar(L::B_K_EMPTY + st), ph ^ 1, ctl, SITE_LOAD_K_EMPTY)) break;
+                    ptx::mbar_arrive_expect_tx(bar(L::B_K_FULL + st), L::KV_BYTES);
+                    for (int c = 0; c < L::COL_BLOCKS; ++c)
+                        ptx::tma_load_3d(sk + st * L::KV_BYTES + c * (BN * 128), &tm_k, c * 64,
+                                         j * BN, bh, bar(L::B_K_FULL + st));
+                    issued = 2 * j + 1;
+                    if (!wait_bar(bar(L::B_V_EMPTY + st), ph ^ 1, ctl, SITE_LOAD_V_EMPTY)) break;
+                    ptx::mbar_arrive_expect_tx(bar(L::B_V_FULL + st), L::KV_BYTES);
+                    for (int c = 0; c < L::COL_BLOCKS; ++c)
+                        ptx::tma_load_3d(sv + st * L::KV_BYTES + c * (BN * 128), &tm_v, c * 64,
+                                         j * BN, bh, bar(L::B_V_FULL + st));
+                    issued = 2 * j + 2;
+                }
+                if (*abort_flag) {
+                    // Drain: every copy this thread started must land before the CTA's shared
+                    // memory is released. The last copy into each stage is its newest phase.
+                    for (int t = 0; t < Q_TILES; ++t)
+                        wait_bar(bar(L::B_Q_FULL + t), 0, ctl, SITE_DRAIN, false);
+                    for (int x = (issued > 2 * STAGES ? issued - 2 * STAGES : 0); x < issued; ++x) {
+                        const int j = x / 2, st = j % STAGES;
+                        const uint32_t ph = (j / STAGES) & 1;
+                        wait_bar(bar((x & 1) ? L::B_V_FULL + st : L::B_K_FULL + st), ph, ctl,
+                                 SITE_DRAIN, false);
+                    }
                 }
             }
-        }
-        __syncwarp();
-    } else if (warp == MMA_WARP) {
-        // ------------------------------------------------------------------ MMA issuer
-        if (lane == 0) {
-            constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);
-            constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, D, false, true);
-            const uint32_t sq = sbase + L::Q_OFF, sk = sbase + L::K_OFF, sv = sbase + L::V_OFF;
-            bool ok = wait_bar(bar(L::B_Q_FULL), 0, ctl, SITE_MMA_Q_FULL);
-
-            // S_j = Q K_j^T: K = D in steps of 16 elements (32 bytes inside a 128-byte swizzle
-            // row); Q and K tiles are K-major, 8-row swizzle atoms 1024 bytes apart.
-            auto issue_s = [&](int j) {
-                const int st = j % STAGES;
-                const uint32_t d_tmem = tmem + ((j & 1) ? TMEM_S1 : TMEM_S0);
+            __syncwarp();
+        } else if (warp == MMA_WARP) {
+            // -------------------------------------------------------------- MMA issuer
+            if (lane == 0) {
+                constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);
+                constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, D, false, true);
+                const uint32_t sq = sbase + L::Q_OFF, sk = sbase + L::K_OFF, sv = sbase + L::V_OFF;
+                // S_t = Q_t K_j^T: K-dimension D in steps of 16 elements (32 bytes inside a
+                // 128-byte swizzle row); Q and K tiles are K-major, 8-row swizzle atoms 1024
+                // bytes apart, the second 64 columns of D one column block further.
+                auto issue_s = [&](int t, int j) {
+                    const int st = j % STAGES;
 #pragma unroll
-                for (int kk = 0; kk < D / 16; ++kk) {
-                    const uint32_t off = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                    const uint64_t a = ptx::sdesc_sw128(sq + off, 16, 1024);
-                    const uint64_t b = ptx::sdesc_sw128(
-                        sk + st * L::KV_BYTES + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
-                    ptx::mma_ss(d_tmem, a, b, IDESC_S, kk > 0 ? 1u : 0u);
-                }
-            };
-            // O += P_j V_j: K = BN keys in steps of 16; P_j is A, read from TMEM (16 keys = 8
-            // columns of 16-bit pairs); V_j is B in MN-major (D contiguous) layout: 16 keys =
-            // 16 rows of 128 bytes, the next 64 columns of D one column block (BN rows) away.
-            auto issue_pv = [&](int j) {
-                const int st = j % STAGES;
-                const uint32_t p_tmem = tmem + ((j & 1) ? TMEM_S1 : TMEM_S0);
+                    for (int kk = 0; kk < D / 16; ++kk) {
+                        const uint32_t off = (kk / 4) * (BM * 128) + (kk % 4) * 32;
+                        const uint64_t a = ptx::sdesc_sw128(sq + t * L::Q_TILE_BYTES + off, 16, 1024);
+                        const uint64_t b = ptx::sdesc_sw128(
+                            sk + st * L::KV_BYTES + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
+                        ptx::mma_ss(tmem + tmem_s(t), a, b, IDESC_S, kk > 0 ? 1u : 0u);
+                    }
+                };
+                // O_t += P_t V_j: K-dimension BN keys in steps of 16; P_t is the A operand from
+                // TMEM (16 keys = 8 columns of 16-bit pairs); V_j is B in MN-major layout (D
+                // contiguous): 16 keys = 16 rows of 128 bytes, the next 64 columns of D one
+                // column block (BN rows) away.
+                auto issue_pv = [&](int t, int j) {
+                    const int st = j % STAGES;
 #pragma unroll
-                for (int kk = 0; kk < BN / 16; ++kk) {
-                    const uint64_t b = ptx::sdesc_sw128(sv + st * L::KV_BYTES + kk * (16 * 128),
-                                                        BN * 128, 1024);
-                    ptx::mma_ts(tmem + TMEM_O, p_tmem + kk * 8, b, IDESC_O,
-                                (j > 0 || kk > 0) ? 1u : 0u);
-                }
-            };
-
-            if (ok) ok = wait_bar(bar(L::B_K_FULL + 0), 0, ctl, SITE_MMA_K_FULL);
-            if (ok) {
-                ptx::tc_fence_after();
-                issue_s(0);
-                ptx::mma_commit(bar(L::B_S_FULL + 0));
-                ptx::mma_commit(bar(L::B_K_EMPTY + 0));
-            }
-            for (int j = 0; ok && j < n_tiles; ++j) {
-                if (j + 1 < n_tiles) {
-                    const int st1 = (j + 1) % STAGES;
-                    ok = wait_bar(bar(L::B_K_FULL + st1), ((j + 1) / STAGES) & 1, ctl,
-                                  SITE_MMA_K_FULL);
-                    if (!ok) break;
+                    for (int kk = 0; kk < BN / 16; ++kk) {
+                        const uint64_t b = ptx::sdesc_sw128(sv + st * L::KV_BYTES + kk * (16 * 128),
+                                                            BN * 128, 1024);
+                        ptx::mma_ts(tmem + tmem_o(t), tmem + tmem_s(t) + kk * 8, b, IDESC_O,
+                                    (j > 0 || kk > 0) ? 1u : 0u);
+                    }
+                };
+                const int n0 = n_tiles[0], n1 = n_tiles[Q_TILES - 1];
+                bool ok = wait_bar(bar(L::B_Q_FULL + 0), 0, ctl, SITE_MMA_Q_FULL) &&
+                          wait_bar(bar(L::B_K_FULL + 0), 0, ctl, SITE_MMA_K_FULL);
+                if (ok) {
                     ptx::tc_fence_after();
-                    issue_s(j + 1);
-                    ptx::mma_commit(bar(L::B_S_FULL + ((j + 1) & 1)));
-                    ptx::mma_commit(bar(L::B_K_EMPTY + st1));
+                    issue_s(0, 0);
+                    ptx::mma_commit(bar(L::B_S_FULL + 0));
+                    ok = wait_bar(bar(L::B_Q_FULL + 1), 0, ctl, SITE_MMA_Q_FULL);
                 }
-                ok = wait_bar(bar(L::B_P_FULL + (j & 1)), (j >> 1) & 1, ctl, SITE_MMA_P_FULL);
-                if (!ok) break;
-                const int st = j % STAGES;
-                ok = wait_bar(bar(L::B_V_FULL + st), (j / STAGES) & 1, ctl, SITE_MMA_V_FULL);
-                if (!ok) break;
-                ptx::tc_fence_after();
-                issue_pv(j);
-                ptx::mma_commit(bar(L::B_O_READY));
-                ptx::mma_commit(bar(L::B_V_EMPTY + st));
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_s(1, 0);
+                    ptx::mma_commit(bar(L::B_S_FULL + 1));
+                    ptx::mma_commit(bar(L::B_K_EMPTY + 0));
+                }
+                for (int j = 0; ok && j < n1; ++j) {
+                    const int st = j % STAGES;
+                    const int st1 = (j + 1) % STAGES;
+                    const uint32_t ph1 = ((j + 1) / STAGES) & 1;
+                    if (!(ok = wait_bar(bar(L::B_V_FULL + st), (j / STAGES) & 1, ctl, SITE_MMA_V_FULL)))
+                        break;
+                    if (j < n0) {
+                        if (!(ok = wait_bar(bar(L::B_P_FULL + 0), j & 1, ctl, SITE_MMA_P_FULL))) break;
+                        ptx::tc_fence_after();
+                        issue_pv(0, j);
+                        ptx::mma_commit(bar(L::B_O_READY + 0));
+                        if (j + 1 < n0) {
+                            if (!(ok = wait_bar(bar(L::B_K_FULL + st1), ph1, ctl, SITE_MMA_K_FULL)))
+                                break;
+                            ptx::tc_fence_after();
+                            issue_s(0, j + 1);
+                            ptx::mma_commit(bar(L::B_S_FULL + 0));
+                        }
+                    }
+                    if (!(ok = wait_bar(bar(L::B_P_FULL + 1), j & 1, ctl, SITE_MMA_P_FULL))) break;
+                    ptx::tc_fence_after();
+                    issue_pv(1, j);
+                    ptx::mma_commit(bar(L::B_O_READY + 1));
+                    ptx::mma_commit(bar(L::B_V_EMPTY + st));
+                    if (j + 1 < n1) {
+                        if (!(ok = wait_bar(bar(L::B_K_FULL + st1), ph1, ctl, SITE_MMA_K_FULL)))
+                            break;
+                        ptx::tc_fence_after();
+                        issue_s(1, j + 1);
+                        ptx::mma_commit(bar(L::B_S_FULL + 1));
+                        ptx::mma_commit(bar(L::B_K_EMPTY + st1));
+                    }
+                }
+                if (*abort_flag) {
+                    // Drain: wait until every MMA this thread issued has finished.
+                    ptx::mma_commit(bar(L::B_DRAIN));
+                    wait_bar(bar(L::B_DRAIN), 0, ctl, SITE_DRAIN, false);
+                }
             }
-            if (*abort_flag) {
-                // Drain: wait until every MMA this thread issued has finished with TMEM/smem.
-                ptx::mma_commit(bar(L::B_DRAIN));
-                wait_bar(bar(L::B_DRAIN), 0, ctl, SITE_DRAIN, false);
-            }
+            __syncwarp();
         }
-        __syncwarp();
+    } else if (wg == 2) {
+        ptx::regs_dec<REG_CORRECTION>();
+        correction_role<D, BF16>(tmem, sbase, rows, p, ctl, bh, q0, n_tiles);
+        ptx::tmem_wait_st();
     } else {
-        // ------------------------------------------------------------------ softmax warps
-        const int t = threadIdx.x;  // row within the tile = TMEM lane
-        const int row = q0 + t;
-        const uint32_t lane_base = static_cast<uint32_t>(warp * 32) << 16;
-        const float c = p.scale_log2;
-        float m = -INFINITY;  // running max of the scaled scores (log2 units)
-        float l = 0.f;        // running denominator
-        bool ok = true;
-
-        for (int j = 0; j < n_tiles; ++j) {
-            const int b = j & 1;
-            const uint32_t s_cols = tmem + lane_base + (b ? TMEM_S1 : TMEM_S0);
-            ok = wait_bar_warp(bar(L::B_S_FULL + b), (j >> 1) & 1, ctl, SITE_SOFTMAX_S_FULL);
-            if (!ok) break;
-            ptx::tc_fence_after();
-
-            uint32_t sr[4][32];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ptx::tmem_ld32(s_cols + q * 32, sr[q]);
-            ptx::tmem_wait_ld();
-#pragma unroll
-            for (int q = 0; q < 4; ++q) ptx::reg_fence(sr[q]);
-
-            const int k0 = j * BN;
-            // Keys of this tile that the row may see: [k0, k_end).
-            int k_end = min(k0 + BN, p.nk);
-            if constexpr (CAUSAL) k_end = min(k_end, row + 1);
-            const int n_vis = k_end - k0;  // may be <= 0 only for padding rows past Nq
-            const bool full_tile = (n_vis >= BN);
-
-            // Tile maximum of the scaled scores over visible keys. Scaling by c >= 0 is monotone
-            // in floating point, so the maximum is taken on the raw scores and scaled once
-            // (for c < 0 the minimum plays that role).
-            const bool neg = c < 0.f;
-            float mx[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) mx[i] = -INFINITY;
-#pragma unroll
-            for (int q = 0; q < 4; ++q)
-#pragma unroll
-                for (int i = 0; i < 32; ++i) {
-                    const float sv = neg ? -__uint_as_float(sr[q][i]) : __uint_as_float(sr[q][i]);
-                    if (full_tile || q * 32 + i < n_vis) mx[i & 7] = fmaxf(mx[i & 7], sv);
-                }
-            float m_tile = fmaxf(fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3])),
-                                 fmaxf(fmaxf(mx[4], mx[5]), fmaxf(mx[6], mx[7])));
-            m_tile = (m_tile == -INFINITY) ? -INFINITY : (neg ? -m_tile : m_tile) * c;
-            const float m_new = fmaxf(m, m_tile);
-            // An empty state (m = -inf) has nothing to rescale; an all-hidden row keeps m = -inf
-            // and is given weight 0 below.
-            const float corr = (m == -INFINITY) ? 0.f : ptx::ex2(m - m_new);
-            const float m_use = (m_new == -INFINITY) ? 0.f : m_new;
-
-            float sum[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) sum[i] = 0.f;
-            uint32_t pk[2][32];
-#pragma unroll
-            for (int q = 0; q < 4; ++q) {
-#pragma unroll
-                for (int i = 0; i < 32; i += 2) {
-                    float p0 = ptx::ex2(fmaf(__uint_as_float(sr[q][i]), c, -m_use));
-                    float p1 = ptx::ex2(fmaf(__uint_as_float(sr[q][i + 1]), c, -m_use));
-                    if (!full_tile) {
-                        if (q * 32 + i >= n_vis) p0 = 0.f;
-                        if (q * 32 + i + 1 >= n_vis) p1 = 0.f;
-                    }
-                    // l sums the same 16-bit-rounded weights the PV product uses, so the
-                    // final O / l is an exact weighted average of V under those weights.
-                    const uint32_t u = pack2<BF16>(p0, p1);
-                    const float2 r = unpack2<BF16>(u);
-                    sum[i & 7] += r.x;
-                    sum[(i + 1) & 7] += r.y;
-                    pk[q >> 1][(q & 1) * 16 + i / 2] = u;
-                }
-            }
-            const float rowsum = ((sum[0] + sum[1]) + (sum[2] + sum[3])) +
-                                 ((sum[4] + sum[5]) + (sum[6] + sum[7]));
-            l = l * corr + rowsum;
-            // P_j over the first 64 columns of this S buffer (all of S_j is already in registers).
-            ptx::tmem_st32(s_cols + 0, pk[0]);
-            ptx::tmem_st32(s_cols + 32, pk[1]);
-
-            if (j > 0) {
-                // O holds sum_{i<j} P_i V_i relative to the old max once PV_{j-1} is done.
-                ok = wait_bar_warp(bar(L::B_O_READY), (j - 1) & 1, ctl, SITE_SOFTMAX_O_READY);
-                if (!ok) break;
-                ptx::tc_fence_after();
-                if (__any_sync(0xffffffffu, corr != 1.f)) {
-                    const uint32_t o_cols = tmem + lane_base + TMEM_O;
-#pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
-                        uint32_t orr[32];
-                        ptx::tmem_ld32(o_cols + q * 32, orr);
-                        ptx::tmem_wait_ld();
-                        ptx::reg_fence(orr);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            orr[i] = __float_as_uint(__uint_as_float(orr[i]) * corr);
-                        ptx::tmem_st32(o_cols + q * 32, orr);
-                    }
-                }
-            }
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(L::B_P_FULL + b));
-            m = m_new;
-        }
-
-        // ---------------------------------------------------------------- epilogue: O / l
-        if (ok && n_tiles > 0) {
-            ok = wait_bar_warp(bar(L::B_O_READY), (n_tiles - 1) & 1, ctl, SITE_SOFTMAX_O_READY);
-        }
-        if (ok && n_tiles > 0) {
-            ptx::tc_fence_after();
-            const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-            const uint32_t o_cols = tmem + lane_base + TMEM_O;
-            uint8_t* out_row = static_cast<uint8_t*>(p.o) +
-                               (static_cast<size_t>(bh) * p.nq + row) * (D * 2);
-#pragma unroll
-            for (int q = 0; q < D / 32; ++q) {
-                uint32_t orr[32];
-                ptx::tmem_ld32(o_cols + q * 32, orr);
-                ptx::tmem_wait_ld();
-                ptx::reg_fence(orr);
-                uint32_t packed[16];
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    packed[i] = pack2<BF16>(__uint_as_float(orr[2 * i]) * inv_l,
-                                            __uint_as_float(orr[2 * i + 1]) * inv_l);
-                if (row < p.nq) {
-                    uint4* dst = reinterpret_cast<uint4*>(out_row + q * 64);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                            packed[4 * v + 3]);
-                }
-            }
-        }
+        ptx::regs_inc<REG_SOFTMAX>();
+        softmax_role<D, BF16, CAUSAL>(wg, tmem, sbase, rows, p, ctl, q0 + wg * BM, n_tiles[wg]);
         ptx::tmem_wait_st();  // no TMEM store of this warp may be pending at dealloc
     }
 

@@ -13,7 +13,8 @@ FA_F16, FA_BF16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED",
           3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_error",
-           "fa_status_string", "fa_last_error_message", "fa_fwd_noalloc")
+           "fa_status_string", "fa_last_error_message", "fa_fwd_noalloc",
+           "fa_set_rescale_threshold", "fa_get_rescale_threshold")
 
 
 class FaError(RuntimeError):
@@ -49,6 +50,10 @@ def lib() -> ctypes.CDLL:
     L.fa_status_string.restype = ctypes.c_char_p
     L.fa_last_error_message.argtypes = []
     L.fa_last_error_message.restype = ctypes.c_char_p
+    L.fa_set_rescale_threshold.argtypes = [ctypes.c_float]
+    L.fa_set_rescale_threshold.restype = ctypes.c_int
+    L.fa_get_rescale_threshold.argtypes = []
+    L.fa_get_rescale_threshold.restype = ctypes.c_float
     _lib = L
     return L
 
@@ -155,6 +160,15 @@ def last_device_error(stream=None) -> tuple[int, int]:
     site = ctypes.c_int(0)
     st = lib().fa_last_device_error(stream.cuda_stream, ctypes.byref(site))
     return st, site.value
+
+
+def set_rescale_threshold(log2_threshold: float) -> None:
+    """Process-wide lazy-rescale threshold (log2 units; 0 = rescale on every rise)."""
+    _raise_if(lib().fa_set_rescale_threshold(float(log2_threshold)))
+
+
+def get_rescale_threshold() -> float:
+    return float(lib().fa_get_rescale_threshold())
 
 
 def status_string(status: int) -> str:
