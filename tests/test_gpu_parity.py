@@ -209,3 +209,30 @@ def test_host_buffer_entry_matches_device_entry(fa):
     oh = torch.empty_like(qh).pin_memory()
     fa.forward_host(qh, kh, vh, oh, causal=False, scale=w.scale)
     assert np.array_equal(inputs.from_torch(oh), dev)
+
+
+def test_rescale_threshold_zero_and_default_agree(fa, orc):
+    """Rescaling on every rise of the maximum (threshold 0) and lazily (threshold 8) are the same
+    computation up to rounding; both meet the bar on the large-magnitude distribution."""
+    w = inputs.WORKLOADS["rescale_stress"].with_(B=1, H=2, Nq=2048, Nk=2048)
+    bits = inputs.draw(w)
+    ref = orc.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"), w.scale, w.causal)
+    old = fa.get_rescale_threshold()
+    try:
+        outs = {}
+        for tau in (0.0, 8.0):
+            fa.set_rescale_threshold(tau)
+            outs[tau] = inputs.from_torch(run_gpu(fa, bits, w))
+            parity.assert_parity(parity.compare(outs[tau], ref, w.dtype), False, f"tau={tau}")
+        diff = np.abs(inputs.bits_to_f64(outs[0.0], w.dtype) - inputs.bits_to_f64(outs[8.0], w.dtype))
+        assert diff.max() <= 2e-2
+    finally:
+        fa.set_rescale_threshold(old)
+
+
+def test_rescale_threshold_setter_validates(fa):
+    old = fa.get_rescale_threshold()
+    for bad in (-1.0, 16.0, float("nan")):
+        with pytest.raises(fa.FaError):
+            fa.set_rescale_threshold(bad)
+    assert fa.get_rescale_threshold() == old

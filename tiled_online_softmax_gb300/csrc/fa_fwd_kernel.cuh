@@ -22,16 +22,17 @@
 //
 // Warp roles (512 threads, registers rebalanced with setmaxnreg):
 //   warpgroup 0 (warps 0-3)  softmax of query tile 0: thread r owns row r (TMEM lane r), so row
-//                            max and sum need no shuffles.
+//                            max and sum need no shuffles. When a row of the warp moves its
+//                            reference max, the warp also rescales its rows of O_0 in TMEM.
 //   warpgroup 1 (warps 4-7)  softmax of query tile 1.
-//   warpgroup 2 (warps 8-11) correction: rescales O_0 / O_1 in TMEM when a row's reference max
-//                            moved, then divides by l and writes O.
+//   warpgroup 2 (warps 8-11) epilogue: O_t / l, rounded, written to global memory.
 //   warp 12                  MMA issuer (one lane) and TMEM owner.
 //   warp 13                  TMA producer (one lane): Q_0 and Q_1 once, then K and V tiles
 //                            through rings of stages.
 //   warps 14-15              idle.
-// The MMA warp issues, per key tile j: PV_0(j-1), S_0(j), PV_1(j-1), S_1(j). While the softmax
-// of one tile runs, the tensor cores work on the other tile's two products.
+// The MMA warp issues, per key tile j: PV_0(j) in two halves (keys 0-63 as soon as the softmax
+// releases them, then 64-127), S_0(j+1), PV_1(j) likewise, S_1(j+1). While one tile's softmax
+// runs, the tensor cores work on the other tile's products.
 //
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   [0,128) S_0 (fp32), its first 64 columns take P_0 (16-bit pairs) once S_0 is read
@@ -68,8 +69,8 @@ __host__ __device__ constexpr uint32_t tmem_s(int t) { return t ? 128u : 0u; }
 __host__ __device__ constexpr uint32_t tmem_o(int t) { return t ? 384u : 256u; }
 
 // Registers per thread after rebalancing; the launch gives 512 x 128.
-constexpr uint32_t REG_SOFTMAX = 184, REG_CORRECTION = 80, REG_MISC = 64;
-static_assert(8 * 32 * REG_SOFTMAX + 4 * 32 * REG_CORRECTION + 4 * 32 * REG_MISC <= 512 * 128,
+constexpr uint32_t REG_SOFTMAX = 184, REG_EPILOGUE = 64, REG_MISC = 72;
+static_assert(8 * 32 * REG_SOFTMAX + 4 * 32 * REG_EPILOGUE + 4 * 32 * REG_MISC <= 512 * 128,
               "setmaxnreg split exceeds the launch's register file");
 
 // Wait-site codes written to the device error word (first timeout wins).
@@ -81,8 +82,8 @@ enum WaitSite : int {
     SITE_MMA_P_FULL = 5,
     SITE_MMA_V_FULL = 6,
     SITE_SOFTMAX_S_FULL = 7,
-    SITE_CORR_SCALE = 8,
-    SITE_CORR_O_READY = 9,
+    SITE_EPI_L_READY = 8,
+    SITE_EPI_O_READY = 9,
     SITE_DRAIN = 10,
 };
 
@@ -115,9 +116,10 @@ struct Smem {
     static constexpr int B_V_FULL = B_K_EMPTY + STAGES;
     static constexpr int B_V_EMPTY = B_V_FULL + STAGES;
     static constexpr int B_S_FULL = B_V_EMPTY + STAGES;         // [2] MMA -> softmax
-    static constexpr int B_SCALE = B_S_FULL + Q_TILES;          // [2] softmax -> correction
-    static constexpr int B_P_FULL = B_SCALE + Q_TILES;          // [2] softmax+correction -> MMA
-    static constexpr int B_O_READY = B_P_FULL + Q_TILES;        // [2] MMA -> correction
+    static constexpr int B_P_HALF = B_S_FULL + Q_TILES;         // [2] softmax -> MMA (keys 0-63)
+    static constexpr int B_P_FULL = B_P_HALF + Q_TILES;         // [2] softmax -> MMA (keys 64-127)
+    static constexpr int B_L_READY = B_P_FULL + Q_TILES;        // [2] softmax -> epilogue
+    static constexpr int B_O_READY = B_L_READY + Q_TILES;       // [2] MMA -> epilogue
     static constexpr int B_DRAIN = B_O_READY + Q_TILES;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + NUM_BARS * 8;
@@ -188,11 +190,12 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
     const int r = threadIdx.x & 127;          // row within the tile = TMEM lane
     const int warp = threadIdx.x >> 5;
     const int row = q_tile0 + r;
-    const uint32_t s_cols = tmem + (static_cast<uint32_t>((warp & 3) * 32) << 16) + tmem_s(t);
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t s_cols = tmem + lane_base + tmem_s(t);
+    const uint32_t o_cols = tmem + lane_base + tmem_o(t);
     const float c = p.scale_log2;
     const bool neg = c < 0.f;
     const float tau = p.rescale_threshold;
-    float* row_scale = rows + (0 * Q_TILES + t) * BM;
     float* row_l = rows + (1 * Q_TILES + t) * BM;
     float* row_m = rows + (2 * Q_TILES + t) * BM;
     float m_ref = -INFINITY;  // reference max of the scaled scores (log2 units)
@@ -254,100 +257,82 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
             corr = (m_ref == -INFINITY) ? 0.f : ptx::ex2(m_ref - m_new);
             m_ref = m_new;
         }
-        row_scale[r] = corr;
-        ptx::mbar_arrive(bar(L::B_SCALE + t));
         const float neg_m = (m_ref == -INFINITY) ? 0.f : -m_ref;
 
         // P = 2^(s*c - m_ref), rounded to 16 bits; l sums the rounded values, so O / l is an
-        // exact weighted average of V under the weights the PV product uses.
+        // exact weighted average of V under the weights the PV product uses. P is released in two
+        // halves (keys 0-63, then 64-127) so the PV product starts on the first half while the
+        // second is computed.
         float acc[8];
 #pragma unroll
         for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-        uint32_t pk[2][32];
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
+        for (int h = 0; h < 2; ++h) {
+            uint32_t pk[32];
 #pragma unroll
-            for (int i = 0; i < 32; i += 2) {
-                float x0, x1;
-                ptx::ffma2(x0, x1, __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]), c,
-                           neg_m);
-                float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-                if (need_mask) {
-                    if (q * 32 + i >= lim) p0 = 0.f;
-                    if (q * 32 + i + 1 >= lim) p1 = 0.f;
+            for (int qq = 0; qq < 2; ++qq) {
+                const int q = 2 * h + qq;
+#pragma unroll
+                for (int i = 0; i < 32; i += 2) {
+                    float x0, x1;
+                    ptx::ffma2(x0, x1, __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]),
+                               c, neg_m);
+                    float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
+                    if (need_mask) {
+                        if (q * 32 + i >= lim) p0 = 0.f;
+                        if (q * 32 + i + 1 >= lim) p1 = 0.f;
+                    }
+                    const uint32_t u = pack2<BF16>(p0, p1);
+                    ptx::add_halves<BF16>(acc[(i >> 1) & 3], acc[4 + ((i >> 1) & 3)], u);
+                    pk[qq * 16 + i / 2] = u;
                 }
-                const uint32_t u = pack2<BF16>(p0, p1);
-                ptx::add_halves<BF16>(acc[(i >> 1) & 3], acc[4 + ((i >> 1) & 3)], u);
-                pk[q >> 1][(q & 1) * 16 + i / 2] = u;
             }
+            ptx::tmem_st32(s_cols + h * 32, pk);
+            if (h == 0 && j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
+                // Rescale this warp's O rows when any of them moved its reference. No wait is
+                // needed: the S_t(j) commit this warp waited on was issued after PV_t(j-1), so
+                // O_t holds every key < k0, and PV_t(j) starts only after this warp's release.
+#pragma unroll
+                for (int q = 0; q < D / 32; ++q) {
+                    uint32_t o[32];
+                    ptx::tmem_ld32(o_cols + q * 32, o);
+                    ptx::tmem_wait_ld();
+                    ptx::reg_fence(o);
+#pragma unroll
+                    for (int i = 0; i < 32; ++i)
+                        o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
+                    ptx::tmem_st32(o_cols + q * 32, o);
+                }
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(h == 0 ? L::B_P_HALF + t : L::B_P_FULL + t));
         }
         const float rowsum =
             ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         l = l * corr + rowsum;
-        ptx::tmem_st32(s_cols + 0, pk[0]);
-        ptx::tmem_st32(s_cols + 32, pk[1]);
-        ptx::tmem_wait_st();
-        ptx::tc_fence_before();
-        ptx::mbar_arrive(bar(L::B_P_FULL + t));
     }
     row_l[r] = l;
     row_m[r] = m_ref;
-    ptx::mbar_arrive(bar(L::B_SCALE + t));
+    ptx::mbar_arrive(bar(L::B_L_READY + t));
 }
 
 // ---------------------------------------------------------------------------------------------
-// correction and epilogue (warpgroup 2)
+// epilogue (warpgroup 2): O_t / l, rounded to the 16-bit type, one row per thread
 // ---------------------------------------------------------------------------------------------
 template <int D, bool BF16>
-__device__ __forceinline__ void correction_role(uint32_t tmem, uint32_t sbase, const float* rows,
-                                                const Params& p, const Ctl& ctl, int bh, int q0,
-                                                const int (&n_tiles)[Q_TILES]) {
+__device__ __forceinline__ void epilogue_role(uint32_t tmem, uint32_t sbase, const float* rows,
+                                              const Params& p, const Ctl& ctl, int bh, int q0) {
     using L = Smem<D>;
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     const int r = threadIdx.x & 127;
     const int warp = threadIdx.x >> 5;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const int n_max = n_tiles[Q_TILES - 1];
-
-    for (int j = 0; j < n_max; ++j) {
-#pragma unroll
-        for (int t = 0; t < Q_TILES; ++t) {
-            if (j >= n_tiles[t]) continue;
-            if (!wait_bar_warp(bar(L::B_SCALE + t), j & 1, ctl, SITE_CORR_SCALE)) return;
-            if (j > 0) {
-                const float corr = rows[(0 * Q_TILES + t) * BM + r];
-                // O_t holds sum_{i<j} P_i V_i relative to the old reference once PV(j-1) is done.
-                if (!wait_bar_warp(bar(L::B_O_READY + t), (j - 1) & 1, ctl, SITE_CORR_O_READY))
-                    return;
-                ptx::tc_fence_after();
-                if (__any_sync(0xffffffffu, corr != 1.f)) {
-                    const uint32_t o_cols = tmem + lane_base + tmem_o(t);
-#pragma unroll
-                    for (int q = 0; q < D / 32; ++q) {
-                        uint32_t o[32];
-                        ptx::tmem_ld32(o_cols + q * 32, o);
-                        ptx::tmem_wait_ld();
-                        ptx::reg_fence(o);
-#pragma unroll
-                        for (int i = 0; i < 32; ++i)
-                            o[i] = __float_as_uint(__uint_as_float(o[i]) * corr);
-                        ptx::tmem_st32(o_cols + q * 32, o);
-                    }
-                    ptx::tmem_wait_st();
-                }
-            }
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(L::B_P_FULL + t));
-        }
-    }
-
-    // Epilogue: O_t / l, rounded to the 16-bit type, one row per thread.
 #pragma unroll
     for (int t = 0; t < Q_TILES; ++t) {
-        const int n = n_tiles[t];
-        if (!wait_bar_warp(bar(L::B_SCALE + t), n & 1, ctl, SITE_CORR_SCALE)) return;
+        if (!wait_bar_warp(bar(L::B_L_READY + t), 0, ctl, SITE_EPI_L_READY)) return;
         const float l = rows[(1 * Q_TILES + t) * BM + r];
-        if (!wait_bar_warp(bar(L::B_O_READY + t), (n - 1) & 1, ctl, SITE_CORR_O_READY)) return;
+        if (!wait_bar_warp(bar(L::B_O_READY + t), 0, ctl, SITE_EPI_O_READY)) return;
         ptx::tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
         const int row = q0 + t * BM + r;
@@ -420,8 +405,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         for (int t = 0; t < Q_TILES; ++t) {
             ptx::mbar_init(bar(L::B_Q_FULL + t), 1);
             ptx::mbar_init(bar(L::B_S_FULL + t), 1);
-            ptx::mbar_init(bar(L::B_SCALE + t), BM);
-            ptx::mbar_init(bar(L::B_P_FULL + t), 2 * BM);  // softmax rows + correction rows
+            ptx::mbar_init(bar(L::B_P_HALF + t), BM);
+            ptx::mbar_init(bar(L::B_P_FULL + t), BM);
+            ptx::mbar_init(bar(L::B_L_READY + t), BM);
             ptx::mbar_init(bar(L::B_O_READY + t), 1);
         }
         for (int s = 0; s < STAGES; ++s) {
@@ -502,28 +488,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // S_t = Q_t K_j^T: K-dimension D in steps of 16 elements (32 bytes inside a
                 // 128-byte swizzle row); Q and K tiles are K-major, 8-row swizzle atoms 1024
                 // bytes apart, the second 64 columns of D one column block further.
+                // Descriptors are built once per operand tile; a step of k adds its byte offset
+                // (>> 4) to the start-address field.
                 auto issue_s = [&](int t, int j) {
                     const int st = j % STAGES;
+                    const uint64_t a0 = ptx::sdesc_sw128(sq + t * L::Q_TILE_BYTES, 16, 1024);
+                    const uint64_t b0 = ptx::sdesc_sw128(sk + st * L::KV_BYTES, 16, 1024);
 #pragma unroll
                     for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk / 4) * (BM * 128) + (kk % 4) * 32;
-                        const uint64_t a = ptx::sdesc_sw128(sq + t * L::Q_TILE_BYTES + off, 16, 1024);
-                        const uint64_t b = ptx::sdesc_sw128(
-                            sk + st * L::KV_BYTES + (kk / 4) * (BN * 128) + (kk % 4) * 32, 16, 1024);
-                        ptx::mma_ss(tmem + tmem_s(t), a, b, IDESC_S, kk > 0 ? 1u : 0u);
+                        const uint32_t off = ((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4;
+                        ptx::mma_ss(tmem + tmem_s(t), a0 + off, b0 + off, IDESC_S, kk > 0 ? 1u : 0u);
                     }
                 };
                 // O_t += P_t V_j: K-dimension BN keys in steps of 16; P_t is the A operand from
                 // TMEM (16 keys = 8 columns of 16-bit pairs); V_j is B in MN-major layout (D
                 // contiguous): 16 keys = 16 rows of 128 bytes, the next 64 columns of D one
                 // column block (BN rows) away.
-                auto issue_pv = [&](int t, int j) {
+                auto issue_pv = [&](int t, int j, int half) {
                     const int st = j % STAGES;
+                    const uint64_t b0 = ptx::sdesc_sw128(sv + st * L::KV_BYTES, BN * 128, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < BN / 16; ++kk) {
-                        const uint64_t b = ptx::sdesc_sw128(sv + st * L::KV_BYTES + kk * (16 * 128),
-                                                            BN * 128, 1024);
-                        ptx::mma_ts(tmem + tmem_o(t), tmem + tmem_s(t) + kk * 8, b, IDESC_O,
+                    for (int kk = half * (BN / 32); kk < (half + 1) * (BN / 32); ++kk) {
+                        ptx::mma_ts(tmem + tmem_o(t), tmem + tmem_s(t) + kk * 8,
+                                    b0 + ((kk * 16 * 128) >> 4), IDESC_O,
                                     (j > 0 || kk > 0) ? 1u : 0u);
                     }
                 };
@@ -549,10 +536,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     if (!(ok = wait_bar(bar(L::B_V_FULL + st), (j / STAGES) & 1, ctl, SITE_MMA_V_FULL)))
                         break;
                     if (j < n0) {
+                        if (!(ok = wait_bar(bar(L::B_P_HALF + 0), j & 1, ctl, SITE_MMA_P_FULL))) break;
+                        ptx::tc_fence_after();
+                        issue_pv(0, j, 0);
                         if (!(ok = wait_bar(bar(L::B_P_FULL + 0), j & 1, ctl, SITE_MMA_P_FULL))) break;
                         ptx::tc_fence_after();
-                        issue_pv(0, j);
-                        ptx::mma_commit(bar(L::B_O_READY + 0));
+                        issue_pv(0, j, 1);
+                        if (j + 1 == n0) ptx::mma_commit(bar(L::B_O_READY + 0));
                         if (j + 1 < n0) {
                             if (!(ok = wait_bar(bar(L::B_K_FULL + st1), ph1, ctl, SITE_MMA_K_FULL)))
                                 break;
@@ -561,10 +551,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             ptx::mma_commit(bar(L::B_S_FULL + 0));
                         }
                     }
+                    if (!(ok = wait_bar(bar(L::B_P_HALF + 1), j & 1, ctl, SITE_MMA_P_FULL))) break;
+                    ptx::tc_fence_after();
+                    issue_pv(1, j, 0);
                     if (!(ok = wait_bar(bar(L::B_P_FULL + 1), j & 1, ctl, SITE_MMA_P_FULL))) break;
                     ptx::tc_fence_after();
-                    issue_pv(1, j);
-                    ptx::mma_commit(bar(L::B_O_READY + 1));
+                    issue_pv(1, j, 1);
+                    if (j + 1 == n1) ptx::mma_commit(bar(L::B_O_READY + 1));
                     ptx::mma_commit(bar(L::B_V_EMPTY + st));
                     if (j + 1 < n1) {
                         if (!(ok = wait_bar(bar(L::B_K_FULL + st1), ph1, ctl, SITE_MMA_K_FULL)))
@@ -584,9 +577,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
         }
     } else if (wg == 2) {
-        ptx::regs_dec<REG_CORRECTION>();
-        correction_role<D, BF16>(tmem, sbase, rows, p, ctl, bh, q0, n_tiles);
-        ptx::tmem_wait_st();
+        ptx::regs_dec<REG_EPILOGUE>();
+        epilogue_role<D, BF16>(tmem, sbase, rows, p, ctl, bh, q0);
     } else {
         ptx::regs_inc<REG_SOFTMAX>();
         softmax_role<D, BF16, CAUSAL>(wg, tmem, sbase, rows, p, ctl, q0 + wg * BM, n_tiles[wg]);
