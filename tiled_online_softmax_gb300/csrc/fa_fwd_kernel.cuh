@@ -26,7 +26,7 @@
 //                            reference max, the warp also rescales its rows of O_0 in TMEM.
 //   warpgroup 1 (warps 4-7)  softmax of query tile 1.
 //   warpgroup 2 (warps 8-11) epilogue: O_t / l, rounded, written to global memory.
-//   warp 12                  MMA issuer (one lane) and TMEM owner.
+//   warp 12                  MMA issuer (an elected lane issues) and TMEM owner.
 //   warp 13                  TMA producer (one lane): Q_0 and Q_1 once, then K and V tiles
 //                            through rings of stages.
 //   warps 14-15              idle.
@@ -193,7 +193,9 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_cols = tmem + lane_base + tmem_s(t);
     const uint32_t o_cols = tmem + lane_base + tmem_o(t);
-    const float c = p.scale_log2;
+    // A zero scale would turn the -inf of a hidden score into 0 * inf = NaN; a tiny positive
+    // scale gives the same weights (every visible score maps to 2^0 = 1) and keeps -inf -> 0.
+    const float c = (p.scale_log2 == 0.f) ? 1e-30f : p.scale_log2;
     const bool neg = c < 0.f;
     const float tau = p.rescale_threshold;
     float* row_l = rows + (1 * Q_TILES + t) * BM;
@@ -277,11 +279,8 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
                     float x0, x1;
                     ptx::ffma2(x0, x1, __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]),
                                c, neg_m);
-                    float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
-                    if (need_mask) {
-                        if (q * 32 + i >= lim) p0 = 0.f;
-                        if (q * 32 + i + 1 >= lim) p1 = 0.f;
-                    }
+                    // A hidden score holds -inf (+inf when c < 0), so its weight is 2^-inf = 0.
+                    const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
                     const uint32_t u = pack2<BF16>(p0, p1);
                     ptx::add_halves<BF16>(acc[(i >> 1) & 3], acc[4 + ((i >> 1) & 3)], u);
                     pk[qq * 16 + i / 2] = u;
@@ -481,98 +480,90 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             __syncwarp();
         } else if (warp == MMA_WARP) {
             // -------------------------------------------------------------- MMA issuer
-            if (lane == 0) {
-                constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);
-                constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, D, false, true);
-                const uint32_t sq = sbase + L::Q_OFF, sk = sbase + L::K_OFF, sv = sbase + L::V_OFF;
-                // S_t = Q_t K_j^T: K-dimension D in steps of 16 elements (32 bytes inside a
-                // 128-byte swizzle row); Q and K tiles are K-major, 8-row swizzle atoms 1024
-                // bytes apart, the second 64 columns of D one column block further.
-                // Descriptors are built once per operand tile; a step of k adds its byte offset
-                // (>> 4) to the start-address field.
-                auto issue_s = [&](int t, int j) {
-                    const int st = j % STAGES;
-                    const uint64_t a0 = ptx::sdesc_sw128(sq + t * L::Q_TILE_BYTES, 16, 1024);
-                    const uint64_t b0 = ptx::sdesc_sw128(sk + st * L::KV_BYTES, 16, 1024);
+            // The whole warp runs the loop (descriptors stay warp-uniform); one elected lane
+            // issues the MMAs and commits.
+            uint32_t leader;
+            asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+                         : "=r"(leader));
+            constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);
+            constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, D, false, true);
+            const uint32_t sq = sbase + L::Q_OFF, sk = sbase + L::K_OFF, sv = sbase + L::V_OFF;
+            // S_t = Q_t K_j^T: K-dimension D in steps of 16 elements (32 bytes inside a 128-byte
+            // swizzle row); Q and K tiles are K-major, 8-row swizzle atoms 1024 bytes apart, the
+            // second 64 columns of D one column block further. Descriptors are built once per
+            // operand tile; a step of k adds its byte offset (>> 4) to the start-address field.
+            auto issue_s = [&](int t, int j) {
+                const uint64_t a0 = ptx::sdesc_sw128(sq + t * L::Q_TILE_BYTES, 16, 1024);
+                const uint64_t b0 = ptx::sdesc_sw128(sk + (j % STAGES) * L::KV_BYTES, 16, 1024);
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = ((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4;
+                for (int kk = 0; kk < D / 16; ++kk) {
+                    const uint32_t off = ((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4;
+                    if (leader)
                         ptx::mma_ss(tmem + tmem_s(t), a0 + off, b0 + off, IDESC_S, kk > 0 ? 1u : 0u);
-                    }
-                };
-                // O_t += P_t V_j: K-dimension BN keys in steps of 16; P_t is the A operand from
-                // TMEM (16 keys = 8 columns of 16-bit pairs); V_j is B in MN-major layout (D
-                // contiguous): 16 keys = 16 rows of 128 bytes, the next 64 columns of D one
-                // column block (BN rows) away.
-                auto issue_pv = [&](int t, int j, int half) {
-                    const int st = j % STAGES;
-                    const uint64_t b0 = ptx::sdesc_sw128(sv + st * L::KV_BYTES, BN * 128, 1024);
+                }
+            };
+            // O_t += P_t V_j over keys [64 half, 64 half + 64): P_t is the A operand from TMEM
+            // (16 keys = 8 columns of 16-bit pairs); V_j is B in MN-major layout (D contiguous):
+            // 16 keys = 16 rows of 128 bytes, the next 64 columns of D one column block away.
+            auto issue_pv = [&](int t, int j, int half) {
+                const uint64_t b0 = ptx::sdesc_sw128(sv + (j % STAGES) * L::KV_BYTES, BN * 128, 1024);
 #pragma unroll
-                    for (int kk = half * (BN / 32); kk < (half + 1) * (BN / 32); ++kk) {
+                for (int kk = half * (BN / 32); kk < (half + 1) * (BN / 32); ++kk)
+                    if (leader)
                         ptx::mma_ts(tmem + tmem_o(t), tmem + tmem_s(t) + kk * 8,
-                                    b0 + ((kk * 16 * 128) >> 4), IDESC_O,
-                                    (j > 0 || kk > 0) ? 1u : 0u);
-                    }
-                };
-                const int n0 = n_tiles[0], n1 = n_tiles[Q_TILES - 1];
-                bool ok = wait_bar(bar(L::B_Q_FULL + 0), 0, ctl, SITE_MMA_Q_FULL) &&
-                          wait_bar(bar(L::B_K_FULL + 0), 0, ctl, SITE_MMA_K_FULL);
-                if (ok) {
+                                    b0 + ((kk * 16 * 128) >> 4), IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+            };
+            auto commit = [&](int b) {
+                if (leader) ptx::mma_commit(bar(b));
+                __syncwarp();
+            };
+            // Per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1). S_t(j+1) overwrites the TMEM
+            // columns P_t(j) occupies, so it follows PV_t(j) (MMAs of one thread run in order).
+            const int n0 = n_tiles[0], n1 = n_tiles[Q_TILES - 1];
+            bool ok = wait_bar_warp(bar(L::B_Q_FULL + 0), 0, ctl, SITE_MMA_Q_FULL) &&
+                      wait_bar_warp(bar(L::B_K_FULL + 0), 0, ctl, SITE_MMA_K_FULL);
+            if (ok) {
+                ptx::tc_fence_after();
+                issue_s(0, 0);
+                commit(L::B_S_FULL + 0);
+                ok = wait_bar_warp(bar(L::B_Q_FULL + 1), 0, ctl, SITE_MMA_Q_FULL);
+            }
+            if (ok) {
+                ptx::tc_fence_after();
+                issue_s(1, 0);
+                commit(L::B_S_FULL + 1);
+                commit(L::B_K_EMPTY + 0);
+            }
+            for (int j = 0; ok && j < n1; ++j) {
+                const int st = j % STAGES, st1 = (j + 1) % STAGES;
+                const uint32_t ph1 = ((j + 1) / STAGES) & 1;
+                if (!(ok = wait_bar_warp(bar(L::B_V_FULL + st), (j / STAGES) & 1, ctl, SITE_MMA_V_FULL)))
+                    break;
+                for (int t = 0; t < Q_TILES; ++t) {
+                    if (j >= n_tiles[t]) continue;
+                    if (!(ok = wait_bar_warp(bar(L::B_P_HALF + t), j & 1, ctl, SITE_MMA_P_FULL))) break;
                     ptx::tc_fence_after();
-                    issue_s(0, 0);
-                    ptx::mma_commit(bar(L::B_S_FULL + 0));
-                    ok = wait_bar(bar(L::B_Q_FULL + 1), 0, ctl, SITE_MMA_Q_FULL);
-                }
-                if (ok) {
+                    issue_pv(t, j, 0);
+                    if (!(ok = wait_bar_warp(bar(L::B_P_FULL + t), j & 1, ctl, SITE_MMA_P_FULL))) break;
                     ptx::tc_fence_after();
-                    issue_s(1, 0);
-                    ptx::mma_commit(bar(L::B_S_FULL + 1));
-                    ptx::mma_commit(bar(L::B_K_EMPTY + 0));
-                }
-                for (int j = 0; ok && j < n1; ++j) {
-                    const int st = j % STAGES;
-                    const int st1 = (j + 1) % STAGES;
-                    const uint32_t ph1 = ((j + 1) / STAGES) & 1;
-                    if (!(ok = wait_bar(bar(L::B_V_FULL + st), (j / STAGES) & 1, ctl, SITE_MMA_V_FULL)))
-                        break;
-                    if (j < n0) {
-                        if (!(ok = wait_bar(bar(L::B_P_HALF + 0), j & 1, ctl, SITE_MMA_P_FULL))) break;
-                        ptx::tc_fence_after();
-                        issue_pv(0, j, 0);
-                        if (!(ok = wait_bar(bar(L::B_P_FULL + 0), j & 1, ctl, SITE_MMA_P_FULL))) break;
-                        ptx::tc_fence_after();
-                        issue_pv(0, j, 1);
-                        if (j + 1 == n0) ptx::mma_commit(bar(L::B_O_READY + 0));
-                        if (j + 1 < n0) {
-                            if (!(ok = wait_bar(bar(L::B_K_FULL + st1), ph1, ctl, SITE_MMA_K_FULL)))
-                                break;
-                            ptx::tc_fence_after();
-                            issue_s(0, j + 1);
-                            ptx::mma_commit(bar(L::B_S_FULL + 0));
-                        }
-                    }
-                    if (!(ok = wait_bar(bar(L::B_P_HALF + 1), j & 1, ctl, SITE_MMA_P_FULL))) break;
-                    ptx::tc_fence_after();
-                    issue_pv(1, j, 0);
-                    if (!(ok = wait_bar(bar(L::B_P_FULL + 1), j & 1, ctl, SITE_MMA_P_FULL))) break;
-                    ptx::tc_fence_after();
-                    issue_pv(1, j, 1);
-                    if (j + 1 == n1) ptx::mma_commit(bar(L::B_O_READY + 1));
-                    ptx::mma_commit(bar(L::B_V_EMPTY + st));
-                    if (j + 1 < n1) {
-                        if (!(ok = wait_bar(bar(L::B_K_FULL + st1), ph1, ctl, SITE_MMA_K_FULL)))
+                    issue_pv(t, j, 1);
+                    if (j + 1 == n_tiles[t]) commit(L::B_O_READY + t);
+                    if (t == Q_TILES - 1) commit(L::B_V_EMPTY + st);
+                    if (j + 1 < n_tiles[t]) {
+                        if (!(ok = wait_bar_warp(bar(L::B_K_FULL + st1), ph1, ctl, SITE_MMA_K_FULL)))
                             break;
                         ptx::tc_fence_after();
-                        issue_s(1, j + 1);
-                        ptx::mma_commit(bar(L::B_S_FULL + 1));
-                        ptx::mma_commit(bar(L::B_K_EMPTY + st1));
+                        issue_s(t, j + 1);
+                        commit(L::B_S_FULL + t);
+                        if (t == Q_TILES - 1) commit(L::B_K_EMPTY + st1);
                     }
                 }
-                if (*abort_flag) {
-                    // Drain: wait until every MMA this thread issued has finished.
-                    ptx::mma_commit(bar(L::B_DRAIN));
-                    wait_bar(bar(L::B_DRAIN), 0, ctl, SITE_DRAIN, false);
-                }
+            }
+            (void)n0;
+            if (*abort_flag) {
+                // Drain: wait until every MMA this warp issued has finished.
+                commit(L::B_DRAIN);
+                wait_bar(bar(L::B_DRAIN), 0, ctl, SITE_DRAIN, false);
             }
             __syncwarp();
         }
