@@ -79,6 +79,17 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
                  void* stream);
 
 /*
+ * fa_fwd_lse -- fa_fwd that also writes each query row's log-sum-exp
+ *   LSE[b, h, i] = log sum_j exp(scale * Q[b,h,i,:] . K[b,h,j,:])   over the visible keys j,
+ * the per-row statistic a backward pass recomputes P from ("Flash Attention 2", "Write the
+ * data back to HBM": L = m + log l). LSE is a device pointer to fp32 [B, H, Nq], 4-byte
+ * aligned, written, not overlapping any other tensor. Everything else is as in fa_fwd.
+ */
+fa_status fa_fwd_lse(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
+                     int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,
+                     fa_dtype dtype, void* stream);
+
+/*
  * fa_fwd_host -- the same operation on HOST buffers, synchronous.
  *
  * Q, K, V, O are host pointers with the layout above (pinned memory gives full copy speed).

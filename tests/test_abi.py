@@ -67,6 +67,14 @@ def test_rejects_bad_arguments(fa, kw, status):
     assert fa.lib().fa_last_error_message().decode()
 
 
+def test_lse_entry_rejects_bad_arguments(fa):
+    lse = fa.lib().fa_fwd_lse
+    assert lse(A, 2 * A, 3 * A, 4 * A, 0, 1, 1, 8, 8, 64, 0.1, 0, 0, 0) == 1          # null LSE
+    assert lse(A, 2 * A, 3 * A, 4 * A, 5 * A + 2, 1, 1, 8, 8, 64, 0.1, 0, 0, 0) == 3  # misaligned
+    assert lse(A, 2 * A, 3 * A, 4 * A, 4 * A, 1, 1, 8, 8, 64, 0.1, 0, 0, 0) == 1      # overlaps O
+    assert lse(A, 2 * A, 3 * A, 4 * A, 5 * A, 1, 1, 8, 8, 96, 0.1, 0, 0, 0) == 2      # D
+
+
 def test_host_entry_rejects_bad_arguments(fa):
     assert fa.fa_fwd_host(0, A, A, A, 1, 1, 8, 8, 64, 0.1, 0, 0, 0) == 1
     assert fa.fa_fwd_host(A, A, A, 4 * A, 1, 1, 8, 8, 80, 0.1, 0, 0, 0) == 2

@@ -169,8 +169,8 @@ fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtens
     return FA_OK;
 }
 
-fa_status launch(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H,
-                 int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, int dtype,
+fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
+                 int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, int dtype,
                  cudaStream_t stream) {
     int dev = 0;
     int* err = nullptr;
@@ -183,6 +183,7 @@ fa_status launch(const void* Q, const void* K, const void* V, void* O, int64_t B
     if ((s = encode_map(&mv, V, bh, Nk, D, dtype)) != FA_OK) return s;
     fa::Params p{};
     p.o = O;
+    p.lse = LSE;
     p.err = err;
     p.bh = static_cast<int>(bh);
     p.nq = static_cast<int>(Nq);
@@ -273,6 +274,7 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, i
     if ((s = encode_map(&mv, V, bh, Nk, D, int(dtype))) != FA_OK) return s;
     fa::Params p{};
     p.o = O;
+    p.lse = nullptr;
     p.err = scratch;
     p.bh = static_cast<int>(bh);
     p.nq = static_cast<int>(Nq);
@@ -299,7 +301,25 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
                  void* stream) {
     fa_status s = validate(Q, K, V, O, B, H, Nq, Nk, D, scale, causal, int(dtype), true);
     if (s != FA_OK) return s;
-    return launch(Q, K, V, O, B, H, Nq, Nk, D, scale, causal, int(dtype),
+    return launch(Q, K, V, O, nullptr, B, H, Nq, Nk, D, scale, causal, int(dtype),
+                  static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_fwd_lse(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
+                     int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,
+                     fa_dtype dtype, void* stream) {
+    fa_status s = validate(Q, K, V, O, B, H, Nq, Nk, D, scale, causal, int(dtype), true);
+    if (s != FA_OK) return s;
+    if (!LSE) return fail(FA_ERR_INVALID_ARGUMENT, "null LSE pointer");
+    if (reinterpret_cast<uintptr_t>(LSE) % 4 != 0)
+        return fail(FA_ERR_MISALIGNED, "LSE pointer %p is not 4-byte aligned", static_cast<void*>(LSE));
+    const size_t q_bytes = size_t(B * H) * size_t(Nq) * size_t(D) * 2;
+    const size_t lse_bytes = size_t(B * H) * size_t(Nq) * 4;
+    const size_t kv_bytes = size_t(B * H) * size_t(Nk) * size_t(D) * 2;
+    if (overlaps(LSE, lse_bytes, O, q_bytes) || overlaps(LSE, lse_bytes, Q, q_bytes) ||
+        overlaps(LSE, lse_bytes, K, kv_bytes) || overlaps(LSE, lse_bytes, V, kv_bytes))
+        return fail(FA_ERR_INVALID_ARGUMENT, "LSE overlaps another tensor");
+    return launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, causal, int(dtype),
                   static_cast<cudaStream_t>(stream));
 }
 
@@ -334,7 +354,7 @@ fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int6
         (e = cudaMemcpyAsync(dk, K, kv_bytes, cudaMemcpyHostToDevice, strm)) != cudaSuccess ||
         (e = cudaMemcpyAsync(dv, V, kv_bytes, cudaMemcpyHostToDevice, strm)) != cudaSuccess)
         return cuda_fail(e, "cudaMemcpyAsync(host to device)");
-    s = launch(dq, dk, dv, dout, B, H, Nq, Nk, D, scale, causal, int(dtype), strm);
+    s = launch(dq, dk, dv, dout, nullptr, B, H, Nq, Nk, D, scale, causal, int(dtype), strm);
     if (s != FA_OK) return s;
     if ((e = cudaMemcpyAsync(O, dout, q_bytes, cudaMemcpyDeviceToHost, strm)) != cudaSuccess)
         return cuda_fail(e, "cudaMemcpyAsync(device to host)");

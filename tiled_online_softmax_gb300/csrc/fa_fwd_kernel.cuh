@@ -89,6 +89,7 @@ enum WaitSite : int {
 
 struct Params {
     void* o;                   // output [bh][nq][D]
+    float* lse;                // optional log-sum-exp output [bh][nq] (natural log), or null
     int* err;                  // device error word (site code of the first timeout)
     int bh;                    // B * H
     int nq, nk;
@@ -331,10 +332,16 @@ __device__ __forceinline__ void epilogue_role(uint32_t tmem, uint32_t sbase, con
     for (int t = 0; t < Q_TILES; ++t) {
         if (!wait_bar_warp(bar(L::B_L_READY + t), 0, ctl, SITE_EPI_L_READY)) return;
         const float l = rows[(1 * Q_TILES + t) * BM + r];
+        const int row = q0 + t * BM + r;
+        if (p.lse != nullptr && row < p.nq) {
+            // L = m + log l in natural-log units ("Flash Attention 2", "Write the data back to
+            // HBM"): the kernel's m and l are in base 2 relative to the reference maximum.
+            const float m2 = rows[(2 * Q_TILES + t) * BM + r];
+            p.lse[static_cast<size_t>(bh) * p.nq + row] = (m2 + __log2f(l)) * 0.6931471805599453f;
+        }
         if (!wait_bar_warp(bar(L::B_O_READY + t), 0, ctl, SITE_EPI_O_READY)) return;
         ptx::tc_fence_after();
         const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-        const int row = q0 + t * BM + r;
         const uint32_t o_cols = tmem + lane_base + tmem_o(t);
         uint8_t* out_row =
             static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.nq + row) * (D * 2);

@@ -14,7 +14,7 @@ STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED",
           3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_error",
            "fa_status_string", "fa_last_error_message", "fa_fwd_noalloc",
-           "fa_set_rescale_threshold", "fa_get_rescale_threshold")
+           "fa_set_rescale_threshold", "fa_get_rescale_threshold", "fa_fwd_lse")
 
 
 class FaError(RuntimeError):
@@ -42,6 +42,8 @@ def lib() -> ctypes.CDLL:
     L.fa_fwd_host.restype = ctypes.c_int
     L.fa_fwd_noalloc.argtypes = sig
     L.fa_fwd_noalloc.restype = ctypes.c_int
+    L.fa_fwd_lse.argtypes = sig[:4] + [vp] + sig[4:]
+    L.fa_fwd_lse.restype = ctypes.c_int
     L.fa_release_host_buffers.argtypes = []
     L.fa_release_host_buffers.restype = ctypes.c_int
     L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
@@ -128,6 +130,32 @@ def forward(q, k, v, causal: bool = False, scale: float | None = None, out=None,
         _raise_if(fa_fwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(), B, H, Nq, Nk,
                          D, float(scale), int(bool(causal)), code, stream.cuda_stream))
     return out
+
+
+def forward_lse(q, k, v, causal: bool = False, scale: float | None = None, out=None, lse=None,
+                stream=None):
+    """(O, LSE) for CUDA tensors; LSE[b, h, i] = log sum_j exp(scale * q_i . k_j), fp32."""
+    import torch
+
+    B, H, Nq, Nk, D = _shape(q, k, v)
+    code = _dtype_code(q)
+    if not q.is_cuda:
+        raise ValueError("forward_lse() takes CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    if lse is None:
+        lse = torch.empty(B, H, Nq, dtype=torch.float32, device=q.device)
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, Nq]")
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        _raise_if(lib().fa_fwd_lse(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                   lse.data_ptr(), B, H, Nq, Nk, D, float(scale),
+                                   int(bool(causal)), code, stream.cuda_stream))
+    return out, lse
 
 
 def forward_host(q, k, v, out, causal: bool = False, scale: float | None = None, stream=None,
