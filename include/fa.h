@@ -34,6 +34,7 @@
 #ifndef TILED_ONLINE_SOFTMAX_FA_H
 #define TILED_ONLINE_SOFTMAX_FA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -88,6 +89,34 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
 fa_status fa_fwd_lse(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
                      int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,
                      fa_dtype dtype, void* stream);
+
+/*
+ * Split over keys (flash-decoding), non-causal only.
+ *
+ * With few query rows (decoding, short chunks against a long context) one CTA per 256 query
+ * rows leaves most SMs idle. fa_fwd_splitkv also splits each slice's keys into ranges: every
+ * (query block, key range) pair runs on its own CTA and leaves its partial online-softmax state
+ * (m, l and the unnormalised o, fp32) in `workspace`; a second kernel merges the states of each
+ * row with the state-merge rule (m = max m_s, l = sum l_s e^(m_s - m), o = sum o_s e^(m_s - m);
+ * "11. Fusion, recompute, and flash attention", section 11.6, last paragraph, and exercise
+ * "Flash-decoding") and writes O = o / l (and LSE when non-null).
+ *
+ *   num_splits  requested number of key ranges per slice; 0 picks one that covers the SMs.
+ *               The effective count is at most ceil(Nk / 128), every range holds whole tiles
+ *               of 128 keys, and 1 runs fa_fwd itself (no workspace needed).
+ *   workspace   caller-owned device memory, 256-byte aligned, at least
+ *               fa_splitkv_workspace_bytes(B, H, Nq, Nk, D, num_splits) bytes; its contents on
+ *               entry do not matter and are overwritten. Calls sharing one workspace must be
+ *               ordered on the GPU.
+ *   LSE         optional fp32 [B, H, Nq] log-sum-exp output (NULL: not written).
+ * Other arguments as in fa_fwd. Asynchronous on `stream`; two launches.
+ */
+size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
+                                  int num_splits);
+fa_status fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                         int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale,
+                         int num_splits, fa_dtype dtype, void* workspace, size_t workspace_bytes,
+                         void* stream);
 
 /*
  * fa_fwd_host -- the same operation on HOST buffers, synchronous.

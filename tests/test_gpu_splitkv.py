@@ -1,0 +1,90 @@
+"""Split over keys (flash-decoding): partial states per key range, merged by the state-merge
+rule, against the fp64 oracle and against the unsplit path."""
+import numpy as np
+import pytest
+
+import oracle
+from tests import parity
+from tiled_online_softmax_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+LSE_TOL = 4e-3
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tiled_online_softmax_gb300 import fa as fa_mod
+
+    fa_mod.lib()
+    return fa_mod
+
+
+CASES = [
+    (inputs.Workload("decode_1row", 1, 8, 1, 4096, 128, "bf16", False, seed=51), 16),
+    (inputs.Workload("decode_7rows_f16", 2, 4, 7, 3000, 64, "f16", False, seed=52), 5),
+    (inputs.Workload("chunk_ragged", 1, 2, 300, 1000, 128, "bf16", False, seed=53), 3),
+    (inputs.Workload("chunk_auto", 1, 4, 130, 777, 64, "bf16", False, seed=54), 0),
+    (inputs.Workload("more_splits_than_tiles", 1, 1, 64, 200, 128, "bf16", False, seed=55), 9),
+]
+
+
+@pytest.mark.parametrize("w,splits", CASES, ids=lambda x: x.name if hasattr(x, "name") else str(x))
+def test_splitkv_matches_oracle(fa, w, splits):
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    lse = torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device="cuda")
+    o = fa.forward_splitkv(q, k, v, num_splits=splits, scale=w.scale, lse=lse)
+    torch.cuda.synchronize()
+    assert fa.last_device_error()[0] == 0
+    ref_o, ref_lse = oracle.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"),
+                                      w.scale, False, with_lse=True)
+    stats = parity.compare(inputs.from_torch(o), ref_o, w.dtype)
+    parity.assert_parity(stats, False, w.name)
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= LSE_TOL
+    # Close to the unsplit path (different summation order, same arithmetic).
+    o1 = inputs.bits_to_f64(inputs.from_torch(fa.forward(q, k, v, scale=w.scale)), w.dtype)
+    assert np.max(np.abs(inputs.bits_to_f64(inputs.from_torch(o), w.dtype) - o1)) <= 2e-2
+
+
+def test_long_context_chunk_full_size(fa):
+    w = inputs.WORKLOADS["long_context_chunk"]
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    o = inputs.from_torch(fa.forward_splitkv(q, k, v, num_splits=0, scale=w.scale))
+    torch.cuda.synchronize()
+    assert fa.last_device_error()[0] == 0
+    for h in (0, 7):
+        ref = oracle.attention_rows(inputs.bits_to_f64(bits["q"][0, h], w.dtype), np.arange(w.Nq),
+                                    inputs.bits_to_f64(bits["k"][0, h], w.dtype),
+                                    inputs.bits_to_f64(bits["v"][0, h], w.dtype), w.scale, False)
+        parity.assert_parity(parity.compare(o[0, h], ref, w.dtype), True, f"head {h}")
+
+
+def test_one_split_is_fa_fwd(fa):
+    w = inputs.Workload("one_split", 1, 2, 200, 500, 128, "bf16", False, seed=56)
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    a = fa.forward_splitkv(q, k, v, num_splits=1, scale=w.scale)
+    b = fa.forward(q, k, v, scale=w.scale)
+    torch.cuda.synchronize()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_workspace_checks(fa):
+    q = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(1, 1, 1024, 64, dtype=torch.bfloat16, device="cuda")
+    o = torch.empty_like(q)
+    need = fa.splitkv_workspace_bytes(1, 1, 16, 1024, 64, 4)
+    assert need > 0 and fa.splitkv_workspace_bytes(1, 1, 16, 1024, 64, 1) == 0
+    ws = torch.empty(need, dtype=torch.uint8, device="cuda")
+    call = lambda ptr, size: fa.lib().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), k.data_ptr(),
+                                                     o.data_ptr(), None, 1, 1, 16, 1024, 64, 0.1,
+                                                     4, 1, ptr, size, None)
+    assert call(ws.data_ptr(), need - 1) == 1      # too small
+    assert call(None, need) == 1                    # missing
+    assert call(ws.data_ptr() + 16, need - 16) in (1, 3)  # misaligned or too small
+    assert call(ws.data_ptr(), need) == 0
+    torch.cuda.synchronize()

@@ -13,6 +13,7 @@
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
+#include "fa_merge_kernel.cuh"
 
 namespace {
 
@@ -162,16 +163,24 @@ fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtens
             g_attr_set[dev] |= 1u << inst;
         }
     }
-    const unsigned grid = static_cast<unsigned>(p.num_units) * static_cast<unsigned>(p.bh);
+    const unsigned grid = static_cast<unsigned>(p.num_units) * static_cast<unsigned>(p.bh) *
+                          static_cast<unsigned>(p.num_splits);
     kernel<<<grid, fa::NUM_THREADS, smem, stream>>>(mq, mk, mv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return FA_OK;
 }
 
+struct Split {
+    int num_splits = 1;
+    int kv_tiles_per_split = 0;
+    float* o_part = nullptr;
+    float* ml_part = nullptr;
+};
+
 fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
                  int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, int dtype,
-                 cudaStream_t stream) {
+                 cudaStream_t stream, const Split& split = Split()) {
     int dev = 0;
     int* err = nullptr;
     fa_status s = device_state(&dev, &err);
@@ -192,6 +201,11 @@ fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LS
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.rescale_threshold = g_rescale_threshold;
     p.timeout_ns = wait_timeout_ns();
+    p.num_splits = split.num_splits;
+    p.kv_tiles_per_split = split.num_splits > 1 ? split.kv_tiles_per_split
+                                                : static_cast<int>((Nk + fa::BN - 1) / fa::BN);
+    p.o_part = split.o_part;
+    p.ml_part = split.ml_part;
     const bool bf16 = dtype == FA_BF16;
     const int inst = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
     switch (inst) {
@@ -249,6 +263,32 @@ fa_status noalloc_device_state(int* dev_out, int** scratch_out) {
     return FA_OK;
 }
 
+// Effective split plan: every split gets at least one key tile.
+struct SplitPlan {
+    int num_splits;
+    int tiles_per_split;
+};
+
+SplitPlan plan_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int requested) {
+    const int64_t nkt = (Nk + fa::BN - 1) / fa::BN;
+    int64_t want = requested;
+    if (want <= 0) {
+        // Automatic: enough CTAs to cover the SMs once.
+        const int64_t units = B * H * ((Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS);
+        want = units >= 152 ? 1 : (152 + units - 1) / units;
+    }
+    want = want < 1 ? 1 : (want > nkt ? nkt : want);
+    const int64_t per = (nkt + want - 1) / want;
+    return SplitPlan{static_cast<int>((nkt + per - 1) / per), static_cast<int>(per)};
+}
+
+size_t workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t D, int splits) {
+    if (splits <= 1) return 0;
+    const size_t rows = size_t(B * H) * size_t(Nq);
+    const size_t o_bytes = (size_t(splits) * rows * size_t(D) * 4 + 255) & ~size_t(255);
+    return o_bytes + size_t(splits) * rows * 8;
+}
+
 }  // namespace
 
 extern "C" {
@@ -276,6 +316,8 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, i
     p.o = O;
     p.lse = nullptr;
     p.err = scratch;
+    p.num_splits = 1;
+    p.kv_tiles_per_split = static_cast<int>((Nk + fa::BN - 1) / fa::BN);
     p.bh = static_cast<int>(bh);
     p.nq = static_cast<int>(Nq);
     p.nk = static_cast<int>(Nk);
@@ -321,6 +363,52 @@ fa_status fa_fwd_lse(const void* Q, const void* K, const void* V, void* O, float
         return fail(FA_ERR_INVALID_ARGUMENT, "LSE overlaps another tensor");
     return launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, causal, int(dtype),
                   static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk,
+                                             int64_t D, int num_splits) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || D < 1) return 0;
+    return workspace_bytes(B, H, Nq, D, plan_splits(B, H, Nq, Nk, num_splits).num_splits);
+}
+
+fa_status fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                                    int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
+                                    float scale, int num_splits, fa_dtype dtype, void* workspace,
+                                    size_t workspace_bytes_given, void* stream) {
+    fa_status s = validate(Q, K, V, O, B, H, Nq, Nk, D, scale, 0, int(dtype), true);
+    if (s != FA_OK) return s;
+    if (LSE && reinterpret_cast<uintptr_t>(LSE) % 4 != 0)
+        return fail(FA_ERR_MISALIGNED, "LSE pointer is not 4-byte aligned");
+    const SplitPlan plan = plan_splits(B, H, Nq, Nk, num_splits);
+    auto strm = static_cast<cudaStream_t>(stream);
+    if (plan.num_splits <= 1) return launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, 0, int(dtype), strm);
+    const size_t need = workspace_bytes(B, H, Nq, D, plan.num_splits);
+    if (!workspace || workspace_bytes_given < need)
+        return fail(FA_ERR_INVALID_ARGUMENT, "workspace of %zu bytes needed for %d splits (got %zu)",
+                    need, plan.num_splits, workspace_bytes_given);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+        return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+    const size_t rows = size_t(B * H) * size_t(Nq);
+    Split sp;
+    sp.num_splits = plan.num_splits;
+    sp.kv_tiles_per_split = plan.tiles_per_split;
+    sp.o_part = static_cast<float*>(workspace);
+    sp.ml_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
+                                          ((size_t(plan.num_splits) * rows * size_t(D) * 4 + 255) & ~size_t(255)));
+    if ((s = launch(Q, K, V, O, nullptr, B, H, Nq, Nk, D, scale, 0, int(dtype), strm, sp)) != FA_OK)
+        return s;
+    const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
+    const bool bf16 = dtype == FA_BF16;
+    if (D == 128) {
+        if (bf16) fa::fa_merge_kernel<128, true><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, int64_t(rows), plan.num_splits);
+        else fa::fa_merge_kernel<128, false><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, int64_t(rows), plan.num_splits);
+    } else {
+        if (bf16) fa::fa_merge_kernel<64, true><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, int64_t(rows), plan.num_splits);
+        else fa::fa_merge_kernel<64, false><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, int64_t(rows), plan.num_splits);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    return FA_OK;
 }
 
 fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int64_t B,

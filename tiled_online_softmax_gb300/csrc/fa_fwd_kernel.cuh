@@ -94,6 +94,14 @@ struct Params {
     int bh;                    // B * H
     int nq, nk;
     int num_units;             // ceil(nq / 256)
+    // Split over keys (non-causal only): CTA (unit, split) covers key tiles
+    // [split * kv_tiles_per_split, ...) and writes its unnormalised state, not O:
+    //   o_part [num_splits][bh][nq][D] fp32, ml_part [num_splits][bh][nq][2] fp32 (m in log2
+    //   units of the scaled scores, l relative to it). num_splits = 1: no split.
+    int num_splits;
+    int kv_tiles_per_split;
+    float* o_part;
+    float* ml_part;
     float scale_log2;          // scale * log2(e)
     float rescale_threshold;   // lazy-rescale threshold, log2 units (0 = rescale on every rise)
     unsigned long long timeout_ns;
@@ -185,7 +193,7 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
 template <int D, bool BF16, bool CAUSAL>
 __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbase, float* rows,
                                              const Params& p, const Ctl& ctl, int q_tile0,
-                                             int n_tiles) {
+                                             int kv0, int n_tiles) {
     using L = Smem<D>;
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     const int r = threadIdx.x & 127;          // row within the tile = TMEM lane
@@ -215,7 +223,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
         for (int q = 0; q < 4; ++q) ptx::reg_fence(sr[q]);
 
         // Keys of this tile the row may see: [k0, k0 + lim).
-        const int k0 = j * BN;
+        const int k0 = (kv0 + j) * BN;
         const bool need_mask = (k0 + BN > p.nk) || (CAUSAL && k0 + BN - 1 > q_tile0);
         int lim = p.nk - k0;
         if constexpr (CAUSAL) lim = min(lim, row + 1 - k0);
@@ -322,7 +330,8 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
 // ---------------------------------------------------------------------------------------------
 template <int D, bool BF16>
 __device__ __forceinline__ void epilogue_role(uint32_t tmem, uint32_t sbase, const float* rows,
-                                              const Params& p, const Ctl& ctl, int bh, int q0) {
+                                              const Params& p, const Ctl& ctl, int bh, int q0,
+                                              int split) {
     using L = Smem<D>;
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     const int r = threadIdx.x & 127;
@@ -333,6 +342,30 @@ __device__ __forceinline__ void epilogue_role(uint32_t tmem, uint32_t sbase, con
         if (!wait_bar_warp(bar(L::B_L_READY + t), 0, ctl, SITE_EPI_L_READY)) return;
         const float l = rows[(1 * Q_TILES + t) * BM + r];
         const int row = q0 + t * BM + r;
+        if (p.num_splits > 1) {
+            // Partial state over this CTA's keys, merged later (split over keys).
+            if (!wait_bar_warp(bar(L::B_O_READY + t), 0, ctl, SITE_EPI_O_READY)) return;
+            ptx::tc_fence_after();
+            const size_t prow = (static_cast<size_t>(split) * p.bh + bh) * p.nq + row;
+            const uint32_t o_cols = tmem + lane_base + tmem_o(t);
+#pragma unroll 1
+            for (int q = 0; q < D / 16; ++q) {
+                uint32_t o[16];
+                ptx::tmem_ld16(o_cols + q * 16, o);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence(o);
+                if (row < p.nq) {
+                    uint4* dst = reinterpret_cast<uint4*>(p.o_part + prow * D + q * 16);
+#pragma unroll
+                    for (int v = 0; v < 4; ++v)
+                        dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+                }
+            }
+            if (row < p.nq)
+                reinterpret_cast<float2*>(p.ml_part)[prow] =
+                    make_float2(rows[(2 * Q_TILES + t) * BM + r], l);
+            continue;
+        }
         if (p.lse != nullptr && row < p.nq) {
             // L = m + log l in natural-log units ("Flash Attention 2", "Write the data back to
             // HBM"): the kernel's m and l are in base 2 relative to the reference maximum.
@@ -345,23 +378,21 @@ __device__ __forceinline__ void epilogue_role(uint32_t tmem, uint32_t sbase, con
         const uint32_t o_cols = tmem + lane_base + tmem_o(t);
         uint8_t* out_row =
             static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.nq + row) * (D * 2);
-#pragma unroll
-        for (int q = 0; q < D / 32; ++q) {
-            uint32_t o[32];
-            ptx::tmem_ld32(o_cols + q * 32, o);
+#pragma unroll 1
+        for (int q = 0; q < D / 16; ++q) {
+            uint32_t o[16];
+            ptx::tmem_ld16(o_cols + q * 16, o);
             ptx::tmem_wait_ld();
             ptx::reg_fence(o);
-            uint32_t packed[16];
+            uint32_t packed[8];
 #pragma unroll
-            for (int i = 0; i < 16; ++i)
+            for (int i = 0; i < 8; ++i)
                 packed[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
                                         __uint_as_float(o[2 * i + 1]) * inv_l);
             if (row < p.nq) {
-                uint4* dst = reinterpret_cast<uint4*>(out_row + q * 64);
-#pragma unroll
-                for (int v = 0; v < 4; ++v)
-                    dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                        packed[4 * v + 3]);
+                uint4* dst = reinterpret_cast<uint4*>(out_row + q * 32);
+                dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
+                dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
             }
         }
     }
@@ -391,20 +422,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // Work unit. Causal: the longest units first, spread over all slices; otherwise the units of
     // one slice are adjacent so its K/V stay hot in L2.
-    int bh, u;
+    int bh, u, split = 0;
     if constexpr (CAUSAL) {
         bh = blockIdx.x % p.bh;
         u = p.num_units - 1 - static_cast<int>(blockIdx.x / p.bh);
     } else {
         u = blockIdx.x % p.num_units;
-        bh = blockIdx.x / p.num_units;
+        const int rest = blockIdx.x / p.num_units;
+        split = rest % p.num_splits;
+        bh = rest / p.num_splits;
     }
     const int q0 = u * UNIT_ROWS;
     const int nkt = (p.nk + BN - 1) / BN;
+    // This CTA's key tiles: [kv0, kv0 + n_tiles[t]) for query tile t.
+    const int kv0 = split * p.kv_tiles_per_split;
     int n_tiles[Q_TILES];
 #pragma unroll
     for (int t = 0; t < Q_TILES; ++t)
-        n_tiles[t] = CAUSAL ? min(nkt, (q0 + t * BM + BM - 1) / BN + 1) : nkt;
+        n_tiles[t] = CAUSAL ? min(nkt, (q0 + t * BM + BM - 1) / BN + 1)
+                            : min(nkt - kv0, p.kv_tiles_per_split);
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;
@@ -462,13 +498,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::mbar_arrive_expect_tx(bar(L::B_K_FULL + st), L::KV_BYTES);
                     for (int c = 0; c < L::COL_BLOCKS; ++c)
                         ptx::tma_load_3d(sk + st * L::KV_BYTES + c * (BN * 128), &tm_k, c * 64,
-                                         j * BN, bh, bar(L::B_K_FULL + st));
+                                         (kv0 + j) * BN, bh, bar(L::B_K_FULL + st));
                     issued = 2 * j + 1;
                     if (!wait_bar(bar(L::B_V_EMPTY + st), ph ^ 1, ctl, SITE_LOAD_V_EMPTY)) break;
                     ptx::mbar_arrive_expect_tx(bar(L::B_V_FULL + st), L::KV_BYTES);
                     for (int c = 0; c < L::COL_BLOCKS; ++c)
                         ptx::tma_load_3d(sv + st * L::KV_BYTES + c * (BN * 128), &tm_v, c * 64,
-                                         j * BN, bh, bar(L::B_V_FULL + st));
+                                         (kv0 + j) * BN, bh, bar(L::B_V_FULL + st));
                     issued = 2 * j + 2;
                 }
                 if (*abort_flag) {
@@ -576,10 +612,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (wg == 2) {
         ptx::regs_dec<REG_EPILOGUE>();
-        epilogue_role<D, BF16>(tmem, sbase, rows, p, ctl, bh, q0);
+        epilogue_role<D, BF16>(tmem, sbase, rows, p, ctl, bh, q0, split);
     } else {
         ptx::regs_inc<REG_SOFTMAX>();
-        softmax_role<D, BF16, CAUSAL>(wg, tmem, sbase, rows, p, ctl, q0 + wg * BM, n_tiles[wg]);
+        softmax_role<D, BF16, CAUSAL>(wg, tmem, sbase, rows, p, ctl, q0 + wg * BM, kv0, n_tiles[wg]);
         ptx::tmem_wait_st();  // no TMEM store of this warp may be pending at dealloc
     }
 

@@ -1,0 +1,73 @@
+// fa_merge_kernel.cuh -- merge of partial attention states computed over disjoint key ranges.
+//
+// Each split s left, for every query row, the state of the online softmax over its keys:
+// m_s (reference maximum of the scaled scores, log2 units), l_s (sum of weights relative to
+// m_s) and o_s (unnormalised weighted sum of V rows). Two states over disjoint key sets merge as
+//   m = max(m_1, m_2),  l = l_1 2^(m_1 - m) + l_2 2^(m_2 - m),  o = o_1 2^(m_1 - m) + o_2 2^(m_2 - m)
+// ("11. Fusion, recompute, and flash attention", section 11.6, last paragraph, and exercise 3;
+// here in base 2, and folded over all splits at once). The answer is O = o / l, and the row's
+// log-sum-exp is (m + log2 l) ln 2.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+#include "sm103_ptx.cuh"
+
+namespace fa {
+
+// One warp per query row; lane i owns D/32 consecutive columns.
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__ o_part,
+                                                       const float* __restrict__ ml_part,
+                                                       void* __restrict__ o, float* __restrict__ lse,
+                                                       int64_t rows, int num_splits) {
+    constexpr int E = D / 32;
+    const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;
+    const float2* ml = reinterpret_cast<const float2*>(ml_part);
+    float m = -INFINITY;
+    for (int s = 0; s < num_splits; ++s) m = fmaxf(m, ml[s * rows + row].x);
+    float l = 0.f;
+    float acc[E];
+#pragma unroll
+    for (int e = 0; e < E; ++e) acc[e] = 0.f;
+    for (int s = 0; s < num_splits; ++s) {
+        const float2 st = ml[s * rows + row];
+        const float w = (st.x == -INFINITY) ? 0.f : ptx::ex2(st.x - m);
+        l += st.y * w;
+        const float* src = o_part + (s * rows + row) * D + lane * E;
+        if constexpr (E == 4) {
+            const float4 v = *reinterpret_cast<const float4*>(src);
+            acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
+        } else {
+            const float2 v = *reinterpret_cast<const float2*>(src);
+            acc[0] += w * v.x; acc[1] += w * v.y;
+        }
+    }
+    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    uint32_t packed[E / 2];
+#pragma unroll
+    for (int e = 0; e < E / 2; ++e) {
+        const float a = acc[2 * e] * inv_l, b = acc[2 * e + 1] * inv_l;
+        if constexpr (BF16) {
+            __nv_bfloat162 v = __floats2bfloat162_rn(a, b);
+            packed[e] = *reinterpret_cast<uint32_t*>(&v);
+        } else {
+            __half2 v = __floats2half2_rn(a, b);
+            packed[e] = *reinterpret_cast<uint32_t*>(&v);
+        }
+    }
+    uint8_t* dst = static_cast<uint8_t*>(o) + (row * D + lane * E) * 2;
+    if constexpr (E == 4) {
+        *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
+    } else {
+        *reinterpret_cast<uint32_t*>(dst) = packed[0];
+    }
+    if (lse != nullptr && lane == 0) lse[row] = (m + __log2f(l)) * 0.6931471805599453f;
+}
+
+}  // namespace fa

@@ -14,7 +14,8 @@ STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED",
           3: "FA_ERR_MISALIGNED", 4: "FA_ERR_CUDA", 5: "FA_ERR_TIMEOUT"}
 EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_error",
            "fa_status_string", "fa_last_error_message", "fa_fwd_noalloc",
-           "fa_set_rescale_threshold", "fa_get_rescale_threshold", "fa_fwd_lse")
+           "fa_set_rescale_threshold", "fa_get_rescale_threshold", "fa_fwd_lse",
+           "fa_splitkv_workspace_bytes", "fa_fwd_splitkv")
 
 
 class FaError(RuntimeError):
@@ -44,6 +45,11 @@ def lib() -> ctypes.CDLL:
     L.fa_fwd_noalloc.restype = ctypes.c_int
     L.fa_fwd_lse.argtypes = sig[:4] + [vp] + sig[4:]
     L.fa_fwd_lse.restype = ctypes.c_int
+    L.fa_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int]
+    L.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
+    L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float,
+                                 ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
+    L.fa_fwd_splitkv.restype = ctypes.c_int
     L.fa_release_host_buffers.argtypes = []
     L.fa_release_host_buffers.restype = ctypes.c_int
     L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
@@ -156,6 +162,39 @@ def forward_lse(q, k, v, causal: bool = False, scale: float | None = None, out=N
                                    lse.data_ptr(), B, H, Nq, Nk, D, float(scale),
                                    int(bool(causal)), code, stream.cuda_stream))
     return out, lse
+
+
+def splitkv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, D: int, num_splits: int = 0) -> int:
+    return int(lib().fa_splitkv_workspace_bytes(B, H, Nq, Nk, D, num_splits))
+
+
+def forward_splitkv(q, k, v, num_splits: int = 0, scale: float | None = None, out=None,
+                    lse=None, workspace=None, stream=None):
+    """Non-causal attention with the keys split into ranges and the partial states merged.
+    `workspace` (a CUDA tensor of at least splitkv_workspace_bytes bytes) is allocated here
+    when not given."""
+    import torch
+
+    B, H, Nq, Nk, D = _shape(q, k, v)
+    code = _dtype_code(q)
+    if not q.is_cuda:
+        raise ValueError("forward_splitkv() takes CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    need = splitkv_workspace_bytes(B, H, Nq, Nk, D, num_splits)
+    if workspace is None:
+        workspace = torch.empty(max(need, 1), dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        _raise_if(lib().fa_fwd_splitkv(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                       lse.data_ptr() if lse is not None else None, B, H, Nq, Nk,
+                                       D, float(scale), int(num_splits), code,
+                                       workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+                                       stream.cuda_stream))
+    return out
 
 
 def forward_host(q, k, v, out, causal: bool = False, scale: float | None = None, stream=None,

@@ -70,6 +70,9 @@ WORKLOADS = {
                  sigma_q=3.0, sigma_k=3.0),
         Workload("long_causal", 1, 16, 16384, 16384, 128, "bf16", True, seed=5),
         Workload("headline", 1, 32, 4096, 4096, 128, "bf16", False, seed=6),
+        # a 128-token chunk against a 64K-token context: one query block per head, so the keys
+        # are split across CTAs (flash-decoding)
+        Workload("long_context_chunk", 1, 8, 128, 65536, 128, "bf16", False, seed=7),
     ]
 }
 
