@@ -50,6 +50,24 @@ def env_rank():
             int(os.environ.get("WORLD_SIZE", 1)))
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest value of x across the ranks of the default process group (x itself when no
+    group is initialised). The timed region's length is the slowest rank's."""
+    import torch
+    import torch.distributed as dist
+
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return float(x)
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(flops_per_rank: float, world: int, seconds: float) -> float:
+    """Whole-job TFLOP/s: every rank runs its own replica of the workload (weak scaling)."""
+    return world * flops_per_rank / seconds / 1e12
+
+
 def workload_desc(w):
     return (f"{w.name}: B={w.B} H={w.H} Nq={w.Nq} Nk={w.Nk} D={w.D} {w.dtype} "
             f"{'causal' if w.causal else 'non-causal'}")
@@ -205,6 +223,8 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="headline")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--splits", type=int, default=0,
+                    help="key splits for workloads with few query blocks (0: automatic)")
     ap.add_argument("--ref-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
@@ -247,9 +267,22 @@ def main():
         sets.append((q, k, v, torch.empty_like(q)))
     stream = torch.cuda.current_stream(dev)
 
+    # Few query blocks per slice (a short chunk against a long context): split the keys across
+    # CTAs and merge (two launches per step).
+    use_split = (not w.causal) and w.B * w.H * -(-w.Nq // 256) < 152 and args.splits != 1
+    workspace = None
+    if use_split:
+        workspace = torch.empty(max(1, fa.splitkv_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.D,
+                                                                  args.splits)),
+                                dtype=torch.uint8, device=dev)
+
     def step(i):
         q, k, v, o = sets[i % n_sets]
-        fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=o, stream=stream)
+        if use_split:
+            fa.forward_splitkv(q, k, v, num_splits=args.splits, scale=w.scale, out=o,
+                               workspace=workspace, stream=stream)
+        else:
+            fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=o, stream=stream)
 
     # Warm-up, then about a second of the same work with the clock sampler already running,
     # so its samples describe the GPU under this load.
@@ -281,12 +314,9 @@ def main():
     if st != 0:
         raise RuntimeError(f"kernel error word set during the bench (site {site})")
 
-    if world > 1:
-        t = torch.tensor([ms_total], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms_total = float(t.item())
+    ms_total = max_over_ranks(ms_total, dev)
     ms_per_step = ms_total / args.steps
-    value = world * w.flops / (ms_per_step * 1e-3) / 1e12
+    value = job_throughput(w.flops, world, ms_per_step * 1e-3)
 
     if args.profile:
         if rank == 0:
@@ -303,11 +333,7 @@ def main():
     for _ in range(args.e2e_steps):
         fa.forward_host(qh, kh, vh, oh, causal=w.causal, scale=w.scale, stream=stream,
                         device=dev.index)
-    e2e_s = (time.perf_counter() - t0) / args.e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_s], device=dev, dtype=torch.float64)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_s = float(t.item())
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / args.e2e_steps, dev)
     h2d = sum(t.numel() * 2 for t in (qh, kh, vh))
     d2h = oh.numel() * 2
 
@@ -339,14 +365,15 @@ def main():
                    "parallelism": f"replicas{world}",
                    "l2": f"{n_sets} rotating input sets of {set_bytes / 2**20:.0f} MiB "
                          f"(> L2 between consecutive steps)",
-                   "pct_of_measured_peak": 100 * achieved / peak},
+                   "pct_of_measured_peak": 100 * achieved / peak,
+                   "key_splits": "auto" if use_split and args.splits == 0 else (args.splits if use_split else 1)},
         "roofline": roofline,
         "cpu_baseline": cpu,
-        "e2e": {"value": world * w.flops / e2e_s / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_throughput(w.flops, world, e2e_s), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
         "clocks": clocks,
-        "gpu_launches": args.steps,
+        "gpu_launches": args.steps * (2 if use_split else 1),
     }
     print(json.dumps(line), flush=True)
     if world > 1:
