@@ -74,6 +74,14 @@ typedef enum fa_status {
  * FA_OK means validated and launched; the result is ready once `stream` reaches this point.
  * The first call on a device allocates one 16-byte device word for kernel error reports
  * (kept until process exit); make that first call outside any stream capture.
+ *
+ * Last-wave balancing (non-causal): when the 256-row work units leave a last wave that fills at
+ * most half of the 152 SMs, those units are split over keys into 2-4 ranges and merged as in
+ * fa_fwd_splitkv (two launches). The partial states live in a device workspace owned by libfa:
+ * allocated the first time a shape needs it, grown when a later shape needs more, kept until
+ * process exit. Calls that might grow it must not run under stream capture; all calls on one
+ * device share it, so fa_fwd calls on different streams must be ordered. fa_set_tail_split(0)
+ * turns the balancing off (one launch, no workspace).
  */
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H,
                  int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, fa_dtype dtype,
@@ -184,6 +192,9 @@ fa_status fa_last_device_error(void* stream, int* site);
  */
 fa_status fa_set_rescale_threshold(float log2_threshold);
 float fa_get_rescale_threshold(void);
+
+/* Turn fa_fwd's last-wave balancing on (1, the default) or off (0). Process-wide. */
+fa_status fa_set_tail_split(int enable);
 
 /* A static, human-readable name for a status code. */
 const char* fa_status_string(fa_status status);

@@ -88,3 +88,28 @@ def test_workspace_checks(fa):
     assert call(ws.data_ptr() + 16, need - 16) in (1, 3)  # misaligned or too small
     assert call(ws.data_ptr(), need) == 0
     torch.cuda.synchronize()
+
+
+def test_last_wave_split_matches_oracle_and_unsplit(fa):
+    """40 heads x 8 units = 320 units: the last 16 (two heads) run split over keys."""
+    w = inputs.Workload("tail", 1, 40, 2048, 1024, 64, "bf16", False, seed=57)
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    lse = torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device="cuda")
+    o, _ = fa.forward_lse(q, k, v, scale=w.scale, lse=lse)
+    try:
+        fa.set_tail_split(False)
+        o_plain = fa.forward(q, k, v, scale=w.scale)
+    finally:
+        fa.set_tail_split(True)
+    torch.cuda.synchronize()
+    assert fa.last_device_error()[0] == 0
+    got = inputs.from_torch(o)
+    for h in (37, 38, 39):  # 37 runs whole, 38 and 39 split
+        ref, ref_lse = oracle.attention(*(inputs.bits_to_f64(bits[n][0, h], w.dtype) for n in "qkv"),
+                                        w.scale, False, with_lse=True)
+        parity.assert_parity(parity.compare(got[0, h], ref, w.dtype), True, f"head {h}")
+        assert np.max(np.abs(lse[0, h].cpu().numpy() - ref_lse)) <= LSE_TOL
+    diff = np.abs(inputs.bits_to_f64(got, "bf16") - inputs.bits_to_f64(inputs.from_torch(o_plain), "bf16"))
+    assert diff[0, :38].max() == 0.0  # whole units: identical bits
+    assert diff.max() <= 2e-2

@@ -18,6 +18,7 @@
 namespace {
 
 constexpr int MAX_DEVICES = 64;
+constexpr int64_t NUM_SMS = 152;  // GB300
 
 thread_local char g_msg[512] = "";
 
@@ -163,17 +164,21 @@ fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtens
             g_attr_set[dev] |= 1u << inst;
         }
     }
-    const unsigned grid = static_cast<unsigned>(p.num_units) * static_cast<unsigned>(p.bh) *
-                          static_cast<unsigned>(p.num_splits);
+    const unsigned grid = static_cast<unsigned>(p.split_begin) +
+                          static_cast<unsigned>(p.split_units) * static_cast<unsigned>(p.num_splits);
     kernel<<<grid, fa::NUM_THREADS, smem, stream>>>(mq, mk, mv, p);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return FA_OK;
 }
 
+// Key split of a launch: units [split_begin, split_begin + split_units) run as num_splits CTAs
+// each; the others run whole. The default splits nothing.
 struct Split {
     int num_splits = 1;
     int kv_tiles_per_split = 0;
+    int split_begin = -1;   // -1: no unit is split
+    int split_units = 0;
     float* o_part = nullptr;
     float* ml_part = nullptr;
 };
@@ -201,9 +206,13 @@ fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LS
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.rescale_threshold = g_rescale_threshold;
     p.timeout_ns = wait_timeout_ns();
-    p.num_splits = split.num_splits;
-    p.kv_tiles_per_split = split.num_splits > 1 ? split.kv_tiles_per_split
-                                                : static_cast<int>((Nk + fa::BN - 1) / fa::BN);
+    const int total_units = p.num_units * p.bh;
+    const bool splitting = split.split_begin >= 0 && split.split_units > 0 && split.num_splits > 1;
+    p.num_splits = splitting ? split.num_splits : 1;
+    p.kv_tiles_per_split = splitting ? split.kv_tiles_per_split
+                                     : static_cast<int>((Nk + fa::BN - 1) / fa::BN);
+    p.split_begin = splitting ? split.split_begin : total_units;
+    p.split_units = splitting ? split.split_units : 0;
     p.o_part = split.o_part;
     p.ml_part = split.ml_part;
     const bool bf16 = dtype == FA_BF16;
@@ -269,24 +278,118 @@ struct SplitPlan {
     int tiles_per_split;
 };
 
-SplitPlan plan_splits(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int requested) {
+SplitPlan plan_splits(int64_t units, int64_t Nk, int64_t want) {
     const int64_t nkt = (Nk + fa::BN - 1) / fa::BN;
-    int64_t want = requested;
-    if (want <= 0) {
-        // Automatic: enough CTAs to cover the SMs once.
-        const int64_t units = B * H * ((Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS);
-        want = units >= 152 ? 1 : (152 + units - 1) / units;
-    }
+    if (want <= 0) want = units >= NUM_SMS ? 1 : (NUM_SMS + units - 1) / units;  // cover the SMs
     want = want < 1 ? 1 : (want > nkt ? nkt : want);
     const int64_t per = (nkt + want - 1) / want;
     return SplitPlan{static_cast<int>((nkt + per - 1) / per), static_cast<int>(per)};
 }
 
-size_t workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t D, int splits) {
-    if (splits <= 1) return 0;
-    const size_t rows = size_t(B * H) * size_t(Nq);
+int64_t units_of(int64_t B, int64_t H, int64_t Nq) {
+    return B * H * ((Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS);
+}
+
+// Bytes of partial state for `split_units` units split `splits` ways.
+size_t workspace_bytes(int64_t split_units, int64_t Nq, int64_t D, int splits) {
+    if (splits <= 1 || split_units <= 0) return 0;
+    const size_t rows = size_t(split_units) * size_t(Nq < fa::UNIT_ROWS ? Nq : fa::UNIT_ROWS);
     const size_t o_bytes = (size_t(splits) * rows * size_t(D) * 4 + 255) & ~size_t(255);
     return o_bytes + size_t(splits) * rows * 8;
+}
+
+// Launch with the units [split_begin, split_begin + split_units) split over keys, then merge
+// their rows. `workspace` holds at least workspace_bytes(split_units, Nq, D, plan.num_splits).
+fa_status launch_split(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                       int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale,
+                       int dtype, cudaStream_t strm, const SplitPlan& plan, int64_t split_begin,
+                       int64_t split_units, void* workspace) {
+    const int64_t split_rows = Nq < fa::UNIT_ROWS ? Nq : fa::UNIT_ROWS;
+    const size_t rows = size_t(split_units) * size_t(split_rows);
+    Split sp;
+    sp.num_splits = plan.num_splits;
+    sp.kv_tiles_per_split = plan.tiles_per_split;
+    sp.split_begin = static_cast<int>(split_begin);
+    sp.split_units = static_cast<int>(split_units);
+    sp.o_part = static_cast<float*>(workspace);
+    sp.ml_part = reinterpret_cast<float*>(
+        static_cast<uint8_t*>(workspace) +
+        ((size_t(plan.num_splits) * rows * size_t(D) * 4 + 255) & ~size_t(255)));
+    fa_status s = launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, 0, dtype, strm, sp);
+    if (s != FA_OK) return s;
+    const fa::MergeMap map{static_cast<int>(split_begin),
+                           static_cast<int>((Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS),
+                           static_cast<int>(split_rows), static_cast<int>(Nq)};
+    const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
+    const int64_t nrows = static_cast<int64_t>(rows);
+    const bool bf16 = dtype == FA_BF16;
+    if (D == 128) {
+        if (bf16) fa::fa_merge_kernel<128, true><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
+        else fa::fa_merge_kernel<128, false><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
+    } else {
+        if (bf16) fa::fa_merge_kernel<64, true><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
+        else fa::fa_merge_kernel<64, false><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    return FA_OK;
+}
+
+// Last-wave balancing for fa_fwd / fa_fwd_lse (non-causal): when the units leave a partial
+// last wave of at most half the SMs, its units are split over keys so that the wave runs on
+// (about) all SMs for a fraction of the time. Returns false when nothing is worth splitting.
+bool plan_tail(int64_t units, int64_t Nk, SplitPlan* plan, int64_t* begin, int64_t* count) {
+    const int64_t tail = units % NUM_SMS;
+    if (units <= NUM_SMS || tail == 0 || tail > NUM_SMS / 2) return false;
+    const int64_t nkt = (Nk + fa::BN - 1) / fa::BN;
+    int64_t want = NUM_SMS / tail;
+    if (want > 4) want = 4;
+    if (nkt < 2 * want) return false;
+    *plan = plan_splits(tail, Nk, want);
+    if (plan->num_splits < 2) return false;
+    *begin = units - tail;
+    *count = tail;
+    return true;
+}
+
+struct Workspace {
+    void* buf = nullptr;
+    size_t bytes = 0;
+};
+Workspace g_workspace[MAX_DEVICES];
+bool g_tail_split = true;
+
+// The library's own workspace on the current device, grown to at least `bytes`.
+fa_status library_workspace(size_t bytes, void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    std::lock_guard<std::mutex> lock(g_mutex);
+    Workspace& w = g_workspace[dev];
+    if (w.bytes < bytes) {
+        if (w.buf) cudaFree(w.buf);
+        w = Workspace{};
+        if ((e = cudaMalloc(&w.buf, bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
+        w.bytes = bytes;
+    }
+    *out = w.buf;
+    return FA_OK;
+}
+
+// fa_fwd / fa_fwd_lse: one launch, or the last wave split over keys and merged.
+fa_status forward(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
+                  int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,
+                  int dtype, cudaStream_t strm) {
+    SplitPlan plan;
+    int64_t begin = 0, count = 0;
+    if (!causal && g_tail_split && plan_tail(units_of(B, H, Nq), Nk, &plan, &begin, &count)) {
+        void* ws = nullptr;
+        fa_status s = library_workspace(workspace_bytes(count, Nq, D, plan.num_splits), &ws);
+        if (s != FA_OK) return s;
+        return launch_split(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, dtype, strm, plan, begin,
+                            count, ws);
+    }
+    return launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, causal, dtype, strm);
 }
 
 }  // namespace
@@ -316,12 +419,14 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, i
     p.o = O;
     p.lse = nullptr;
     p.err = scratch;
-    p.num_splits = 1;
-    p.kv_tiles_per_split = static_cast<int>((Nk + fa::BN - 1) / fa::BN);
     p.bh = static_cast<int>(bh);
     p.nq = static_cast<int>(Nq);
     p.nk = static_cast<int>(Nk);
     p.num_units = static_cast<int>((Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS);
+    p.num_splits = 1;  // no key split: the whole computation stays in one launch
+    p.kv_tiles_per_split = static_cast<int>((Nk + fa::BN - 1) / fa::BN);
+    p.split_begin = p.num_units * p.bh;
+    p.split_units = 0;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.rescale_threshold = g_rescale_threshold;
     p.timeout_ns = wait_timeout_ns();
@@ -343,8 +448,8 @@ fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B
                  void* stream) {
     fa_status s = validate(Q, K, V, O, B, H, Nq, Nk, D, scale, causal, int(dtype), true);
     if (s != FA_OK) return s;
-    return launch(Q, K, V, O, nullptr, B, H, Nq, Nk, D, scale, causal, int(dtype),
-                  static_cast<cudaStream_t>(stream));
+    return forward(Q, K, V, O, nullptr, B, H, Nq, Nk, D, scale, causal, int(dtype),
+                   static_cast<cudaStream_t>(stream));
 }
 
 fa_status fa_fwd_lse(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
@@ -361,53 +466,42 @@ fa_status fa_fwd_lse(const void* Q, const void* K, const void* V, void* O, float
     if (overlaps(LSE, lse_bytes, O, q_bytes) || overlaps(LSE, lse_bytes, Q, q_bytes) ||
         overlaps(LSE, lse_bytes, K, kv_bytes) || overlaps(LSE, lse_bytes, V, kv_bytes))
         return fail(FA_ERR_INVALID_ARGUMENT, "LSE overlaps another tensor");
-    return launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, causal, int(dtype),
-                  static_cast<cudaStream_t>(stream));
+    return forward(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, causal, int(dtype),
+                   static_cast<cudaStream_t>(stream));
 }
 
-size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk,
-                                             int64_t D, int num_splits) {
+size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
+                                  int num_splits) {
     if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || D < 1) return 0;
-    return workspace_bytes(B, H, Nq, D, plan_splits(B, H, Nq, Nk, num_splits).num_splits);
+    const int64_t units = units_of(B, H, Nq);
+    return workspace_bytes(units, Nq, D, plan_splits(units, Nk, num_splits).num_splits);
 }
 
 fa_status fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
-                                    int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,
-                                    float scale, int num_splits, fa_dtype dtype, void* workspace,
-                                    size_t workspace_bytes_given, void* stream) {
+                         int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale,
+                         int num_splits, fa_dtype dtype, void* workspace,
+                         size_t workspace_bytes_given, void* stream) {
     fa_status s = validate(Q, K, V, O, B, H, Nq, Nk, D, scale, 0, int(dtype), true);
     if (s != FA_OK) return s;
     if (LSE && reinterpret_cast<uintptr_t>(LSE) % 4 != 0)
         return fail(FA_ERR_MISALIGNED, "LSE pointer is not 4-byte aligned");
-    const SplitPlan plan = plan_splits(B, H, Nq, Nk, num_splits);
+    const int64_t units = units_of(B, H, Nq);
+    const SplitPlan plan = plan_splits(units, Nk, num_splits);
     auto strm = static_cast<cudaStream_t>(stream);
     if (plan.num_splits <= 1) return launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, 0, int(dtype), strm);
-    const size_t need = workspace_bytes(B, H, Nq, D, plan.num_splits);
+    const size_t need = workspace_bytes(units, Nq, D, plan.num_splits);
     if (!workspace || workspace_bytes_given < need)
         return fail(FA_ERR_INVALID_ARGUMENT, "workspace of %zu bytes needed for %d splits (got %zu)",
                     need, plan.num_splits, workspace_bytes_given);
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
         return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
-    const size_t rows = size_t(B * H) * size_t(Nq);
-    Split sp;
-    sp.num_splits = plan.num_splits;
-    sp.kv_tiles_per_split = plan.tiles_per_split;
-    sp.o_part = static_cast<float*>(workspace);
-    sp.ml_part = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) +
-                                          ((size_t(plan.num_splits) * rows * size_t(D) * 4 + 255) & ~size_t(255)));
-    if ((s = launch(Q, K, V, O, nullptr, B, H, Nq, Nk, D, scale, 0, int(dtype), strm, sp)) != FA_OK)
-        return s;
-    const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
-    const bool bf16 = dtype == FA_BF16;
-    if (D == 128) {
-        if (bf16) fa::fa_merge_kernel<128, true><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, int64_t(rows), plan.num_splits);
-        else fa::fa_merge_kernel<128, false><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, int64_t(rows), plan.num_splits);
-    } else {
-        if (bf16) fa::fa_merge_kernel<64, true><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, int64_t(rows), plan.num_splits);
-        else fa::fa_merge_kernel<64, false><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, int64_t(rows), plan.num_splits);
-    }
-    cudaError_t e = cudaGetLastError();
-    if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
+    return launch_split(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, int(dtype), strm, plan, 0, units,
+                        workspace);
+}
+
+fa_status fa_set_tail_split(int enable) {
+    if (enable != 0 && enable != 1) return fail(FA_ERR_INVALID_ARGUMENT, "enable must be 0 or 1");
+    g_tail_split = enable != 0;
     return FA_OK;
 }
 
@@ -442,7 +536,7 @@ fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int6
         (e = cudaMemcpyAsync(dk, K, kv_bytes, cudaMemcpyHostToDevice, strm)) != cudaSuccess ||
         (e = cudaMemcpyAsync(dv, V, kv_bytes, cudaMemcpyHostToDevice, strm)) != cudaSuccess)
         return cuda_fail(e, "cudaMemcpyAsync(host to device)");
-    s = launch(dq, dk, dv, dout, nullptr, B, H, Nq, Nk, D, scale, causal, int(dtype), strm);
+    s = forward(dq, dk, dv, dout, nullptr, B, H, Nq, Nk, D, scale, causal, int(dtype), strm);
     if (s != FA_OK) return s;
     if ((e = cudaMemcpyAsync(O, dout, q_bytes, cudaMemcpyDeviceToHost, strm)) != cudaSuccess)
         return cuda_fail(e, "cudaMemcpyAsync(device to host)");

@@ -94,12 +94,16 @@ struct Params {
     int bh;                    // B * H
     int nq, nk;
     int num_units;             // ceil(nq / 256)
-    // Split over keys (non-causal only): CTA (unit, split) covers key tiles
-    // [split * kv_tiles_per_split, ...) and writes its unnormalised state, not O:
-    //   o_part [num_splits][bh][nq][D] fp32, ml_part [num_splits][bh][nq][2] fp32 (m in log2
-    //   units of the scaled scores, l relative to it). num_splits = 1: no split.
+    // Split over keys (non-causal only). Units are numbered bh * num_units + u. CTAs below
+    // split_begin run one whole unit each; the units from split_begin on run as num_splits CTAs
+    // each, CTA (unit, s) covering key tiles [s * kv_tiles_per_split, ...) and writing its
+    // unnormalised state instead of O, for split unit t = unit - split_begin and its row r:
+    //   o_part [num_splits][t][split_rows][D] fp32, ml_part [num_splits][t][split_rows][2]
+    //   fp32 (m in log2 units of the scaled scores, l relative to it), split_rows = min(256, nq).
     int num_splits;
     int kv_tiles_per_split;
+    int split_begin;
+    int split_units;
     float* o_part;
     float* ml_part;
     float scale_log2;          // scale * log2(e)
@@ -342,11 +346,14 @@ __device__ __forceinline__ void epilogue_role(uint32_t tmem, uint32_t sbase, con
         if (!wait_bar_warp(bar(L::B_L_READY + t), 0, ctl, SITE_EPI_L_READY)) return;
         const float l = rows[(1 * Q_TILES + t) * BM + r];
         const int row = q0 + t * BM + r;
-        if (p.num_splits > 1) {
+        if (split >= 0) {
             // Partial state over this CTA's keys, merged later (split over keys).
             if (!wait_bar_warp(bar(L::B_O_READY + t), 0, ctl, SITE_EPI_O_READY)) return;
             ptx::tc_fence_after();
-            const size_t prow = (static_cast<size_t>(split) * p.bh + bh) * p.nq + row;
+            const int split_rows = min(UNIT_ROWS, p.nq);
+            const int tu = bh * p.num_units + q0 / UNIT_ROWS - p.split_begin;
+            const size_t prow =
+                (static_cast<size_t>(split) * p.split_units + tu) * split_rows + (row - q0);
             const uint32_t o_cols = tmem + lane_base + tmem_o(t);
 #pragma unroll 1
             for (int q = 0; q < D / 16; ++q) {
@@ -422,25 +429,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     // Work unit. Causal: the longest units first, spread over all slices; otherwise the units of
     // one slice are adjacent so its K/V stay hot in L2.
-    int bh, u, split = 0;
+    int bh, u, split = -1;  // split < 0: the whole key range, O written directly
+    const int nkt = (p.nk + BN - 1) / BN;
     if constexpr (CAUSAL) {
         bh = blockIdx.x % p.bh;
         u = p.num_units - 1 - static_cast<int>(blockIdx.x / p.bh);
     } else {
-        u = blockIdx.x % p.num_units;
-        const int rest = blockIdx.x / p.num_units;
-        split = rest % p.num_splits;
-        bh = rest / p.num_splits;
+        int unit = blockIdx.x;
+        if (unit >= p.split_begin) {
+            const int idx = unit - p.split_begin;
+            unit = p.split_begin + idx / p.num_splits;
+            split = idx % p.num_splits;
+        }
+        u = unit % p.num_units;
+        bh = unit / p.num_units;
     }
     const int q0 = u * UNIT_ROWS;
-    const int nkt = (p.nk + BN - 1) / BN;
     // This CTA's key tiles: [kv0, kv0 + n_tiles[t]) for query tile t.
-    const int kv0 = split * p.kv_tiles_per_split;
+    const int kv0 = split < 0 ? 0 : split * p.kv_tiles_per_split;
     int n_tiles[Q_TILES];
 #pragma unroll
     for (int t = 0; t < Q_TILES; ++t)
         n_tiles[t] = CAUSAL ? min(nkt, (q0 + t * BM + BM - 1) / BN + 1)
-                            : min(nkt - kv0, p.kv_tiles_per_split);
+                            : (split < 0 ? nkt : min(nkt - kv0, p.kv_tiles_per_split));
 
     if (threadIdx.x == 0) {
         *abort_flag = 0;

@@ -18,16 +18,26 @@
 
 namespace fa {
 
-// One warp per query row; lane i owns D/32 consecutive columns.
+// Where the split units' rows live: split unit t is unit split_begin + t, numbered
+// bh * num_units + u, whose rows are u * 256 + r for r < split_rows = min(256, nq).
+struct MergeMap {
+    int split_begin, num_units, split_rows, nq;
+};
+
+// One warp per merged row; lane i owns D/32 consecutive columns.
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__ o_part,
                                                        const float* __restrict__ ml_part,
                                                        void* __restrict__ o, float* __restrict__ lse,
-                                                       int64_t rows, int num_splits) {
+                                                       int64_t rows, int num_splits, MergeMap map) {
     constexpr int E = D / 32;
     const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
+    const int64_t unit = map.split_begin + row / map.split_rows;
+    const int64_t q_row = (unit % map.num_units) * 256 + row % map.split_rows;
+    if (q_row >= map.nq) return;
+    const int64_t out_row = (unit / map.num_units) * map.nq + q_row;
     const float2* ml = reinterpret_cast<const float2*>(ml_part);
     float m = -INFINITY;
     for (int s = 0; s < num_splits; ++s) m = fmaxf(m, ml[s * rows + row].x);
@@ -61,13 +71,13 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__
             packed[e] = *reinterpret_cast<uint32_t*>(&v);
         }
     }
-    uint8_t* dst = static_cast<uint8_t*>(o) + (row * D + lane * E) * 2;
+    uint8_t* dst = static_cast<uint8_t*>(o) + (out_row * D + lane * E) * 2;
     if constexpr (E == 4) {
         *reinterpret_cast<uint2*>(dst) = make_uint2(packed[0], packed[1]);
     } else {
         *reinterpret_cast<uint32_t*>(dst) = packed[0];
     }
-    if (lse != nullptr && lane == 0) lse[row] = (m + __log2f(l)) * 0.6931471805599453f;
+    if (lse != nullptr && lane == 0) lse[out_row] = (m + __log2f(l)) * 0.6931471805599453f;
 }
 
 }  // namespace fa

@@ -15,7 +15,7 @@ STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED",
 EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_error",
            "fa_status_string", "fa_last_error_message", "fa_fwd_noalloc",
            "fa_set_rescale_threshold", "fa_get_rescale_threshold", "fa_fwd_lse",
-           "fa_splitkv_workspace_bytes", "fa_fwd_splitkv")
+           "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_set_tail_split")
 
 
 class FaError(RuntimeError):
@@ -50,6 +50,8 @@ def lib() -> ctypes.CDLL:
     L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float,
                                  ctypes.c_int, ctypes.c_int, vp, ctypes.c_size_t, vp]
     L.fa_fwd_splitkv.restype = ctypes.c_int
+    L.fa_set_tail_split.argtypes = [ctypes.c_int]
+    L.fa_set_tail_split.restype = ctypes.c_int
     L.fa_release_host_buffers.argtypes = []
     L.fa_release_host_buffers.restype = ctypes.c_int
     L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
@@ -232,6 +234,11 @@ def last_device_error(stream=None) -> tuple[int, int]:
 def set_rescale_threshold(log2_threshold: float) -> None:
     """Process-wide lazy-rescale threshold (log2 units; 0 = rescale on every rise)."""
     _raise_if(lib().fa_set_rescale_threshold(float(log2_threshold)))
+
+
+def set_tail_split(enable: bool) -> None:
+    """Turn the last-wave key split of forward() on or off (process-wide)."""
+    _raise_if(lib().fa_set_tail_split(int(bool(enable))))
 
 
 def get_rescale_threshold() -> float:
