@@ -15,6 +15,8 @@ Functions and the passages they follow (page title, section):
   "Flash Attention 2", "Overview of the algorithm".
 * ``online_state``     -- the unnormalised running state (m, l, o) of that recurrence.
 * ``merge_state``      -- section 11.6, merge of two partial states (exercise 3).
+* ``rope``             -- "Attention" (phobos stdlib docs), "Rotary position embeddings":
+  `rope` (rotate-half) and `rope_pairs` (interleaved pairs).
 
 Every function is pinned by ``tests/test_oracle.py`` against values the pages print, closed
 forms, invariants and brute force; none is "parity unpinned".
@@ -61,10 +63,11 @@ def load(path: Path | None = None) -> ctypes.CDLL:
                                        ctypes.c_double, _dp, _i64, _dp, _dp, _dp]
     lib.oracle_attention_online.argtypes = [_dp, _dp, _dp, _i64, _i64, _i64, _i64,
                                             ctypes.c_double, ctypes.c_int, _i64, _dp, _dp]
+    lib.oracle_rope.argtypes = [_dp, _dp, _dp, _i64, _i64, ctypes.c_int]
     lib.oracle_num_threads.argtypes = []
     for name in ("oracle_attention", "oracle_attention_rows", "oracle_softmax",
                  "oracle_online_state", "oracle_merge_state", "oracle_attention_online",
-                 "oracle_num_threads"):
+                 "oracle_rope", "oracle_num_threads"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -173,6 +176,17 @@ class Oracle:
                                            _ptr(o)), "merge_state")
         return m.value, l.value, o
 
+    def rope(self, x, cos_t, sin_t, form: int = 0) -> np.ndarray:
+        """Rotary embedding of x [..., rows, d] with per-row angle tables cos/sin [rows, d/2]
+        (form 0: rotate-half, 1: interleaved pairs). Returns a new array."""
+        x = np.array(x, dtype=np.float64, order="C", copy=True)
+        c, s_ = _f64(cos_t), _f64(sin_t)
+        *lead, rows, d = x.shape
+        flat = x.reshape(-1, rows, d)
+        for sl in flat:  # the same table for every leading index
+            _check(self.lib.oracle_rope(_ptr(sl), _ptr(c), _ptr(s_), rows, d, int(form)), "rope")
+        return flat.reshape(x.shape)
+
     def num_threads(self) -> int:
         return int(self.lib.oracle_num_threads())
 
@@ -204,6 +218,10 @@ def online_state(*a, **kw):
 
 def merge_state(*a, **kw):
     return default().merge_state(*a, **kw)
+
+
+def rope(*a, **kw):
+    return default().rope(*a, **kw)
 
 
 def num_threads() -> int:

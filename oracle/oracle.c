@@ -22,6 +22,8 @@
  *   [LSE]   "Flash Attention 2", "Write the data back to HBM": L = m + log l per row.
  *   [CAUSAL] section 11.6 exercises ("query i may only attend to keys j <= i") and the
  *           "Attention" page of the phobos stdlib docs, "Causal attention".
+ *   [ROPE]  the same "Attention" page, "Rotary position embeddings": `rope` (rotate-half) and
+ *           `rope_pairs` (interleaved pairs).
  *
  * Masking reading: a key that does not exist (j >= Nk) or that causal masking hides (j > i) is
  * left out of every maximum and sum; it is never given a sentinel score.
@@ -251,6 +253,34 @@ int oracle_attention_online(const double* q, const double* k, const double* v, i
         if (lse) lse[r] = m + log(l);
     }
     return status;
+}
+
+/*
+ * Rotary position embedding of rows of width d, in place [ROPE]:
+ *   form 0, rotate-half (phobos "Attention", `rope`): row = [a | b] with halves a, b of d/2;
+ *     a' = a cos - b sin,  b' = b cos + a sin   (element i of a pairs with element i of b)
+ *   form 1, interleaved pairs (`rope_pairs`): elements 2i and 2i+1 form the pair (x0, x1);
+ *     x0' = x0 cos - x1 sin,  x1' = x1 cos + x0 sin
+ * x: [rows][d]; cos_t, sin_t: [rows][d/2], the angle of pair i of each row. Both halves are read
+ * before either is written.
+ */
+int oracle_rope(double* x, const double* cos_t, const double* sin_t, int64_t rows, int64_t d,
+                int form) {
+    if (!x || !cos_t || !sin_t || rows < 0 || d < 2 || d % 2 != 0 || (form != 0 && form != 1))
+        return ORACLE_ERR_ARG;
+    const int64_t h = d / 2;
+    for (int64_t r = 0; r < rows; ++r) {
+        double* row = x + r * d;
+        for (int64_t i = 0; i < h; ++i) {
+            const int64_t i0 = (form == 0) ? i : 2 * i;
+            const int64_t i1 = (form == 0) ? i + h : 2 * i + 1;
+            const double x0 = row[i0], x1 = row[i1];
+            const double c = cos_t[r * h + i], sn = sin_t[r * h + i];
+            row[i0] = x0 * c - x1 * sn;
+            row[i1] = x1 * c + x0 * sn;
+        }
+    }
+    return ORACLE_OK;
 }
 
 /* Threads an OpenMP region of this library would use (1 without OpenMP). */

@@ -363,6 +363,72 @@ def pin_split_and_merge(orc):
     _close([mm, ll], [m, l], 0, 0, "merge with empty state")
 
 
+# --- rotary position embedding ------------------------------------------------------------------
+
+def _angles(rows, half, base=10000.0, offset=0):
+    """The usual RoPE angles: position p, pair i -> p * base^(-2i/d)."""
+    pos = np.arange(offset, offset + rows, dtype=np.float64)[:, None]
+    inv = base ** (-np.arange(half, dtype=np.float64) / half)
+    return pos * inv[None, :]
+
+
+def pin_rope_closed_forms(orc):
+    """Zero angle is the identity; a quarter turn sends each pair (a, b) to (-b, a); every
+    rotation keeps the length of each pair."""
+    rng = _rng(31)
+    x = rng.standard_normal((5, 8))
+    zeros, ones = np.zeros((5, 4)), np.ones((5, 4))
+    for form in (0, 1):
+        _close(orc.rope(x, ones, zeros, form), x, 0, 0, f"identity form {form}")
+        y = orc.rope(x, zeros, ones, form)
+        i0 = np.arange(4) if form == 0 else 2 * np.arange(4)
+        i1 = i0 + 4 if form == 0 else i0 + 1
+        _close(y[:, i0], -x[:, i1], 0, 0, f"quarter turn a, form {form}")
+        _close(y[:, i1], x[:, i0], 0, 0, f"quarter turn b, form {form}")
+        th = rng.uniform(-7, 7, (5, 4))
+        z = orc.rope(x, np.cos(th), np.sin(th), form)
+        _close(z[:, i0] ** 2 + z[:, i1] ** 2, x[:, i0] ** 2 + x[:, i1] ** 2, 1e-13, 1e-13,
+               f"pair norms form {form}")
+
+
+def pin_rope_composes(orc):
+    """Rotating by t1 then by t2 is rotating by t1 + t2."""
+    rng = _rng(32)
+    x = rng.standard_normal((6, 10))
+    t1, t2 = rng.uniform(-3, 3, (6, 5)), rng.uniform(-3, 3, (6, 5))
+    for form in (0, 1):
+        two = orc.rope(orc.rope(x, np.cos(t1), np.sin(t1), form), np.cos(t2), np.sin(t2), form)
+        one = orc.rope(x, np.cos(t1 + t2), np.sin(t1 + t2), form)
+        _close(two, one, 1e-13, 1e-13, f"composition form {form}")
+
+
+def pin_rope_relative_position(orc):
+    """With position-proportional angles, q_m . k_n depends only on m - n: shifting every
+    position by the same amount leaves all scores unchanged."""
+    rng = _rng(33)
+    q, k = rng.standard_normal((7, 16)), rng.standard_normal((9, 16))
+    for form in (0, 1):
+        s = []
+        for off in (0, 37):
+            aq, ak = _angles(7, 8, offset=off), _angles(9, 8, offset=off)
+            qr = orc.rope(q, np.cos(aq), np.sin(aq), form)
+            kr = orc.rope(k, np.cos(ak), np.sin(ak), form)
+            s.append(qr @ kr.T)
+        _close(s[0], s[1], 1e-10, 1e-10, f"relative position form {form}")
+
+
+def pin_rope_forms_are_a_permutation(orc):
+    """Interleaved pairs on x equal rotate-half on x with its columns reordered so that pair i
+    sits at (i, i + d/2)."""
+    rng = _rng(34)
+    x = rng.standard_normal((4, 12))
+    th = rng.uniform(-2, 2, (4, 6))
+    perm = np.concatenate([np.arange(0, 12, 2), np.arange(1, 12, 2)])
+    pairs = orc.rope(x, np.cos(th), np.sin(th), 1)
+    half = orc.rope(x[:, perm], np.cos(th), np.sin(th), 0)
+    _close(pairs[:, perm], half, 0, 0, "forms")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

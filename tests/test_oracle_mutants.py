@@ -37,6 +37,10 @@ MUTANTS = {
     "merge_o_sign": ("o[c] = o1[c] * f1 + o2[c] * f2;", "o[c] = o1[c] * f1 - o2[c] * f2;"),
     "lse_drops_max": ("if (lse) *lse = m + log(l);", "if (lse) *lse = log(l);"),
     "online_lse_drops_log": ("lse[r] = m + log(l);", "lse[r] = m + l;"),
+    "rope_sign": ("row[i0] = x0 * c - x1 * sn;", "row[i0] = x0 * c + x1 * sn;"),
+    "rope_half_offset": ("const int64_t i1 = (form == 0) ? i + h : 2 * i + 1;",
+                         "const int64_t i1 = (form == 0) ? i + h - 1 : 2 * i + 1;"),
+    "rope_in_place_overwrite": ("row[i1] = x1 * c + x0 * sn;", "row[i1] = x1 * c + row[i0] * sn;"),
     "rows_wrong_slice": ("int64_t h = r / nq, i = r % nq;\n            int rc = two_pass_row(q + r * d, k + h * nk * d",
                          "int64_t h = r / nq, i = r % nq;\n            int rc = two_pass_row(q + r * d, k"),
 }
