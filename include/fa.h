@@ -127,6 +127,34 @@ fa_status fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, f
                          void* stream);
 
 /*
+ * Rotary position embedding ("Attention", phobos stdlib docs, "Rotary position embeddings").
+ *
+ * fa_rope rotates every row of X [B, H, N, D] (16-bit `dtype`) pairwise and writes Y:
+ *   form 0, rotate-half: pair i of a row is (x_i, x_{i+D/2});
+ *   form 1, interleaved: pair i is (x_{2i}, x_{2i+1});
+ *   x0' = x0 cos - x1 sin,  x1' = x1 cos + x0 sin,
+ * with cos/sin of row n's pair i from the fp32 tables cos_t, sin_t [N][D/2] (shared by every
+ * batch and head: row n holds the angles of the position that row sits at). fp32 arithmetic,
+ * one rounding to `dtype`. Y may equal X (in place); otherwise they must not overlap. All
+ * pointers are device pointers, 16-byte aligned; D a multiple of 16 (at most 512).
+ *
+ * fa_fwd_rope runs attention on the rotated Q and K: it rotates Q (tables cos_q/sin_q [Nq][D/2])
+ * and K (cos_k/sin_k [Nk][D/2]) into `workspace` (caller-owned device memory, 256-byte aligned,
+ * at least fa_rope_workspace_bytes(B, H, Nq, Nk, D) bytes) and then computes fa_fwd_lse on
+ * them (LSE may be NULL). Q and K themselves are left unchanged. The rotation is a separate
+ * memory-bound pass in front of the attention kernel: K is read by every query block of its
+ * slice, so rotating it once is cheaper than rotating it inside each thread block.
+ */
+fa_status fa_rope(const void* X, void* Y, const float* cos_t, const float* sin_t, int64_t B,
+                  int64_t H, int64_t N, int64_t D, int form, fa_dtype dtype, void* stream);
+size_t fa_rope_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D);
+fa_status fa_fwd_rope(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                      const float* cos_q, const float* sin_q, const float* cos_k,
+                      const float* sin_k, int rope_form, int64_t B, int64_t H, int64_t Nq,
+                      int64_t Nk, int64_t D, float scale, int causal, fa_dtype dtype,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/*
  * fa_fwd_host -- the same operation on HOST buffers, synchronous.
  *
  * Q, K, V, O are host pointers with the layout above (pinned memory gives full copy speed).

@@ -1,0 +1,73 @@
+"""Rotary position embedding on the GPU against the fp64 oracle, alone and in front of attention.
+
+fa_rope computes in fp32 and rounds once to the 16-bit type, so each output is within one unit
+in the last place of the exactly rotated value (half an ulp of rounding plus fp32 error, which
+can tip a near-tie)."""
+import numpy as np
+import pytest
+
+import oracle
+from tests import parity
+from tiled_online_softmax_gb300 import inputs
+
+pytestmark = pytest.mark.gpu
+torch = pytest.importorskip("torch")
+
+
+@pytest.fixture(scope="module")
+def fa():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from tiled_online_softmax_gb300 import fa as fa_mod
+
+    fa_mod.lib()
+    return fa_mod
+
+
+def tables(n, d, offset=0, base=10000.0):
+    pos = np.arange(offset, offset + n, dtype=np.float64)[:, None]
+    ang = pos * base ** (-np.arange(d // 2, dtype=np.float64) / (d // 2))
+    return np.cos(ang).astype(np.float32), np.sin(ang).astype(np.float32)
+
+
+@pytest.mark.parametrize("form", [0, 1])
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("D", [64, 128])
+def test_rope_matches_oracle(fa, form, dtype, D):
+    w = inputs.Workload("rope", 2, 3, 257, 257, D, dtype, False, seed=61 + D + form)
+    x = inputs.draw(w)["q"]
+    c, s = tables(w.Nq, D, offset=5)
+    xt = inputs.to_torch(x, dtype).cuda()
+    ct, st = torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda()
+    y = fa.rope(xt, ct, st, form=form)
+    inplace = xt.clone()
+    fa.rope(inplace, ct, st, form=form, out=inplace)
+    torch.cuda.synchronize()
+    ref = oracle.rope(inputs.bits_to_f64(x, dtype), c.astype(np.float64), s.astype(np.float64),
+                      form)
+    got = inputs.bits_to_f64(inputs.from_torch(y), dtype)
+    assert np.all(np.abs(got - ref) <= parity.ulp(ref, dtype) + 1e-30)
+    assert torch.equal(y.view(torch.int16), inplace.view(torch.int16))
+
+
+@pytest.mark.parametrize("form", [0, 1])
+def test_attention_on_rotated_inputs(fa, form):
+    w = inputs.Workload("rope_attn", 1, 4, 300, 300, 128, "bf16", True, seed=71 + form)
+    bits = inputs.draw(w)
+    c, s = tables(w.Nq, w.D)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    ct, st = torch.from_numpy(c).cuda(), torch.from_numpy(s).cuda()
+    lse = torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device="cuda")
+    q_before = q.clone()
+    o = fa.forward_rope(q, k, v, ct, st, ct, st, form=form, causal=True, scale=w.scale, lse=lse)
+    torch.cuda.synchronize()
+    assert fa.last_device_error()[0] == 0
+    assert torch.equal(q.view(torch.int16), q_before.view(torch.int16))  # inputs untouched
+    c64, s64 = c.astype(np.float64), s.astype(np.float64)
+    rot = {n: inputs.bits_to_f64(inputs.round_to_bits(
+        oracle.rope(inputs.bits_to_f64(bits[n], "bf16"), c64, s64, form).astype(np.float32), "bf16"),
+        "bf16") for n in "qk"}
+    ref, ref_lse = oracle.attention(rot["q"], rot["k"], inputs.bits_to_f64(bits["v"], "bf16"),
+                                    w.scale, True, with_lse=True)
+    parity.assert_parity(parity.compare(inputs.from_torch(o), ref, "bf16"), False, "rope attention")
+    assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= 4e-3

@@ -14,6 +14,7 @@
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
 #include "fa_merge_kernel.cuh"
+#include "fa_rope_kernel.cuh"
 
 namespace {
 
@@ -392,6 +393,45 @@ fa_status forward(const void* Q, const void* K, const void* V, void* O, float* L
     return launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, causal, dtype, strm);
 }
 
+fa_status launch_rope(const void* X, void* Y, const float* cos_t, const float* sin_t,
+                      int64_t rows_total, int64_t n, int64_t D, int form, int dtype,
+                      cudaStream_t strm) {
+    const int64_t work = rows_total * (D / 16);
+    int64_t blocks = (work + 255) / 256;
+    if (blocks > 152 * 16) blocks = 152 * 16;
+    if (blocks < 1) blocks = 1;
+    auto x = static_cast<const uint16_t*>(X);
+    auto y = static_cast<uint16_t*>(Y);
+    const bool bf16 = dtype == FA_BF16;
+    const unsigned g = static_cast<unsigned>(blocks);
+    if (form == 0) {
+        if (bf16) fa::fa_rope_kernel<true, 0><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
+        else fa::fa_rope_kernel<false, 0><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
+    } else {
+        if (bf16) fa::fa_rope_kernel<true, 1><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
+        else fa::fa_rope_kernel<false, 1><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
+    }
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "rope kernel launch");
+    return FA_OK;
+}
+
+fa_status validate_rope(const void* X, const void* Y, const float* cos_t, const float* sin_t,
+                        int64_t rows_total, int64_t n, int64_t D, int form, int dtype) {
+    if (!X || !Y || !cos_t || !sin_t) return fail(FA_ERR_INVALID_ARGUMENT, "null pointer");
+    if (rows_total < 1 || n < 1 || D < 1) return fail(FA_ERR_INVALID_ARGUMENT, "sizes must be >= 1");
+    if (form != 0 && form != 1) return fail(FA_ERR_INVALID_ARGUMENT, "rope form must be 0 or 1");
+    if (dtype != FA_F16 && dtype != FA_BF16) return fail(FA_ERR_INVALID_ARGUMENT, "unknown dtype");
+    if (D % 16 != 0 || D > 512) return fail(FA_ERR_UNSUPPORTED, "rope needs D a multiple of 16, <= 512");
+    for (const void* p : {X, Y, static_cast<const void*>(cos_t), static_cast<const void*>(sin_t)})
+        if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
+            return fail(FA_ERR_MISALIGNED, "rope pointer %p is not 16-byte aligned", p);
+    const size_t x_bytes = size_t(rows_total) * size_t(D) * 2;
+    if (X != Y && overlaps(X, x_bytes, Y, x_bytes))
+        return fail(FA_ERR_INVALID_ARGUMENT, "rope output partially overlaps its input");
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -497,6 +537,49 @@ fa_status fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, f
         return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
     return launch_split(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, int(dtype), strm, plan, 0, units,
                         workspace);
+}
+
+fa_status fa_rope(const void* X, void* Y, const float* cos_t, const float* sin_t, int64_t B,
+                  int64_t H, int64_t N, int64_t D, int form, fa_dtype dtype, void* stream) {
+    if (B < 1 || H < 1) return fail(FA_ERR_INVALID_ARGUMENT, "sizes must be >= 1");
+    fa_status s = validate_rope(X, Y, cos_t, sin_t, B * H * N, N, D, form, int(dtype));
+    if (s != FA_OK) return s;
+    return launch_rope(X, Y, cos_t, sin_t, B * H * N, N, D, form, int(dtype),
+                       static_cast<cudaStream_t>(stream));
+}
+
+size_t fa_rope_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D) {
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || D < 1) return 0;
+    const size_t q = (size_t(B * H) * size_t(Nq) * size_t(D) * 2 + 255) & ~size_t(255);
+    return q + size_t(B * H) * size_t(Nk) * size_t(D) * 2;
+}
+
+fa_status fa_fwd_rope(const void* Q, const void* K, const void* V, void* O, float* LSE,
+                      const float* cos_q, const float* sin_q, const float* cos_k,
+                      const float* sin_k, int rope_form, int64_t B, int64_t H, int64_t Nq,
+                      int64_t Nk, int64_t D, float scale, int causal, fa_dtype dtype,
+                      void* workspace, size_t workspace_bytes_given, void* stream) {
+    fa_status s = validate(Q, K, V, O, B, H, Nq, Nk, D, scale, causal, int(dtype), true);
+    if (s != FA_OK) return s;
+    const size_t need = fa_rope_workspace_bytes(B, H, Nq, Nk, D);
+    if (!workspace || workspace_bytes_given < need)
+        return fail(FA_ERR_INVALID_ARGUMENT, "workspace of %zu bytes needed (got %zu)", need,
+                    workspace_bytes_given);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+        return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+    if (LSE && reinterpret_cast<uintptr_t>(LSE) % 4 != 0)
+        return fail(FA_ERR_MISALIGNED, "LSE pointer is not 4-byte aligned");
+    void* qr = workspace;
+    void* kr = static_cast<uint8_t*>(workspace) +
+               ((size_t(B * H) * size_t(Nq) * size_t(D) * 2 + 255) & ~size_t(255));
+    if ((s = validate_rope(Q, qr, cos_q, sin_q, B * H * Nq, Nq, D, rope_form, int(dtype))) != FA_OK ||
+        (s = validate_rope(K, kr, cos_k, sin_k, B * H * Nk, Nk, D, rope_form, int(dtype))) != FA_OK)
+        return s;
+    auto strm = static_cast<cudaStream_t>(stream);
+    if ((s = launch_rope(Q, qr, cos_q, sin_q, B * H * Nq, Nq, D, rope_form, int(dtype), strm)) != FA_OK ||
+        (s = launch_rope(K, kr, cos_k, sin_k, B * H * Nk, Nk, D, rope_form, int(dtype), strm)) != FA_OK)
+        return s;
+    return forward(qr, kr, V, O, LSE, B, H, Nq, Nk, D, scale, causal, int(dtype), strm);
 }
 
 fa_status fa_set_tail_split(int enable) {

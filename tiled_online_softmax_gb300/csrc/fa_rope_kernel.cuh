@@ -1,0 +1,97 @@
+// fa_rope_kernel.cuh -- rotary position embedding of 16-bit rows, the prologue of attention with
+// rotary positions ("Attention", phobos stdlib docs, "Rotary position embeddings").
+//
+//   form 0, rotate-half (`rope`): a row is [a | b], halves of D/2; pair i is (a_i, b_i).
+//   form 1, interleaved pairs (`rope_pairs`): pair i is (x_{2i}, x_{2i+1}).
+//   x0' = x0 cos - x1 sin,  x1' = x1 cos + x0 sin,  with cos/sin of row n's pair i taken from
+//   fp32 tables [N][D/2] (the same table for every batch and head).
+// Both elements of a pair are read before either is written, so in-place use is safe. The
+// arithmetic is fp32, rounded once to the 16-bit type. Memory-bound: each thread moves 8 pairs
+// (32 bytes of X, 64 bytes of tables) with 16-byte accesses.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include <cstdint>
+
+namespace fa {
+
+template <bool BF16>
+__device__ __forceinline__ float2 to_f2(uint32_t u) {
+    if constexpr (BF16) {
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    } else {
+        return __half22float2(*reinterpret_cast<const __half2*>(&u));
+    }
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint32_t from_f2(float lo, float hi) {
+    if constexpr (BF16) {
+        __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    } else {
+        __half2 v = __floats2half2_rn(lo, hi);
+        return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+// Grid-stride over (row, group of 8 pairs). x, y: [rows_total][d] (y may equal x);
+// cos_t, sin_t: [n][d/2], row r uses table row r % n.
+template <bool BF16, int FORM>
+__global__ void __launch_bounds__(256) fa_rope_kernel(const uint16_t* x, uint16_t* y,
+                                                      const float* __restrict__ cos_t,
+                                                      const float* __restrict__ sin_t,
+                                                      int64_t rows_total, int64_t n, int d) {
+    const int half = d / 2;
+    const int groups = half / 8;  // groups of 8 pairs per row
+    const int64_t total = rows_total * groups;
+    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
+         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t row = g / groups;
+        const int i0 = static_cast<int>(g % groups) * 8;  // first pair of the group
+        const float* ct = cos_t + (row % n) * half + i0;
+        const float* st = sin_t + (row % n) * half + i0;
+        const float4 c0 = *reinterpret_cast<const float4*>(ct);
+        const float4 c1 = *reinterpret_cast<const float4*>(ct + 4);
+        const float4 s0 = *reinterpret_cast<const float4*>(st);
+        const float4 s1 = *reinterpret_cast<const float4*>(st + 4);
+        const float cs[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+        const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
+        const uint16_t* src = x + row * d;
+        uint16_t* dst = y + row * d;
+        if constexpr (FORM == 0) {
+            // 8 elements of each half: a_i0.. and b_i0..
+            const uint4 a = *reinterpret_cast<const uint4*>(src + i0);
+            const uint4 b = *reinterpret_cast<const uint4*>(src + half + i0);
+            const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+            uint32_t ao[4], bo[4];
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const float2 fa = to_f2<BF16>(av[w]), fb = to_f2<BF16>(bv[w]);
+                const float c_lo = cs[2 * w], c_hi = cs[2 * w + 1];
+                const float s_lo = sn[2 * w], s_hi = sn[2 * w + 1];
+                ao[w] = from_f2<BF16>(fa.x * c_lo - fb.x * s_lo, fa.y * c_hi - fb.y * s_hi);
+                bo[w] = from_f2<BF16>(fb.x * c_lo + fa.x * s_lo, fb.y * c_hi + fa.y * s_hi);
+            }
+            *reinterpret_cast<uint4*>(dst + i0) = make_uint4(ao[0], ao[1], ao[2], ao[3]);
+            *reinterpret_cast<uint4*>(dst + half + i0) = make_uint4(bo[0], bo[1], bo[2], bo[3]);
+        } else {
+            // 16 consecutive elements = pairs i0..i0+7, one pair per 32-bit word
+            const uint4 p0 = *reinterpret_cast<const uint4*>(src + 2 * i0);
+            const uint4 p1 = *reinterpret_cast<const uint4*>(src + 2 * i0 + 8);
+            const uint32_t pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
+            uint32_t po[8];
+#pragma unroll
+            for (int w = 0; w < 8; ++w) {
+                const float2 f = to_f2<BF16>(pv[w]);
+                po[w] = from_f2<BF16>(f.x * cs[w] - f.y * sn[w], f.y * cs[w] + f.x * sn[w]);
+            }
+            *reinterpret_cast<uint4*>(dst + 2 * i0) = make_uint4(po[0], po[1], po[2], po[3]);
+            *reinterpret_cast<uint4*>(dst + 2 * i0 + 8) = make_uint4(po[4], po[5], po[6], po[7]);
+        }
+    }
+}
+
+}  // namespace fa

@@ -15,7 +15,8 @@ STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED",
 EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_error",
            "fa_status_string", "fa_last_error_message", "fa_fwd_noalloc",
            "fa_set_rescale_threshold", "fa_get_rescale_threshold", "fa_fwd_lse",
-           "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_set_tail_split")
+           "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_set_tail_split", "fa_rope",
+           "fa_rope_workspace_bytes", "fa_fwd_rope")
 
 
 class FaError(RuntimeError):
@@ -52,6 +53,14 @@ def lib() -> ctypes.CDLL:
     L.fa_fwd_splitkv.restype = ctypes.c_int
     L.fa_set_tail_split.argtypes = [ctypes.c_int]
     L.fa_set_tail_split.restype = ctypes.c_int
+    L.fa_rope.argtypes = [vp, vp, vp, vp, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int, vp]
+    L.fa_rope.restype = ctypes.c_int
+    L.fa_rope_workspace_bytes.argtypes = [i64, i64, i64, i64, i64]
+    L.fa_rope_workspace_bytes.restype = ctypes.c_size_t
+    L.fa_fwd_rope.argtypes = [vp, vp, vp, vp, vp, vp, vp, vp, vp, ctypes.c_int, i64, i64, i64,
+                              i64, i64, ctypes.c_float, ctypes.c_int, ctypes.c_int, vp,
+                              ctypes.c_size_t, vp]
+    L.fa_fwd_rope.restype = ctypes.c_int
     L.fa_release_host_buffers.argtypes = []
     L.fa_release_host_buffers.restype = ctypes.c_int
     L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
@@ -196,6 +205,53 @@ def forward_splitkv(q, k, v, num_splits: int = 0, scale: float | None = None, ou
                                        D, float(scale), int(num_splits), code,
                                        workspace.data_ptr(), workspace.numel() * workspace.element_size(),
                                        stream.cuda_stream))
+    return out
+
+
+def rope(x, cos_t, sin_t, form: int = 0, out=None, stream=None):
+    """Rotary embedding of x [B, H, N, D] (CUDA, 16-bit) with fp32 tables [N, D/2]; returns out
+    (pass out=x to rotate in place)."""
+    import torch
+
+    if x.dim() != 4 or not x.is_cuda or not x.is_contiguous():
+        raise ValueError("x must be a contiguous CUDA tensor [B, H, N, D]")
+    B, H, N, D = x.shape
+    for t in (cos_t, sin_t):
+        if t.dtype != torch.float32 or tuple(t.shape) != (N, D // 2) or not t.is_contiguous():
+            raise ValueError("cos/sin tables must be contiguous float32 [N, D/2]")
+    if out is None:
+        out = torch.empty_like(x)
+    if stream is None:
+        stream = torch.cuda.current_stream(x.device)
+    with torch.cuda.device(x.device):
+        _raise_if(lib().fa_rope(x.data_ptr(), out.data_ptr(), cos_t.data_ptr(), sin_t.data_ptr(),
+                                B, H, N, D, int(form), _dtype_code(x), stream.cuda_stream))
+    return out
+
+
+def forward_rope(q, k, v, cos_q, sin_q, cos_k, sin_k, form: int = 0, causal: bool = False,
+                 scale: float | None = None, out=None, lse=None, workspace=None, stream=None):
+    """Attention on rotary-embedded q and k (the rotation runs on device copies)."""
+    import torch
+
+    B, H, Nq, Nk, D = _shape(q, k, v)
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    if out is None:
+        out = torch.empty_like(q)
+    need = int(lib().fa_rope_workspace_bytes(B, H, Nq, Nk, D))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        _raise_if(lib().fa_fwd_rope(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                    lse.data_ptr() if lse is not None else None,
+                                    cos_q.data_ptr(), sin_q.data_ptr(), cos_k.data_ptr(),
+                                    sin_k.data_ptr(), int(form), B, H, Nq, Nk, D, float(scale),
+                                    int(bool(causal)), code, workspace.data_ptr(),
+                                    workspace.numel(), stream.cuda_stream))
     return out
 
 
