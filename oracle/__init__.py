@@ -15,6 +15,8 @@ Functions and the passages they follow (page title, section):
   "Flash Attention 2", "Overview of the algorithm".
 * ``online_state``     -- the unnormalised running state (m, l, o) of that recurrence.
 * ``merge_state``      -- section 11.6, merge of two partial states (exercise 3).
+* ``attention_backward`` -- dQ, dK, dV of the definition (section 11.9, "Backward"; the pages
+  print no formulas, so this is the plain derivative of section 11.2's definition).
 * ``rope``             -- "Attention" (phobos stdlib docs), "Rotary position embeddings":
   `rope` (rotate-half) and `rope_pairs` (interleaved pairs).
 
@@ -64,10 +66,12 @@ def load(path: Path | None = None) -> ctypes.CDLL:
     lib.oracle_attention_online.argtypes = [_dp, _dp, _dp, _i64, _i64, _i64, _i64,
                                             ctypes.c_double, ctypes.c_int, _i64, _dp, _dp]
     lib.oracle_rope.argtypes = [_dp, _dp, _dp, _i64, _i64, ctypes.c_int]
+    lib.oracle_attention_backward.argtypes = [_dp, _dp, _dp, _dp, _i64, _i64, _i64, _i64,
+                                              ctypes.c_double, ctypes.c_int, _dp, _dp, _dp]
     lib.oracle_num_threads.argtypes = []
     for name in ("oracle_attention", "oracle_attention_rows", "oracle_softmax",
                  "oracle_online_state", "oracle_merge_state", "oracle_attention_online",
-                 "oracle_rope", "oracle_num_threads"):
+                 "oracle_rope", "oracle_attention_backward", "oracle_num_threads"):
         getattr(lib, name).restype = ctypes.c_int
     return lib
 
@@ -176,6 +180,19 @@ class Oracle:
                                            _ptr(o)), "merge_state")
         return m.value, l.value, o
 
+    def attention_backward(self, q, k, v, dout, scale: float, causal: bool = False):
+        """(dQ, dK, dV) of O = softmax(scale q k^T) v for the upstream gradient dout."""
+        q, k, v, dout = _f64(q), _f64(k), _f64(v), _f64(dout)
+        *lead, nq, d = q.shape
+        nk = k.shape[-2]
+        bh = int(np.prod(lead)) if lead else 1
+        dq, dk, dv = np.empty(q.shape), np.empty(k.shape), np.empty(v.shape)
+        _check(self.lib.oracle_attention_backward(_ptr(q), _ptr(k), _ptr(v), _ptr(dout), bh, nq,
+                                                  nk, d, float(scale), int(bool(causal)),
+                                                  _ptr(dq), _ptr(dk), _ptr(dv)),
+               "attention_backward")
+        return dq, dk, dv
+
     def rope(self, x, cos_t, sin_t, form: int = 0) -> np.ndarray:
         """Rotary embedding of x [..., rows, d] with per-row angle tables cos/sin [rows, d/2]
         (form 0: rotate-half, 1: interleaved pairs). Returns a new array."""
@@ -222,6 +239,10 @@ def merge_state(*a, **kw):
 
 def rope(*a, **kw):
     return default().rope(*a, **kw)
+
+
+def attention_backward(*a, **kw):
+    return default().attention_backward(*a, **kw)
 
 
 def num_threads() -> int:

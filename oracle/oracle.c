@@ -22,6 +22,8 @@
  *   [LSE]   "Flash Attention 2", "Write the data back to HBM": L = m + log l per row.
  *   [CAUSAL] section 11.6 exercises ("query i may only attend to keys j <= i") and the
  *           "Attention" page of the phobos stdlib docs, "Causal attention".
+ *   [BWD]   same chapter, section 11.9 ("Backward") and exercise "Backward with recompute":
+ *           gradients from Q, K, V, dO with P recomputed.
  *   [ROPE]  the same "Attention" page, "Rotary position embeddings": `rope` (rotate-half) and
  *           `rope_pairs` (interleaved pairs).
  *
@@ -251,6 +253,70 @@ int oracle_attention_online(const double* q, const double* k, const double* v, i
         }
         for (int64_t c = 0; c < d; ++c) o[c] = o[c] / l;
         if (lse) lse[r] = m + log(l);
+    }
+    return status;
+}
+
+/*
+ * Gradients of the attention forward [BWD]. With P = softmax(scale * Q K^T) row by row (hidden
+ * keys have P = 0) and O = P V, and an upstream gradient dO of the loss with respect to O:
+ *   dV = P^T dO
+ *   dP = dO V^T
+ *   dS = P * (dP - rowsum(dO * O))        (elementwise; rowsum over the head dimension)
+ *   dQ = scale * dS K,   dK = scale * dS^T Q
+ * The pages name the backward pass and its recompute of P from Q, K and the log-sum-exp, but
+ * print no formulas; these are the derivative of the forward definition [DEF], taken plainly.
+ *   q, dout: [bh][nq][d]; k, v: [bh][nk][d]; dq: [bh][nq][d]; dk, dv: [bh][nk][d].
+ */
+int oracle_attention_backward(const double* q, const double* k, const double* v,
+                              const double* dout, int64_t bh, int64_t nq, int64_t nk, int64_t d,
+                              double scale, int causal, double* dq, double* dk, double* dv) {
+    if (!q || !k || !v || !dout || !dq || !dk || !dv || bh < 1 || nq < 1 || nk < 1 || d < 1)
+        return ORACLE_ERR_ARG;
+    int status = ORACLE_OK;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t h = 0; h < bh; ++h) {
+        const double* qh = q + h * nq * d;
+        const double* kh = k + h * nk * d;
+        const double* vh = v + h * nk * d;
+        const double* doh = dout + h * nq * d;
+        double* dqh = dq + h * nq * d;
+        double* dkh = dk + h * nk * d;
+        double* dvh = dv + h * nk * d;
+        double* p = (double*)calloc((size_t)(nq * nk), sizeof(double));
+        double* s = (double*)malloc((size_t)nk * sizeof(double));
+        double* o = (double*)malloc((size_t)d * sizeof(double));
+        if (!p || !s || !o) {
+            free(p); free(s); free(o);
+#pragma omp atomic write
+            status = ORACLE_ERR_NOMEM;
+            continue;
+        }
+        for (int64_t i = 0; i < nq * d; ++i) dqh[i] = 0.0;
+        for (int64_t i = 0; i < nk * d; ++i) dkh[i] = dvh[i] = 0.0;
+        for (int64_t i = 0; i < nq; ++i) {
+            const int64_t n = visible_keys(i, nk, causal);
+            int rc = two_pass_row(qh + i * d, kh, vh, n, d, scale, s, o, NULL, p + i * nk);
+            if (rc != ORACLE_OK) {
+#pragma omp atomic write
+                status = rc;
+                break;
+            }
+            double delta = 0.0;  /* rowsum(dO * O) */
+            for (int64_t c = 0; c < d; ++c) delta += doh[i * d + c] * o[c];
+            for (int64_t j = 0; j < n; ++j) {
+                const double pij = p[i * nk + j];
+                double dp = 0.0;
+                for (int64_t c = 0; c < d; ++c) dp += doh[i * d + c] * vh[j * d + c];
+                const double ds = pij * (dp - delta);
+                for (int64_t c = 0; c < d; ++c) {
+                    dvh[j * d + c] += pij * doh[i * d + c];
+                    dqh[i * d + c] += scale * ds * kh[j * d + c];
+                    dkh[j * d + c] += scale * ds * qh[i * d + c];
+                }
+            }
+        }
+        free(p); free(s); free(o);
     }
     return status;
 }

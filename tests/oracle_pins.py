@@ -429,6 +429,60 @@ def pin_rope_forms_are_a_permutation(orc):
     _close(pairs[:, perm], half, 0, 0, "forms")
 
 
+# --- backward ------------------------------------------------------------------------------------
+
+def pin_backward_finite_differences(orc):
+    """Each gradient element matches the central difference of L = sum(dO * O) computed by the
+    oracle's own forward pass."""
+    rng = _rng(41)
+    for causal, (nq, nk, d) in ((False, (4, 6, 3)), (True, (5, 5, 2)), (True, (3, 7, 3))):
+        q, k, v = (rng.standard_normal((n, d)) for n in (nq, nk, nk))
+        do = rng.standard_normal((nq, d))
+        dq, dk, dv = orc.attention_backward(q, k, v, do, 0.7, causal)
+        h = 1e-6
+
+        def loss(qq, kk, vv):
+            return float(np.sum(do * orc.attention(qq, kk, vv, 0.7, causal)))
+
+        for name, x, g in (("q", q, dq), ("k", k, dk), ("v", v, dv)):
+            num = np.zeros_like(x)
+            for idx in np.ndindex(x.shape):
+                xp, xm = x.copy(), x.copy()
+                xp[idx] += h
+                xm[idx] -= h
+                args_p = {"q": q, "k": k, "v": v}
+                args_m = dict(args_p)
+                args_p[name], args_m[name] = xp, xm
+                num[idx] = (loss(args_p["q"], args_p["k"], args_p["v"]) -
+                            loss(args_m["q"], args_m["k"], args_m["v"])) / (2 * h)
+            _close(g, num, 1e-6, 1e-8, f"d{name} causal={causal}")
+
+
+def pin_backward_constant_values(orc):
+    """When every row of V is the same vector, O does not depend on Q or K: dQ = dK = 0, and
+    dV distributes dO by the attention weights (uniform when q = 0)."""
+    rng = _rng(42)
+    q, k = rng.standard_normal((6, 4)), rng.standard_normal((8, 4))
+    v = np.repeat(rng.standard_normal((1, 4)), 8, 0)
+    do = rng.standard_normal((6, 4))
+    for causal in (False, True):
+        dq, dk, dv = orc.attention_backward(q, k, v, do, 0.5, causal)
+        _close(dq, np.zeros_like(dq), 0, 1e-13, "dq with constant V")
+        _close(dk, np.zeros_like(dk), 0, 1e-13, "dk with constant V")
+    _, _, dv = orc.attention_backward(np.zeros((6, 4)), k, rng.standard_normal((8, 4)), do, 0.5)
+    _close(dv, np.repeat(do.sum(0, keepdims=True) / 8, 8, 0), 1e-13, 1e-13, "dv uniform")
+
+
+def pin_backward_key_shift_gradient_sums_to_zero(orc):
+    """Moving every key by the same vector leaves O unchanged, so the key gradients sum to 0."""
+    rng = _rng(43)
+    q, k, v = rng.standard_normal((7, 5)), rng.standard_normal((9, 5)), rng.standard_normal((9, 5))
+    do = rng.standard_normal((7, 5))
+    for causal in (False, True):
+        _, dk, _ = orc.attention_backward(q, k, v, do, 0.9, causal)
+        _close(dk.sum(0), np.zeros(5), 0, 1e-12, f"sum dk causal={causal}")
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
 
 

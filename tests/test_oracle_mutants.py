@@ -41,6 +41,10 @@ MUTANTS = {
     "rope_half_offset": ("const int64_t i1 = (form == 0) ? i + h : 2 * i + 1;",
                          "const int64_t i1 = (form == 0) ? i + h - 1 : 2 * i + 1;"),
     "rope_in_place_overwrite": ("row[i1] = x1 * c + x0 * sn;", "row[i1] = x1 * c + row[i0] * sn;"),
+    "bwd_delta_sign": ("const double ds = pij * (dp - delta);", "const double ds = pij * (dp + delta);"),
+    "bwd_dq_no_scale": ("dqh[i * d + c] += scale * ds * kh[j * d + c];", "dqh[i * d + c] += ds * kh[j * d + c];"),
+    "bwd_dv_uses_dq_row": ("dvh[j * d + c] += pij * doh[i * d + c];", "dvh[j * d + c] += pij * doh[j % nq * d + c];"),
+    "bwd_dk_uses_k": ("dkh[j * d + c] += scale * ds * qh[i * d + c];", "dkh[j * d + c] += scale * ds * kh[j * d + c];"),
     "rows_wrong_slice": ("int64_t h = r / nq, i = r % nq;\n            int rc = two_pass_row(q + r * d, k + h * nk * d",
                          "int64_t h = r / nq, i = r % nq;\n            int rc = two_pass_row(q + r * d, k"),
 }
