@@ -155,6 +155,31 @@ fa_status fa_fwd_rope(const void* Q, const void* K, const void* V, void* O, floa
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /*
+ * fa_bwd -- gradients of the forward pass, by recompute ("11. Fusion, recompute, and flash
+ * attention", section 11.9 "Backward" and the exercise "Backward with recompute"): the forward
+ * keeps only O and the per-row log-sum-exp; P is recomputed tile by tile from Q, K and LSE.
+ * With P = exp(scale Q K^T - LSE) and D_i = sum_d dO_i O_i:
+ *   dV = P^T dO,  dS = P * (dO V^T - D),  dQ = scale dS K,  dK = scale dS^T Q.
+ *
+ *   Q, K, V    the forward's inputs ([B,H,Nq,D], [B,H,Nk,D], [B,H,Nk,D], 16-bit `dtype`)
+ *   O, LSE     the forward's outputs (fa_fwd_lse): [B,H,Nq,D] and fp32 [B,H,Nq]
+ *   dO         gradient of the loss with respect to O, [B,H,Nq,D]
+ *   dQ, dK, dV written, shaped like Q, K, V; they must not overlap any input or each other
+ *   scale, causal, dtype as in the forward call that produced O and LSE
+ *   workspace  caller-owned device memory, 256-byte aligned, at least
+ *              fa_bwd_workspace_bytes(B, H, Nq) bytes (per-row D_i and base-2 LSE)
+ * Device pointers, 16-byte aligned (LSE 4-byte). Three launches on `stream`: a per-row
+ * preprocessing kernel, a key-block-outer kernel for dK and dV, a query-block-outer kernel
+ * for dQ (no atomics: results do not depend on scheduling). Accumulation is fp32; P and dS
+ * are rounded to `dtype` as MMA operands; outputs are rounded once.
+ */
+size_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq);
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, int64_t B, int64_t H, int64_t Nq,
+                 int64_t Nk, int64_t D, float scale, int causal, fa_dtype dtype, void* workspace,
+                 size_t workspace_bytes, void* stream);
+
+/*
  * fa_fwd_host -- the same operation on HOST buffers, synchronous.
  *
  * Q, K, V, O are host pointers with the layout above (pinned memory gives full copy speed).

@@ -15,6 +15,7 @@
 #include "fa_fwd_kernel.cuh"
 #include "fa_merge_kernel.cuh"
 #include "fa_rope_kernel.cuh"
+#include "fa_bwd_kernel.cuh"
 
 namespace {
 
@@ -432,6 +433,34 @@ fa_status validate_rope(const void* X, const void* Y, const float* cos_t, const 
     return FA_OK;
 }
 
+template <int D, bool BF16, bool CAUSAL>
+fa_status launch_bwd_instance(int dev, const CUtensorMap& mq, const CUtensorMap& mk,
+                              const CUtensorMap& mv, const CUtensorMap& mdo, const fa::BwdParams& p,
+                              cudaStream_t strm) {
+    constexpr int smem = fa::BwdSmem<D>::ALLOC_BYTES;
+    auto k_kv = fa::fa_bwd_dkdv_kernel<D, BF16, CAUSAL>;
+    auto k_q = fa::fa_bwd_dq_kernel<D, BF16, CAUSAL>;
+    static unsigned attr_set[MAX_DEVICES] = {};  // one per template instance
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if (!attr_set[dev]) {
+            cudaError_t e;
+            if ((e = cudaFuncSetAttribute(k_kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
+                (e = cudaFuncSetAttribute(k_q, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+                return cuda_fail(e, "cudaFuncSetAttribute(backward)");
+            attr_set[dev] = 1;
+        }
+    }
+    const unsigned nkb = static_cast<unsigned>((p.nk + 127) / 128);
+    const unsigned nqb = static_cast<unsigned>((p.nq + 127) / 128);
+    k_kv<<<nkb * static_cast<unsigned>(p.bh), fa::BWD_THREADS, smem, strm>>>(mq, mk, mv, mdo, p);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
+    k_q<<<nqb * static_cast<unsigned>(p.bh), fa::BWD_THREADS, smem, strm>>>(mq, mk, mv, mdo, p);
+    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "backward dQ launch");
+    return FA_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -580,6 +609,96 @@ fa_status fa_fwd_rope(const void* Q, const void* K, const void* V, void* O, floa
         (s = launch_rope(K, kr, cos_k, sin_k, B * H * Nk, Nk, D, rope_form, int(dtype), strm)) != FA_OK)
         return s;
     return forward(qr, kr, V, O, LSE, B, H, Nq, Nk, D, scale, causal, int(dtype), strm);
+}
+
+size_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq) {
+    if (B < 1 || H < 1 || Nq < 1) return 0;
+    const size_t nq_pad = size_t((Nq + 127) / 128) * 128;
+    return 2 * ((size_t(B * H) * nq_pad * 4 + 255) & ~size_t(255));
+}
+
+fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, const void* dO,
+                 const float* LSE, void* dQ, void* dK, void* dV, int64_t B, int64_t H, int64_t Nq,
+                 int64_t Nk, int64_t D, float scale, int causal, fa_dtype dtype, void* workspace,
+                 size_t workspace_bytes_given, void* stream) {
+    fa_status s = validate(Q, K, V, dQ, B, H, Nq, Nk, D, scale, causal, int(dtype), true);
+    if (s != FA_OK) return s;
+    if (!O || !dO || !LSE || !dK || !dV) return fail(FA_ERR_INVALID_ARGUMENT, "null tensor pointer");
+    for (const void* ptr : {O, dO, static_cast<const void*>(dK), static_cast<const void*>(dV)})
+        if (reinterpret_cast<uintptr_t>(ptr) % 16 != 0)
+            return fail(FA_ERR_MISALIGNED, "tensor pointer %p is not 16-byte aligned", ptr);
+    if (reinterpret_cast<uintptr_t>(LSE) % 4 != 0) return fail(FA_ERR_MISALIGNED, "LSE is not 4-byte aligned");
+    const size_t qb = size_t(B * H) * size_t(Nq) * size_t(D) * 2, kb = size_t(B * H) * size_t(Nk) * size_t(D) * 2;
+    const void* ins[] = {Q, K, V, O, dO, LSE};
+    const size_t in_bytes[] = {qb, kb, kb, qb, qb, size_t(B * H) * size_t(Nq) * 4};
+    const void* outs[] = {dQ, dK, dV};
+    const size_t out_bytes[] = {qb, kb, kb};
+    for (int a = 0; a < 3; ++a) {
+        for (int b = 0; b < 6; ++b)
+            if (overlaps(outs[a], out_bytes[a], ins[b], in_bytes[b]))
+                return fail(FA_ERR_INVALID_ARGUMENT, "a gradient output overlaps an input");
+        for (int b = a + 1; b < 3; ++b)
+            if (overlaps(outs[a], out_bytes[a], outs[b], out_bytes[b]))
+                return fail(FA_ERR_INVALID_ARGUMENT, "gradient outputs overlap");
+    }
+    const size_t need = fa_bwd_workspace_bytes(B, H, Nq);
+    if (!workspace || workspace_bytes_given < need)
+        return fail(FA_ERR_INVALID_ARGUMENT, "workspace of %zu bytes needed (got %zu)", need, workspace_bytes_given);
+    if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
+        return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+    int dev = 0;
+    int* err = nullptr;
+    if ((s = device_state(&dev, &err)) != FA_OK) return s;
+    const int64_t bh = B * H;
+    const int64_t nq_pad = (Nq + 127) / 128 * 128;
+    float* lse2 = static_cast<float*>(workspace);
+    float* delta = reinterpret_cast<float*>(static_cast<uint8_t*>(workspace) + need / 2);
+    auto strm = static_cast<cudaStream_t>(stream);
+    const bool bf16 = dtype == FA_BF16;
+    {
+        const int64_t warps = bh * nq_pad;
+        const unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
+        if (D == 128) {
+            if (bf16) fa::fa_bwd_prep_kernel<128, true><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
+            else fa::fa_bwd_prep_kernel<128, false><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
+        } else {
+            if (bf16) fa::fa_bwd_prep_kernel<64, true><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
+            else fa::fa_bwd_prep_kernel<64, false><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
+        }
+        cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess) return cuda_fail(e, "backward prep launch");
+    }
+    CUtensorMap mq, mk, mv, mdo;
+    if ((s = encode_map(&mq, Q, bh, Nq, D, int(dtype))) != FA_OK ||
+        (s = encode_map(&mk, K, bh, Nk, D, int(dtype))) != FA_OK ||
+        (s = encode_map(&mv, V, bh, Nk, D, int(dtype))) != FA_OK ||
+        (s = encode_map(&mdo, dO, bh, Nq, D, int(dtype))) != FA_OK)
+        return s;
+    fa::BwdParams p{};
+    p.dq = dQ;
+    p.dk = dK;
+    p.dv = dV;
+    p.lse2 = lse2;
+    p.delta = delta;
+    p.err = err;
+    p.bh = int(bh);
+    p.nq = int(Nq);
+    p.nk = int(Nk);
+    p.nq_pad = int(nq_pad);
+    p.scale = scale;
+    p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+    p.timeout_ns = wait_timeout_ns();
+    const int inst = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
+    switch (inst) {
+        case 0: return launch_bwd_instance<64, false, false>(dev, mq, mk, mv, mdo, p, strm);
+        case 1: return launch_bwd_instance<64, false, true>(dev, mq, mk, mv, mdo, p, strm);
+        case 2: return launch_bwd_instance<64, true, false>(dev, mq, mk, mv, mdo, p, strm);
+        case 3: return launch_bwd_instance<64, true, true>(dev, mq, mk, mv, mdo, p, strm);
+        case 4: return launch_bwd_instance<128, false, false>(dev, mq, mk, mv, mdo, p, strm);
+        case 5: return launch_bwd_instance<128, false, true>(dev, mq, mk, mv, mdo, p, strm);
+        case 6: return launch_bwd_instance<128, true, false>(dev, mq, mk, mv, mdo, p, strm);
+        default: return launch_bwd_instance<128, true, true>(dev, mq, mk, mv, mdo, p, strm);
+    }
 }
 
 fa_status fa_set_tail_split(int enable) {

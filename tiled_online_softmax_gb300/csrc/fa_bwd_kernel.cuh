@@ -1,0 +1,577 @@
+// fa_bwd_kernel.cuh -- attention backward by recompute on sm_103a.
+//
+// The forward pass keeps no P; the backward recomputes it tile by tile from Q, K and the saved
+// log-sum-exp ("11. Fusion, recompute, and flash attention", section 11.9, "Backward", and the
+// exercise "Backward with recompute"). With P = exp(scale * Q K^T - LSE) row by row:
+//   dV = P^T dO,   dP = dO V^T,   dS = P * (dP - D)  with D_i = sum_d dO_i O_i,
+//   dQ = scale * dS K,   dK = scale * dS^T Q.
+// Three kernels, no atomics (results are deterministic):
+//   fa_bwd_prep_kernel  D_i and LSE_i * log2(e) per query row (padded rows: +inf and 0, so
+//                       padded queries get P = 0 with no further mask).
+//   fa_bwd_dkdv_kernel  one CTA per 128 keys: S^T = K Q_i^T and dP^T = V dO_i^T into TMEM,
+//                       P^T and dS^T rounded to 16 bits over them, dV += P^T dO_i and
+//                       dK += dS^T Q_i accumulating in TMEM, over every query block i.
+//   fa_bwd_dq_kernel    one CTA per 128 queries: S = Q K_j^T and dP = dO V_j^T, dS over S,
+//                       dQ += dS K_j, over every key block j.
+// Warp roles (192 threads): warps 0-3 compute (thread r owns TMEM lane r: a key row in the
+// first kernel, a query row in the second), warp 4 issues MMAs (an elected lane) and owns TMEM,
+// warp 5 issues TMA copies. Every wait is bounded as in the forward kernel.
+#pragma once
+
+#include "fa_fwd_kernel.cuh"
+
+namespace fa {
+
+struct BwdParams {
+    void* dq;             // [bh][nq][D]
+    void* dk;             // [bh][nk][D]
+    void* dv;             // [bh][nk][D]
+    const float* lse2;    // [bh][nq_pad]: LSE * log2(e); +inf on rows >= nq
+    const float* delta;   // [bh][nq_pad]: sum_d dO * O; 0 on rows >= nq
+    int* err;
+    int bh, nq, nk, nq_pad;
+    float scale;          // softmax scale
+    float scale_log2;     // scale * log2(e)
+    unsigned long long timeout_ns;
+};
+
+constexpr int BWD_THREADS = 192;
+constexpr int BWD_MMA_WARP = 4;
+constexpr int BWD_LOAD_WARP = 5;
+constexpr uint32_t BWD_TMEM_S = 0, BWD_TMEM_DP = 128, BWD_TMEM_A = 256, BWD_TMEM_B = 384;
+
+enum BwdSite : int {
+    SITE_BWD_LOAD = 21,
+    SITE_BWD_MMA = 22,
+    SITE_BWD_COMPUTE = 23,
+    SITE_BWD_DRAIN = 24,
+};
+
+// ---------------------------------------------------------------------------------------------
+// D_i and LSE2_i: one warp per (padded) query row
+// ---------------------------------------------------------------------------------------------
+template <int D, bool BF16>
+__global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const void* __restrict__ o,
+                                                          const void* __restrict__ dout,
+                                                          const float* __restrict__ lse,
+                                                          float* __restrict__ lse2,
+                                                          float* __restrict__ delta, int bh,
+                                                          int nq, int nq_pad) {
+    constexpr int E = D / 32;
+    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    const int lane = threadIdx.x & 31;
+    if (w >= static_cast<int64_t>(bh) * nq_pad) return;
+    const int64_t h = w / nq_pad, r = w % nq_pad;
+    if (r >= nq) {
+        if (lane == 0) {
+            lse2[w] = INFINITY;
+            delta[w] = 0.f;
+        }
+        return;
+    }
+    const int64_t src = (h * nq + r) * D + lane * E;
+    const uint16_t* op = static_cast<const uint16_t*>(o) + src;
+    const uint16_t* dp = static_cast<const uint16_t*>(dout) + src;
+    float acc = 0.f;
+#pragma unroll
+    for (int e = 0; e < E; e += 2) {
+        const float2 a = unpack2<BF16>(*reinterpret_cast<const uint32_t*>(op + e));
+        const float2 b = unpack2<BF16>(*reinterpret_cast<const uint32_t*>(dp + e));
+        acc = fmaf(a.x, b.x, acc);
+        acc = fmaf(a.y, b.y, acc);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (lane == 0) {
+        delta[w] = acc;
+        lse2[w] = lse[h * nq + r] * 1.4426950408889634f;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// shared memory of the two main kernels
+// ---------------------------------------------------------------------------------------------
+template <int D>
+struct BwdSmem {
+    static constexpr int COL_BLOCKS = D / 64;
+    static constexpr int TILE = 128 * D * 2;          // one 128-row tile of Q, K, V or dO
+    static constexpr int STAGES = 2;
+    // Two resident tiles (R0, R1), then two rings of STAGES tiles (A, B), then per-stage
+    // vectors (lse2, delta: 2 x 128 floats).
+    static constexpr int R0_OFF = 0;
+    static constexpr int R1_OFF = TILE;
+    static constexpr int A_OFF = 2 * TILE;
+    static constexpr int B_OFF = A_OFF + STAGES * TILE;
+    static constexpr int VEC_OFF = B_OFF + STAGES * TILE;
+    static constexpr int BAR_OFF = VEC_OFF + STAGES * 1024;
+    static constexpr int B_RES_FULL = 0;              // resident tiles landed
+    static constexpr int B_A_FULL = 1;                // [STAGES]
+    static constexpr int B_B_FULL = B_A_FULL + STAGES;  // [STAGES]
+    static constexpr int B_EMPTY = B_B_FULL + STAGES;   // [STAGES]
+    static constexpr int B_S_FULL = B_EMPTY + STAGES;
+    static constexpr int B_DP_FULL = B_S_FULL + 1;
+    static constexpr int B_P_FULL = B_DP_FULL + 1;
+    static constexpr int B_DS_FULL = B_P_FULL + 1;
+    static constexpr int B_MMA_DONE = B_DS_FULL + 1;
+    static constexpr int B_DRAIN = B_MMA_DONE + 1;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int TMEM_SLOT_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
+    static constexpr int BYTES = ABORT_OFF + 4;
+    static constexpr int ALLOC_BYTES = (BYTES + 1024 > 116 * 1024) ? BYTES + 1024 : 116 * 1024;
+    static_assert(ALLOC_BYTES <= 232448, "shared memory budget");
+};
+
+// Operand descriptors of a 128-row tile staged by TMA in 64-column blocks (128-byte swizzle).
+// K-major use (the tile's D is the MMA's K): step kk of 16 elements.
+__device__ __forceinline__ uint64_t kmajor_desc(uint32_t tile, int kk) {
+    return ptx::sdesc_sw128(tile + (kk / 4) * (128 * 128) + (kk % 4) * 32, 16, 1024);
+}
+// MN-major use (the tile's rows are the MMA's K, its D the N): step kk of 16 rows.
+__device__ __forceinline__ uint64_t mnmajor_desc(uint32_t tile, int kk) {
+    return ptx::sdesc_sw128(tile + kk * (16 * 128), 128 * 128, 1024);
+}
+
+template <int D>
+__device__ __forceinline__ void tma_tile(uint32_t dst, const CUtensorMap* map, int row, int slice,
+                                         uint32_t bar) {
+#pragma unroll
+    for (int c = 0; c < D / 64; ++c) ptx::tma_load_3d(dst + c * (128 * 128), map, c * 64, row, slice, bar);
+}
+
+// Convert 32 fp32 registers to 16 words of 16-bit pairs.
+template <bool BF16>
+__device__ __forceinline__ void pack16(const float* f, uint32_t (&u)[16]) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) u[i] = pack2<BF16>(f[2 * i], f[2 * i + 1]);
+}
+
+// Write a 16-bit row of D values from TMEM columns (fp32) times `mul` to global memory.
+template <int D, bool BF16>
+__device__ __forceinline__ void store_row(uint32_t tmem_cols, float mul, void* dst_row, bool keep) {
+#pragma unroll 1
+    for (int q = 0; q < D / 16; ++q) {
+        uint32_t o[16];
+        ptx::tmem_ld16(tmem_cols + q * 16, o);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(o);
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+            w[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * mul, __uint_as_float(o[2 * i + 1]) * mul);
+        if (keep) {
+            uint4* d = reinterpret_cast<uint4*>(static_cast<uint8_t*>(dst_row) + q * 32);
+            d[0] = make_uint4(w[0], w[1], w[2], w[3]);
+            d[1] = make_uint4(w[4], w[5], w[6], w[7]);
+        }
+    }
+}
+
+template <int D>
+__device__ __forceinline__ void zero_row(void* dst_row) {
+    uint4* d = static_cast<uint4*>(dst_row);
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) d[i] = make_uint4(0, 0, 0, 0);
+}
+
+// Common prologue: barriers, TMEM. Returns the TMEM base.
+template <int D>
+__device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t sbase, uint32_t tmem_slot_addr,
+                                              uint32_t* tmem_slot, volatile int* abort_flag,
+                                              int a_full_count) {
+    using L = BwdSmem<D>;
+    auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
+    const int warp = threadIdx.x >> 5;
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        ptx::mbar_init(bar(L::B_RES_FULL), 1);
+        for (int s = 0; s < L::STAGES; ++s) {
+            ptx::mbar_init(bar(L::B_A_FULL + s), a_full_count);
+            ptx::mbar_init(bar(L::B_B_FULL + s), 1);
+            ptx::mbar_init(bar(L::B_EMPTY + s), 1);
+        }
+        ptx::mbar_init(bar(L::B_S_FULL), 1);
+        ptx::mbar_init(bar(L::B_DP_FULL), 1);
+        ptx::mbar_init(bar(L::B_P_FULL), 128);
+        ptx::mbar_init(bar(L::B_DS_FULL), 128);
+        ptx::mbar_init(bar(L::B_MMA_DONE), 1);
+        ptx::mbar_init(bar(L::B_DRAIN), 1);
+        ptx::fence_barrier_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == BWD_MMA_WARP) {
+        ptx::tmem_alloc(tmem_slot_addr, TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    return *tmem_slot;
+}
+
+__device__ __forceinline__ uint32_t elect_leader() {
+    uint32_t leader;
+    asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
+                 : "=r"(leader));
+    return leader;
+}
+
+// ---------------------------------------------------------------------------------------------
+// dK, dV: one CTA per (slice, 128 keys); resident K (R0) and V (R1); ring A = Q_i, ring B = dO_i
+// ---------------------------------------------------------------------------------------------
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                       const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                       const BwdParams p) {
+    using L = BwdSmem<D>;
+    constexpr int STAGES = L::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sbase = ptx::smem_u32(smem);
+    auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::ABORT_OFF);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int nkb = (p.nk + 127) / 128, nqb = (p.nq + 127) / 128;
+    const int bh = blockIdx.x / nkb, kb = blockIdx.x % nkb;
+    const int k0 = kb * 128;
+    const int i_begin = CAUSAL ? kb : 0;  // query blocks before the diagonal see none of these keys
+    const int n = nqb > i_begin ? nqb - i_begin : 0;
+    const uint32_t tmem = bwd_setup<D>(smem, sbase, ptx::smem_u32(tmem_slot), tmem_slot, abort_flag, 1);
+    const Ctl ctl{abort_flag, p.err, p.timeout_ns};
+
+    if (warp == BWD_LOAD_WARP) {
+        if (lane == 0 && n > 0) {
+            ptx::mbar_arrive_expect_tx(bar(L::B_RES_FULL), 2 * L::TILE);
+            tma_tile<D>(sbase + L::R0_OFF, &tm_k, k0, bh, bar(L::B_RES_FULL));
+            tma_tile<D>(sbase + L::R1_OFF, &tm_v, k0, bh, bar(L::B_RES_FULL));
+            int issued = 0;
+            for (int it = 0; it < n; ++it) {
+                const int st = it % STAGES;
+                if (!wait_bar(bar(L::B_EMPTY + st), ((it / STAGES) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
+                const int i = i_begin + it;
+                ptx::mbar_arrive_expect_tx(bar(L::B_A_FULL + st), 2 * L::TILE + 1024);
+                tma_tile<D>(sbase + L::A_OFF + st * L::TILE, &tm_q, i * 128, bh, bar(L::B_A_FULL + st));
+                tma_tile<D>(sbase + L::B_OFF + st * L::TILE, &tm_do, i * 128, bh, bar(L::B_A_FULL + st));
+                const size_t vo = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(i) * 128;
+                ptx::bulk_load(sbase + L::VEC_OFF + st * 1024, p.lse2 + vo, 512, bar(L::B_A_FULL + st));
+                ptx::bulk_load(sbase + L::VEC_OFF + st * 1024 + 512, p.delta + vo, 512, bar(L::B_A_FULL + st));
+                issued = it + 1;
+            }
+            if (*abort_flag) {
+                wait_bar(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_DRAIN, false);
+                for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
+                    wait_bar(bar(L::B_A_FULL + it % STAGES), (it / STAGES) & 1, ctl, SITE_BWD_DRAIN, false);
+            }
+        }
+        __syncwarp();
+    } else if (warp == BWD_MMA_WARP) {
+        const uint32_t leader = elect_leader();
+        constexpr uint32_t IDESC_SQ = ptx::idesc_f16(BF16, 128, 128, false, false);
+        constexpr uint32_t IDESC_OD = ptx::idesc_f16(BF16, 128, D, false, true);
+        const uint32_t d_s = tmem + BWD_TMEM_S, d_dp = tmem + BWD_TMEM_DP;
+        const uint32_t d_dv = tmem + BWD_TMEM_A, d_dk = tmem + BWD_TMEM_B;
+        auto stage_q = [&](int it) { return sbase + L::A_OFF + (it % STAGES) * L::TILE; };
+        auto stage_do = [&](int it) { return sbase + L::B_OFF + (it % STAGES) * L::TILE; };
+        auto issue_s = [&](int it) {  // S^T = K Q_i^T
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                if (leader) ptx::mma_ss(d_s, kmajor_desc(sbase + L::R0_OFF, kk), kmajor_desc(stage_q(it), kk), IDESC_SQ, kk > 0);
+        };
+        auto issue_dp = [&](int it) {  // dP^T = V dO_i^T
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)
+                if (leader) ptx::mma_ss(d_dp, kmajor_desc(sbase + L::R1_OFF, kk), kmajor_desc(stage_do(it), kk), IDESC_SQ, kk > 0);
+        };
+        auto commit = [&](int b) {
+            if (leader) ptx::mma_commit(bar(b));
+            __syncwarp();
+        };
+        bool ok = n > 0 && wait_bar_warp(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_MMA) &&
+                  wait_bar_warp(bar(L::B_A_FULL + 0), 0, ctl, SITE_BWD_MMA);
+        if (ok) {
+            ptx::tc_fence_after();
+            issue_s(0);
+            commit(L::B_S_FULL);
+            issue_dp(0);
+            commit(L::B_DP_FULL);
+        }
+        for (int it = 0; ok && it < n; ++it) {
+            // dV += P^T dO_i (P^T over the S^T columns)
+            if (!(ok = wait_bar_warp(bar(L::B_P_FULL), it & 1, ctl, SITE_BWD_MMA))) break;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                if (leader) ptx::mma_ts(d_dv, d_s + kk * 8, mnmajor_desc(stage_do(it), kk), IDESC_OD, (it > 0 || kk > 0));
+            if (it + 1 < n) {  // S^T of the next block may overwrite P^T now (MMAs run in order)
+                if (!(ok = wait_bar_warp(bar(L::B_A_FULL + (it + 1) % STAGES), ((it + 1) / STAGES) & 1, ctl, SITE_BWD_MMA))) break;
+                ptx::tc_fence_after();
+                issue_s(it + 1);
+                commit(L::B_S_FULL);
+            }
+            // dK += dS^T Q_i (dS^T over the dP^T columns)
+            if (!(ok = wait_bar_warp(bar(L::B_DS_FULL), it & 1, ctl, SITE_BWD_MMA))) break;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+                if (leader) ptx::mma_ts(d_dk, d_dp + kk * 8, mnmajor_desc(stage_q(it), kk), IDESC_OD, (it > 0 || kk > 0));
+            commit(L::B_EMPTY + it % STAGES);
+            if (it + 1 < n) {
+                issue_dp(it + 1);
+                commit(L::B_DP_FULL);
+            }
+        }
+        if (ok && n > 0) commit(L::B_MMA_DONE);
+        if (*abort_flag) {
+            commit(L::B_DRAIN);
+            wait_bar(bar(L::B_DRAIN), 0, ctl, SITE_BWD_DRAIN, false);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- compute warps
+        const int r = threadIdx.x;  // key row within the block
+        const int kr = k0 + r;
+        const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t s_cols = tmem + lanes + BWD_TMEM_S, dp_cols = tmem + lanes + BWD_TMEM_DP;
+        const float c = p.scale_log2;
+        bool ok = true;
+        for (int it = 0; it < n; ++it) {
+            const int i = i_begin + it;
+            const float* vec = reinterpret_cast<const float*>(smem + L::VEC_OFF + (it % STAGES) * 1024);
+            if (!(ok = wait_bar_warp(bar(L::B_S_FULL), it & 1, ctl, SITE_BWD_COMPUTE))) break;
+            ptx::tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ptx::tmem_ld32(s_cols + q * 32, sr[q]);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ptx::reg_fence(sr[q]);
+            // P^T[r][col] = 2^(s*c - LSE2[col]); padded queries have LSE2 = +inf, so P = 0.
+            // On the diagonal block a query before this key (q < k) does not see it.
+            const bool diag = CAUSAL && (i == kb);
+            float pf[128];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    const int col = q * 32 + e;
+                    float pv = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -vec[col]));
+                    if (diag && i * 128 + col < kr) pv = 0.f;
+                    pf[col] = pv;
+                }
+            uint32_t pk[2][32];
+#pragma unroll
+            for (int h = 0; h < 2; ++h)
+#pragma unroll
+                for (int w = 0; w < 32; ++w) pk[h][w] = pack2<BF16>(pf[h * 64 + 2 * w], pf[h * 64 + 2 * w + 1]);
+            ptx::tmem_st32(s_cols, pk[0]);
+            ptx::tmem_st32(s_cols + 32, pk[1]);
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(L::B_P_FULL));
+            // dS^T[r][col] = P^T (dP^T - D[col]), written over the dP^T columns chunk by chunk
+            // (chunk q of fp32 columns 32q.. becomes 16-bit pairs at 16q.., already read).
+            if (!(ok = wait_bar_warp(bar(L::B_DP_FULL), it & 1, ctl, SITE_BWD_COMPUTE))) break;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t dr[32];
+                ptx::tmem_ld32(dp_cols + q * 32, dr);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence(dr);
+                float ds[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e)
+                    ds[e] = pf[q * 32 + e] * (__uint_as_float(dr[e]) - vec[128 + q * 32 + e]);
+                uint32_t w[16];
+                pack16<BF16>(ds, w);
+                ptx::tmem_st16(dp_cols + q * 16, w);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(L::B_DS_FULL));
+        }
+        // Epilogue: dV and scale * dK for this thread's key row.
+        const size_t row_off = (static_cast<size_t>(bh) * p.nk + kr) * D * 2;
+        if (n == 0) {
+            if (kr < p.nk) {
+                zero_row<D>(static_cast<uint8_t*>(p.dv) + row_off);
+                zero_row<D>(static_cast<uint8_t*>(p.dk) + row_off);
+            }
+        } else if (ok && wait_bar_warp(bar(L::B_MMA_DONE), 0, ctl, SITE_BWD_COMPUTE)) {
+            ptx::tc_fence_after();
+            store_row<D, BF16>(tmem + lanes + BWD_TMEM_A, 1.f, static_cast<uint8_t*>(p.dv) + row_off, kr < p.nk);
+            store_row<D, BF16>(tmem + lanes + BWD_TMEM_B, p.scale, static_cast<uint8_t*>(p.dk) + row_off, kr < p.nk);
+        }
+        ptx::tmem_wait_st();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == BWD_MMA_WARP) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
+// dQ: one CTA per (slice, 128 queries); resident Q (R0) and dO (R1); ring A = K_j, ring B = V_j
+// ---------------------------------------------------------------------------------------------
+template <int D, bool BF16, bool CAUSAL>
+__global__ void __launch_bounds__(BWD_THREADS, 1)
+    fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                     const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                     const BwdParams p) {
+    using L = BwdSmem<D>;
+    constexpr int STAGES = L::STAGES;
+    extern __shared__ uint8_t smem_raw[];
+    const uint32_t raw = ptx::smem_u32(smem_raw);
+    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t sbase = ptx::smem_u32(smem);
+    auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::ABORT_OFF);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+
+    const int nkb = (p.nk + 127) / 128, nqb = (p.nq + 127) / 128;
+    const int bh = blockIdx.x / nqb, qb = blockIdx.x % nqb;
+    const int q0 = qb * 128;
+    const int n = CAUSAL ? min(nkb, qb + 1) : nkb;  // key blocks up to the diagonal
+    const uint32_t tmem = bwd_setup<D>(smem, sbase, ptx::smem_u32(tmem_slot), tmem_slot, abort_flag, 1);
+    const Ctl ctl{abort_flag, p.err, p.timeout_ns};
+
+    if (warp == BWD_LOAD_WARP) {
+        if (lane == 0) {
+            ptx::mbar_arrive_expect_tx(bar(L::B_RES_FULL), 2 * L::TILE);
+            tma_tile<D>(sbase + L::R0_OFF, &tm_q, q0, bh, bar(L::B_RES_FULL));
+            tma_tile<D>(sbase + L::R1_OFF, &tm_do, q0, bh, bar(L::B_RES_FULL));
+            int issued = 0;
+            for (int j = 0; j < n; ++j) {
+                const int st = j % STAGES;
+                if (!wait_bar(bar(L::B_EMPTY + st), ((j / STAGES) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
+                ptx::mbar_arrive_expect_tx(bar(L::B_A_FULL + st), L::TILE);
+                tma_tile<D>(sbase + L::A_OFF + st * L::TILE, &tm_k, j * 128, bh, bar(L::B_A_FULL + st));
+                ptx::mbar_arrive_expect_tx(bar(L::B_B_FULL + st), L::TILE);
+                tma_tile<D>(sbase + L::B_OFF + st * L::TILE, &tm_v, j * 128, bh, bar(L::B_B_FULL + st));
+                issued = j + 1;
+            }
+            if (*abort_flag) {
+                wait_bar(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_DRAIN, false);
+                for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j) {
+                    wait_bar(bar(L::B_A_FULL + j % STAGES), (j / STAGES) & 1, ctl, SITE_BWD_DRAIN, false);
+                    wait_bar(bar(L::B_B_FULL + j % STAGES), (j / STAGES) & 1, ctl, SITE_BWD_DRAIN, false);
+                }
+            }
+        }
+        __syncwarp();
+    } else if (warp == BWD_MMA_WARP) {
+        const uint32_t leader = elect_leader();
+        constexpr uint32_t IDESC_SQ = ptx::idesc_f16(BF16, 128, 128, false, false);
+        constexpr uint32_t IDESC_OD = ptx::idesc_f16(BF16, 128, D, false, true);
+        const uint32_t d_s = tmem + BWD_TMEM_S, d_dp = tmem + BWD_TMEM_DP, d_dq = tmem + BWD_TMEM_A;
+        auto commit = [&](int b) {
+            if (leader) ptx::mma_commit(bar(b));
+            __syncwarp();
+        };
+        bool ok = wait_bar_warp(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_MMA);
+        for (int j = 0; ok && j < n; ++j) {
+            const int st = j % STAGES;
+            const uint32_t ph = (j / STAGES) & 1;
+            const uint32_t k_tile = sbase + L::A_OFF + st * L::TILE, v_tile = sbase + L::B_OFF + st * L::TILE;
+            if (!(ok = wait_bar_warp(bar(L::B_A_FULL + st), ph, ctl, SITE_BWD_MMA))) break;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)  // S = Q K_j^T
+                if (leader) ptx::mma_ss(d_s, kmajor_desc(sbase + L::R0_OFF, kk), kmajor_desc(k_tile, kk), IDESC_SQ, kk > 0);
+            commit(L::B_S_FULL);
+            if (!(ok = wait_bar_warp(bar(L::B_B_FULL + st), ph, ctl, SITE_BWD_MMA))) break;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < D / 16; ++kk)  // dP = dO V_j^T
+                if (leader) ptx::mma_ss(d_dp, kmajor_desc(sbase + L::R1_OFF, kk), kmajor_desc(v_tile, kk), IDESC_SQ, kk > 0);
+            commit(L::B_DP_FULL);
+            if (!(ok = wait_bar_warp(bar(L::B_DS_FULL), j & 1, ctl, SITE_BWD_MMA))) break;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j (dS over the S columns)
+                if (leader) ptx::mma_ts(d_dq, d_s + kk * 8, mnmajor_desc(k_tile, kk), IDESC_OD, (j > 0 || kk > 0));
+            commit(L::B_EMPTY + st);
+        }
+        if (ok) commit(L::B_MMA_DONE);
+        if (*abort_flag) {
+            commit(L::B_DRAIN);
+            wait_bar(bar(L::B_DRAIN), 0, ctl, SITE_BWD_DRAIN, false);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------------------- compute warps
+        const int r = threadIdx.x;
+        const int row = q0 + r;
+        const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
+        const uint32_t s_cols = tmem + lanes + BWD_TMEM_S, dp_cols = tmem + lanes + BWD_TMEM_DP;
+        const float c = p.scale_log2;
+        const size_t vo = static_cast<size_t>(bh) * p.nq_pad + row;  // row < nq_pad always
+        const float lse2 = p.lse2[vo], dlt = p.delta[vo];
+        bool ok = true;
+        for (int j = 0; j < n; ++j) {
+            if (!(ok = wait_bar_warp(bar(L::B_S_FULL), j & 1, ctl, SITE_BWD_COMPUTE))) break;
+            ptx::tc_fence_after();
+            uint32_t sr[4][32];
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ptx::tmem_ld32(s_cols + q * 32, sr[q]);
+            ptx::tmem_wait_ld();
+#pragma unroll
+            for (int q = 0; q < 4; ++q) ptx::reg_fence(sr[q]);
+            // P = 2^(s*c - LSE2); keys past Nk and (causal) keys after the query get 0.
+            const int k0 = j * 128;
+            int lim = p.nk - k0;
+            if constexpr (CAUSAL) lim = min(lim, row + 1 - k0);
+            const bool need_mask = lim < 128;
+            float pf[128];
+#pragma unroll
+            for (int q = 0; q < 4; ++q)
+#pragma unroll
+                for (int e = 0; e < 32; ++e) {
+                    float pv = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -lse2));
+                    if (need_mask && q * 32 + e >= lim) pv = 0.f;
+                    pf[q * 32 + e] = pv;
+                }
+            if (!(ok = wait_bar_warp(bar(L::B_DP_FULL), j & 1, ctl, SITE_BWD_COMPUTE))) break;
+            ptx::tc_fence_after();
+            // dS = P (dP - D), written over the S columns (all of S is already in registers).
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t dr[32];
+                ptx::tmem_ld32(dp_cols + q * 32, dr);
+                ptx::tmem_wait_ld();
+                ptx::reg_fence(dr);
+                float ds[32];
+#pragma unroll
+                for (int e = 0; e < 32; ++e) ds[e] = pf[q * 32 + e] * (__uint_as_float(dr[e]) - dlt);
+                uint32_t w[16];
+                pack16<BF16>(ds, w);
+                ptx::tmem_st16(s_cols + q * 16, w);
+            }
+            ptx::tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(bar(L::B_DS_FULL));
+        }
+        if (ok && n > 0 && wait_bar_warp(bar(L::B_MMA_DONE), 0, ctl, SITE_BWD_COMPUTE)) {
+            ptx::tc_fence_after();
+            store_row<D, BF16>(tmem + lanes + BWD_TMEM_A, p.scale,
+                               static_cast<uint8_t*>(p.dq) + (static_cast<size_t>(bh) * p.nq + row) * D * 2,
+                               row < p.nq);
+        }
+        ptx::tmem_wait_st();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == BWD_MMA_WARP) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tmem, TMEM_COLS);
+    }
+}
+
+}  // namespace fa

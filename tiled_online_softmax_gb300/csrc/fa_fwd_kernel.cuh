@@ -191,6 +191,16 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
     }
 }
 
+// The two 16-bit halves of a 32-bit word as fp32 (low half first).
+template <bool BF16>
+__device__ __forceinline__ float2 unpack2(uint32_t u) {
+    if constexpr (BF16) {
+        return make_float2(__uint_as_float(u << 16), __uint_as_float(u & 0xFFFF0000u));
+    } else {
+        return __half22float2(*reinterpret_cast<const __half2*>(&u));
+    }
+}
+
 // ---------------------------------------------------------------------------------------------
 // softmax of one query tile (warpgroup t)
 // ---------------------------------------------------------------------------------------------

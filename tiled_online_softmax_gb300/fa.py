@@ -16,7 +16,7 @@ EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_e
            "fa_status_string", "fa_last_error_message", "fa_fwd_noalloc",
            "fa_set_rescale_threshold", "fa_get_rescale_threshold", "fa_fwd_lse",
            "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_set_tail_split", "fa_rope",
-           "fa_rope_workspace_bytes", "fa_fwd_rope")
+           "fa_rope_workspace_bytes", "fa_fwd_rope", "fa_bwd_workspace_bytes", "fa_bwd")
 
 
 class FaError(RuntimeError):
@@ -61,6 +61,11 @@ def lib() -> ctypes.CDLL:
                               i64, i64, ctypes.c_float, ctypes.c_int, ctypes.c_int, vp,
                               ctypes.c_size_t, vp]
     L.fa_fwd_rope.restype = ctypes.c_int
+    L.fa_bwd_workspace_bytes.argtypes = [i64, i64, i64]
+    L.fa_bwd_workspace_bytes.restype = ctypes.c_size_t
+    L.fa_bwd.argtypes = [vp] * 9 + [i64] * 5 + [ctypes.c_float, ctypes.c_int, ctypes.c_int, vp,
+                                                 ctypes.c_size_t, vp]
+    L.fa_bwd.restype = ctypes.c_int
     L.fa_release_host_buffers.argtypes = []
     L.fa_release_host_buffers.restype = ctypes.c_int
     L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
@@ -253,6 +258,35 @@ def forward_rope(q, k, v, cos_q, sin_q, cos_k, sin_k, form: int = 0, causal: boo
                                     int(bool(causal)), code, workspace.data_ptr(),
                                     workspace.numel(), stream.cuda_stream))
     return out
+
+
+def backward(q, k, v, o, lse, dout, causal: bool = False, scale: float | None = None,
+             workspace=None, stream=None):
+    """(dQ, dK, dV) for CUDA tensors, from the forward's inputs, its O and LSE (forward_lse)
+    and the upstream gradient dout."""
+    import torch
+
+    B, H, Nq, Nk, D = _shape(q, k, v)
+    code = _dtype_code(q)
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    need = int(lib().fa_bwd_workspace_bytes(B, H, Nq))
+    if workspace is None:
+        workspace = torch.empty(need, dtype=torch.uint8, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    for t in (o, dout):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_contiguous():
+            raise ValueError("o and dout must be contiguous and shaped like q")
+    if lse.dtype != torch.float32 or tuple(lse.shape) != (B, H, Nq) or not lse.is_contiguous():
+        raise ValueError("lse must be a contiguous float32 tensor [B, H, Nq]")
+    with torch.cuda.device(q.device):
+        _raise_if(lib().fa_bwd(q.data_ptr(), k.data_ptr(), v.data_ptr(), o.data_ptr(),
+                               dout.data_ptr(), lse.data_ptr(), dq.data_ptr(), dk.data_ptr(),
+                               dv.data_ptr(), B, H, Nq, Nk, D, float(scale), int(bool(causal)),
+                               code, workspace.data_ptr(), workspace.numel(), stream.cuda_stream))
+    return dq, dk, dv
 
 
 def forward_host(q, k, v, out, causal: bool = False, scale: float | None = None, stream=None,
