@@ -34,6 +34,8 @@ import sys
 import time
 from pathlib import Path
 
+import numpy as np
+
 ROOT = Path(__file__).resolve().parent
 sys.path.insert(0, str(ROOT))
 
@@ -215,6 +217,68 @@ def run_reference(args, w):
     return 0
 
 
+def run_other_pass(args, w):
+    """Timing of the backward pass or of the rotary-embedding pass on one GPU (one JSON line;
+    not the headline metric)."""
+    import torch
+
+    from tiled_online_softmax_gb300 import fa, inputs
+
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    fa.lib()
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).to(dev) for n in "qkv")
+    stream = torch.cuda.current_stream(dev)
+    if args.which == "bwd":
+        do = inputs.to_torch(inputs.draw(w.with_(seed=w.seed + 1000))["q"], w.dtype).to(dev)
+        o, lse = fa.forward_lse(q, k, v, causal=w.causal, scale=w.scale)
+        ws = torch.empty(fa.lib().fa_bwd_workspace_bytes(w.B, w.H, w.Nq), dtype=torch.uint8, device=dev)
+        step = lambda: fa.backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale,
+                                   workspace=ws, stream=stream)
+        work, unit, launches = 2.5 * w.flops, "TFLOP/s", 3
+        metric = "attention bwd TFLOP/s (10*B*H*Nq*Nk*D, halved for causal)"
+    else:
+        half = w.D // 2
+        ang = np.arange(max(w.Nq, w.Nk))[:, None] * 10000.0 ** (-np.arange(half) / half)
+        ct = torch.from_numpy(np.cos(ang).astype(np.float32)).to(dev)
+        st_ = torch.from_numpy(np.sin(ang).astype(np.float32)).to(dev)
+        qo, ko = torch.empty_like(q), torch.empty_like(k)
+
+        def step():
+            fa.rope(q, ct[:w.Nq], st_[:w.Nq], out=qo, stream=stream)
+            fa.rope(k, ct[:w.Nk], st_[:w.Nk], out=ko, stream=stream)
+        # bytes moved: read and write Q and K, read the tables once per row
+        work = 2 * (q.numel() + k.numel()) * 2 + (w.B * w.H) * (w.Nq + w.Nk) * half * 8
+        unit, launches = "GB/s", 2
+        metric = "rotary embedding of Q and K, GB/s"
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize(dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    st, site = fa.last_device_error(stream)
+    if st != 0:
+        raise RuntimeError(f"kernel error word set (site {site})")
+    ms = e0.elapsed_time(e1) / args.steps
+    value = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
+    peaks, kind = load_peaks()
+    peak = float(peaks["bf16_tflops"] if unit == "TFLOP/s" else peaks["hbm_gbs"])
+    print(json.dumps({
+        "metric": metric, "pass": args.which, "value": value, "unit": unit, "n_gpus": 1,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
+        "dtype": w.dtype, "data": "synthetic", "config": {"workload": workload_desc(w)},
+        "roofline": {"bound": "tensor" if unit == "TFLOP/s" else "hbm", "achieved": value,
+                     "peak": peak, "unit": unit, "frac": value / peak,
+                     "peak_kind": f"{kind} " + ("bf16 dense (burst)" if unit == "TFLOP/s" else "copy bandwidth")},
+        "gpu_launches": args.steps * launches}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -223,6 +287,9 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default="headline")
     ap.add_argument("--e2e-steps", type=int, default=10)
+    ap.add_argument("--pass", dest="which", choices=["fwd", "bwd", "rope"], default="fwd",
+                    help="fwd: the forward pass (the headline metric); bwd: fa_bwd after one "
+                         "forward; rope: the rotary-embedding pass over Q and K")
     ap.add_argument("--splits", type=int, default=0,
                     help="key splits for workloads with few query blocks (0: automatic)")
     ap.add_argument("--ref-seconds", type=float, default=12.0)
@@ -238,6 +305,8 @@ def main():
     w = inputs.WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
+    if args.which != "fwd":
+        return run_other_pass(args, w)
 
     import torch
     import torch.distributed as dist
