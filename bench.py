@@ -248,8 +248,9 @@ def run_other_pass(args, w):
         def step():
             fa.rope(q, ct[:w.Nq], st_[:w.Nq], out=qo, stream=stream)
             fa.rope(k, ct[:w.Nk], st_[:w.Nk], out=ko, stream=stream)
-        # bytes moved: read and write Q and K, read the tables once per row
-        work = 2 * (q.numel() + k.numel()) * 2 + (w.B * w.H) * (w.Nq + w.Nk) * half * 8
+        # algorithmic bytes: read and write Q and K once; the cos/sin tables ([N, D/2] fp32,
+        # shared by every batch and head) once
+        work = 2 * (q.numel() + k.numel()) * 2 + (w.Nq + w.Nk) * half * 8
         unit, launches = "GB/s", 2
         metric = "rotary embedding of Q and K, GB/s"
     for _ in range(args.warmup):

@@ -308,6 +308,7 @@ fa_status launch_split(const void* Q, const void* K, const void* V, void* O, flo
                        int64_t split_units, void* workspace) {
     const int64_t split_rows = Nq < fa::UNIT_ROWS ? Nq : fa::UNIT_ROWS;
     const size_t rows = size_t(split_units) * size_t(split_rows);
+    if (rows > size_t(INT32_MAX) / 32) return fail(FA_ERR_UNSUPPORTED, "too many rows to split");
     Split sp;
     sp.num_splits = plan.num_splits;
     sp.kv_tiles_per_split = plan.tiles_per_split;
@@ -423,7 +424,8 @@ fa_status validate_rope(const void* X, const void* Y, const float* cos_t, const 
     if (rows_total < 1 || n < 1 || D < 1) return fail(FA_ERR_INVALID_ARGUMENT, "sizes must be >= 1");
     if (form != 0 && form != 1) return fail(FA_ERR_INVALID_ARGUMENT, "rope form must be 0 or 1");
     if (dtype != FA_F16 && dtype != FA_BF16) return fail(FA_ERR_INVALID_ARGUMENT, "unknown dtype");
-    if (D % 16 != 0 || D > 512) return fail(FA_ERR_UNSUPPORTED, "rope needs D a multiple of 16, <= 512");
+    if (D % 16 != 0 || D > 512 || ((D / 16) & (D / 16 - 1)) != 0)
+        return fail(FA_ERR_UNSUPPORTED, "rope needs D = 16 * 2^k, at most 512");
     for (const void* p : {X, Y, static_cast<const void*>(cos_t), static_cast<const void*>(sin_t)})
         if (reinterpret_cast<uintptr_t>(p) % 16 != 0)
             return fail(FA_ERR_MISALIGNED, "rope pointer %p is not 16-byte aligned", p);

@@ -31,32 +31,62 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__
                                                        void* __restrict__ o, float* __restrict__ lse,
                                                        int64_t rows, int num_splits, MergeMap map) {
     constexpr int E = D / 32;
-    const int64_t row = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
+    // 32-bit index arithmetic: rows, units and query rows all fit in int (checked on the host).
+    const int row = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;
-    const int64_t unit = map.split_begin + row / map.split_rows;
-    const int64_t q_row = (unit % map.num_units) * 256 + row % map.split_rows;
+    const int tu = row / map.split_rows;
+    const int unit = map.split_begin + tu;
+    const int bh = unit / map.num_units;
+    const int q_row = (unit - bh * map.num_units) * 256 + (row - tu * map.split_rows);
     if (q_row >= map.nq) return;
-    const int64_t out_row = (unit / map.num_units) * map.nq + q_row;
+    const int64_t out_row = static_cast<int64_t>(bh) * map.nq + q_row;
     const float2* ml = reinterpret_cast<const float2*>(ml_part);
-    float m = -INFINITY;
-    for (int s = 0; s < num_splits; ++s) m = fmaxf(m, ml[s * rows + row].x);
-    float l = 0.f;
+    float m = -INFINITY, l = 0.f;
     float acc[E];
 #pragma unroll
     for (int e = 0; e < E; ++e) acc[e] = 0.f;
-    for (int s = 0; s < num_splits; ++s) {
-        const float2 st = ml[s * rows + row];
-        const float w = (st.x == -INFINITY) ? 0.f : ptx::ex2(st.x - m);
-        l += st.y * w;
-        const float* src = o_part + (s * rows + row) * D + lane * E;
-        if constexpr (E == 4) {
-            const float4 v = *reinterpret_cast<const float4*>(src);
-            acc[0] += w * v.x; acc[1] += w * v.y; acc[2] += w * v.z; acc[3] += w * v.w;
-        } else {
-            const float2 v = *reinterpret_cast<const float2*>(src);
-            acc[0] += w * v.x; acc[1] += w * v.y;
+    // Splits in groups of 4: every load of a group is issued before any is used, so each
+    // thread keeps several memory requests in flight. Within a group the states are merged
+    // against the group maximum, then the group is merged into the running state.
+    for (int s0 = 0; s0 < num_splits; s0 += 4) {
+        const int g = min(4, num_splits - s0);
+        float2 st[4];
+        float v[4][E];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            if (u < g) {
+                const int64_t prow = static_cast<int64_t>(s0 + u) * rows + row;
+                st[u] = ml[prow];
+                const float* src = o_part + prow * D + lane * E;
+                if constexpr (E == 4) {
+                    const float4 x = *reinterpret_cast<const float4*>(src);
+                    v[u][0] = x.x; v[u][1] = x.y; v[u][2] = x.z; v[u][3] = x.w;
+                } else {
+                    const float2 x = *reinterpret_cast<const float2*>(src);
+                    v[u][0] = x.x; v[u][1] = x.y;
+                }
+            } else {
+                st[u] = make_float2(-INFINITY, 0.f);
+#pragma unroll
+                for (int e = 0; e < E; ++e) v[u][e] = 0.f;
+            }
         }
+        float m_new = m;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) m_new = fmaxf(m_new, st[u].x);
+        const float c_old = (m == -INFINITY) ? 0.f : ptx::ex2(m - m_new);
+        l *= c_old;
+#pragma unroll
+        for (int e = 0; e < E; ++e) acc[e] *= c_old;
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            const float w = (st[u].x == -INFINITY) ? 0.f : ptx::ex2(st[u].x - m_new);
+            l += st[u].y * w;
+#pragma unroll
+            for (int e = 0; e < E; ++e) acc[e] += w * v[u][e];
+        }
+        m = m_new;
     }
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
     uint32_t packed[E / 2];

@@ -45,14 +45,23 @@ __global__ void __launch_bounds__(256) fa_rope_kernel(const uint16_t* x, uint16_
                                                       const float* __restrict__ sin_t,
                                                       int64_t rows_total, int64_t n, int d) {
     const int half = d / 2;
-    const int groups = half / 8;  // groups of 8 pairs per row
+    const int groups = half / 8;  // groups of 8 pairs per row (a power of two: d/16)
+    const int shift = __ffs(groups) - 1;
     const int64_t total = rows_total * groups;
-    for (int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; g < total;
-         g += static_cast<int64_t>(gridDim.x) * blockDim.x) {
-        const int64_t row = g / groups;
-        const int i0 = static_cast<int>(g % groups) * 8;  // first pair of the group
-        const float* ct = cos_t + (row % n) * half + i0;
-        const float* st = sin_t + (row % n) * half + i0;
+    // The grid-stride loop walks rows; the row within its slice advances by the same stride
+    // modulo n, so no 64-bit division runs per element.
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t g = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    int64_t nrow = (g >> shift) % n;
+    const int64_t nstep_rows = stride >> shift;  // stride is a multiple of groups
+    const int64_t nstep = nstep_rows % n;
+    for (; g < total; g += stride) {
+        const int64_t row = g >> shift;
+        const int i0 = static_cast<int>(g & (groups - 1)) * 8;  // first pair of the group
+        const float* ct = cos_t + nrow * half + i0;
+        const float* st = sin_t + nrow * half + i0;
+        nrow += nstep;
+        if (nrow >= n) nrow -= n;
         const float4 c0 = *reinterpret_cast<const float4*>(ct);
         const float4 c1 = *reinterpret_cast<const float4*>(ct + 4);
         const float4 s0 = *reinterpret_cast<const float4*>(st);
