@@ -236,6 +236,17 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, i
 fa_status fa_last_device_error(void* stream, int* site);
 
 /*
+ * fa_wait_selftest -- check the bounded-wait machinery on the device, asynchronous on `stream`.
+ * Launches one warp that waits, through the same routine every libfa kernel waits with, on a
+ * barrier that nothing ever arrives on. After `timeout_ns` (0 < timeout_ns <= 1e9) the wait
+ * gives up and records site code 30 in the error word, so the next fa_last_device_error on
+ * `stream` returns FA_ERR_TIMEOUT with *site == 30; the CUDA context stays usable. Nothing is
+ * read or written besides the error word. FA_ERR_INVALID_ARGUMENT for a timeout out of range.
+ * The pages have no counterpart; it exists so that the failure path can be tested.
+ */
+fa_status fa_wait_selftest(unsigned long long timeout_ns, void* stream);
+
+/*
  * Lazy (conditional) rescaling threshold, process-wide, in log2 units of the scaled scores.
  * A row keeps its reference maximum, and so skips rescaling its accumulator, while the new
  * maximum exceeds the reference by at most this much (the conditional rescaling paragraph of

@@ -88,3 +88,8 @@ def test_binding_refuses_cpu_tensors(fa):
         fa.forward(q, q, q)
     with pytest.raises(TypeError):
         fa.forward(q.float(), q.float(), q.float())
+
+
+def test_wait_selftest_rejects_bad_timeout(fa):
+    assert fa.lib().fa_wait_selftest(0, None) == 1
+    assert fa.lib().fa_wait_selftest(2_000_000_000, None) == 1

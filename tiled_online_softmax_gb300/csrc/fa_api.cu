@@ -760,6 +760,19 @@ fa_status fa_release_host_buffers(void) {
     return FA_OK;
 }
 
+fa_status fa_wait_selftest(unsigned long long timeout_ns, void* stream) {
+    if (timeout_ns == 0 || timeout_ns > 1000000000ull)
+        return fail(FA_ERR_INVALID_ARGUMENT, "selftest timeout must be in (0, 1e9] ns");
+    int dev = 0;
+    int* err = nullptr;
+    fa_status st = device_state(&dev, &err);
+    if (st != FA_OK) return st;
+    fa::fa_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(err, timeout_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+    return FA_OK;
+}
+
 fa_status fa_last_device_error(void* stream, int* site) {
     if (site) *site = 0;
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));

@@ -85,7 +85,12 @@ enum WaitSite : int {
     SITE_EPI_L_READY = 8,
     SITE_EPI_O_READY = 9,
     SITE_DRAIN = 10,
+    SITE_SELFTEST = 30,   // fa_wait_selftest: a barrier that nothing arrives on
 };
+
+// Floor of the time limit of drain waits (for copies and MMAs this CTA started, which always
+// complete): a short limit for the ordinary waits never lets a CTA exit with copies in flight.
+constexpr unsigned long long DRAIN_FLOOR_NS = 1000000000ull;
 
 struct Params {
     void* o;                   // output [bh][nq][D]
@@ -160,11 +165,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
                                          bool honor_abort = true) {
     if (ptx::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = ptx::globaltimer_ns();
+    const uint64_t limit =
+        honor_abort || ctl.timeout_ns >= DRAIN_FLOOR_NS ? ctl.timeout_ns : DRAIN_FLOOR_NS;
     for (uint32_t it = 1;; ++it) {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         if ((it & 31u) == 0) {
             if (honor_abort && *ctl.abort) return false;
-            if (ptx::globaltimer_ns() - t0 > ctl.timeout_ns) {
+            if (ptx::globaltimer_ns() - t0 > limit) {
                 *ctl.abort = 1;
                 atomicCAS(ctl.err, 0, site);
                 return false;
@@ -178,6 +185,22 @@ __device__ __forceinline__ bool wait_bar_warp(uint32_t bar, uint32_t parity, con
                                               int site) {
     const bool ok = wait_bar(bar, parity, ctl, site);
     return __all_sync(0xffffffffu, ok);
+}
+
+// One warp waits, through wait_bar, on an mbarrier that expects one arrival which never comes:
+// the wait runs out after timeout_ns and leaves SITE_SELFTEST in the error word. It exercises
+// the timeout path of every kernel's waits without a real stall.
+__global__ void __launch_bounds__(32) fa_wait_selftest_kernel(int* err, unsigned long long timeout_ns) {
+    __shared__ __align__(8) uint64_t mbar;
+    __shared__ int abort_flag;
+    if (threadIdx.x == 0) {
+        abort_flag = 0;
+        ptx::mbar_init(static_cast<uint32_t>(__cvta_generic_to_shared(&mbar)), 1);
+        ptx::fence_barrier_init();
+    }
+    __syncwarp();
+    const Ctl ctl{&abort_flag, err, timeout_ns};
+    wait_bar_warp(static_cast<uint32_t>(__cvta_generic_to_shared(&mbar)), 0, ctl, SITE_SELFTEST);
 }
 
 template <bool BF16>

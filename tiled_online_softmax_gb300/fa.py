@@ -16,7 +16,8 @@ EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_e
            "fa_status_string", "fa_last_error_message", "fa_fwd_noalloc",
            "fa_set_rescale_threshold", "fa_get_rescale_threshold", "fa_fwd_lse",
            "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_set_tail_split", "fa_rope",
-           "fa_rope_workspace_bytes", "fa_fwd_rope", "fa_bwd_workspace_bytes", "fa_bwd")
+           "fa_rope_workspace_bytes", "fa_fwd_rope", "fa_bwd_workspace_bytes", "fa_bwd",
+           "fa_wait_selftest")
 
 
 class FaError(RuntimeError):
@@ -70,6 +71,8 @@ def lib() -> ctypes.CDLL:
     L.fa_release_host_buffers.restype = ctypes.c_int
     L.fa_last_device_error.argtypes = [vp, ctypes.POINTER(ctypes.c_int)]
     L.fa_last_device_error.restype = ctypes.c_int
+    L.fa_wait_selftest.argtypes = [ctypes.c_ulonglong, vp]
+    L.fa_wait_selftest.restype = ctypes.c_int
     L.fa_status_string.argtypes = [ctypes.c_int]
     L.fa_status_string.restype = ctypes.c_char_p
     L.fa_last_error_message.argtypes = []
@@ -319,6 +322,16 @@ def last_device_error(stream=None) -> tuple[int, int]:
     site = ctypes.c_int(0)
     st = lib().fa_last_device_error(stream.cuda_stream, ctypes.byref(site))
     return st, site.value
+
+
+def wait_selftest(timeout_ns: int, stream=None) -> None:
+    """Launch the bounded-wait self-test on `stream`: a wait that runs out after timeout_ns and
+    leaves its site code in the device error word (read it with last_device_error)."""
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    _raise_if(lib().fa_wait_selftest(int(timeout_ns), stream.cuda_stream))
 
 
 def set_rescale_threshold(log2_threshold: float) -> None:
