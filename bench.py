@@ -236,8 +236,12 @@ def run_other_pass(args, w):
         ws = torch.empty(fa.lib().fa_bwd_workspace_bytes(w.B, w.H, w.Nq), dtype=torch.uint8, device=dev)
         step = lambda: fa.backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale,
                                    workspace=ws, stream=stream)
-        work, unit, launches = 2.5 * w.flops, "TFLOP/s", 3
+        work, unit = 2.5 * w.flops, "TFLOP/s"
         metric = "attention bwd TFLOP/s (10*B*H*Nq*Nk*D, halved for causal)"
+        # Tensor-core work each kernel executes: 2*B*H*Nq*Nk*D (halved causal) per product;
+        # dK/dV recomputes S and dP and forms dV and dK (4 products), dQ recomputes S and dP and
+        # forms dQ (3 products).
+        kernel_work = {"bwd_dkdv": 2.0 * w.flops, "bwd_dq": 1.5 * w.flops}
     else:
         half = w.D // 2
         ang = np.arange(max(w.Nq, w.Nk))[:, None] * 10000.0 ** (-np.arange(half) / half)
@@ -251,7 +255,8 @@ def run_other_pass(args, w):
         # algorithmic bytes: read and write Q and K once; the cos/sin tables ([N, D/2] fp32,
         # shared by every batch and head) once
         work = 2 * (q.numel() + k.numel()) * 2 + (w.Nq + w.Nk) * half * 8
-        unit, launches = "GB/s", 2
+        unit = "GB/s"
+        kernel_work = {"rope": work}
         metric = "rotary embedding of Q and K, GB/s"
     for _ in range(args.warmup):
         step()
@@ -262,6 +267,13 @@ def run_other_pass(args, w):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    # Per-kernel device times from a second pass with the library's kernel timer on (its events
+    # add small gaps between launches, so it stays out of the timed region).
+    fa.timer_start()
+    for _ in range(args.steps):
+        step()
+    torch.cuda.synchronize(dev)
+    kernels = fa.timer_stop()
     st, site = fa.last_device_error(stream)
     if st != 0:
         raise RuntimeError(f"kernel error word set (site {site})")
@@ -269,14 +281,20 @@ def run_other_pass(args, w):
     value = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
     peaks, kind = load_peaks()
     peak = float(peaks["bf16_tflops"] if unit == "TFLOP/s" else peaks["hbm_gbs"])
+    # Roofline of the dominant kernel: its work per step over its own event-timed device time.
+    top = max(kernel_work, key=lambda k: kernels[k][0])
+    top_ms = kernels[top][0] / args.steps
+    achieved = kernel_work[top] / (top_ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
     print(json.dumps({
         "metric": metric, "pass": args.which, "value": value, "unit": unit, "n_gpus": 1,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True,
         "dtype": w.dtype, "data": "synthetic", "config": {"workload": workload_desc(w)},
-        "roofline": {"bound": "tensor" if unit == "TFLOP/s" else "hbm", "achieved": value,
-                     "peak": peak, "unit": unit, "frac": value / peak,
+        "roofline": {"bound": "tensor" if unit == "TFLOP/s" else "hbm", "achieved": achieved,
+                     "peak": peak, "unit": unit, "frac": achieved / peak, "kernel": top,
+                     "kernel_ms_per_step": top_ms,
+                     "kernels_ms_per_step": {k: v[0] / args.steps for k, v in kernels.items()},
                      "peak_kind": f"{kind} " + ("bf16 dense (burst)" if unit == "TFLOP/s" else "copy bandwidth")},
-        "gpu_launches": args.steps * launches}), flush=True)
+        "gpu_launches": sum(n for _, n in kernels.values())}), flush=True)
     return 0
 
 
@@ -379,6 +397,14 @@ def main():
     torch.cuda.synchronize(dev)
     barrier()
     ms_total = ev0.elapsed_time(ev1)
+    # The same K steps again with the library's kernel timer on: CUDA events around each launch,
+    # on its stream, give every kernel's own device time. The events add small gaps between
+    # launches, so this pass is kept out of the timed region above.
+    fa.timer_start()
+    for i in range(args.steps):
+        step(i)
+    torch.cuda.synchronize(dev)
+    kernels = fa.timer_stop()
     clocks = sampler.stop() if sampler else None
     st, site = fa.last_device_error(stream)
     if st != 0:
@@ -414,8 +440,14 @@ def main():
 
     peaks, peaks_kind = load_peaks()
     peak = float(peaks["bf16_tflops"])
-    achieved = w.flops / (ms_per_step * 1e-3) / 1e12  # one launch per step
+    # The dominant kernel: the attention kernel, one launch per step (the merge of a split
+    # last wave, when there is one, is a second, short launch).
+    fwd_ms, fwd_launches = kernels["fwd"]
+    kernel_ms = fwd_ms / fwd_launches
+    achieved = w.flops / (kernel_ms * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                "kernel": "fa_fwd_kernel", "kernel_ms": kernel_ms,
+                "kernels_ms_per_step": {k: v[0] / args.steps for k, v in kernels.items()},
                 "frac": achieved / peak, "traffic": profiled_traffic(w.name),
                 "peak_kind": f"{peaks_kind} bf16 dense (burst)",
                 "frac_of_datasheet": achieved / DATASHEET_DENSE_BF16_TFLOPS}
@@ -443,7 +475,7 @@ def main():
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": e2e_s * 1e3},
         "clocks": clocks,
-        "gpu_launches": args.steps * (2 if use_split else 1),
+        "gpu_launches": sum(n for _, n in kernels.values()),  # per K steps, by the timer
     }
     print(json.dumps(line), flush=True)
     if world > 1:

@@ -260,6 +260,29 @@ float fa_get_rescale_threshold(void);
 /* Turn fa_fwd's last-wave balancing on (1, the default) or off (0). Process-wide. */
 fa_status fa_set_tail_split(int enable);
 
+/*
+ * Kernel timer, a measurement aid (no counterpart in the pages). Between fa_timer_start and
+ * fa_timer_stop, every kernel launch libfa makes, on any stream, is bracketed by two CUDA events
+ * recorded on that stream; fa_timer_stop waits for the events and sums each launch's device
+ * time by kernel kind; fa_timer_read returns the sum (milliseconds) and the launch count of one
+ * kind. The events come from a pool of 8192 pairs created by the first fa_timer_start on the
+ * current device (kept until process exit); launches past that are not timed and
+ * fa_timer_stop returns FA_ERR_UNSUPPORTED. Use one device while the timer runs. Off, the timer
+ * costs one flag test per launch.
+ */
+typedef enum {
+    FA_KERNEL_FWD = 0,        /* the attention forward kernel (all fa_fwd* entry points) */
+    FA_KERNEL_MERGE = 1,      /* merge of split-over-keys partial states */
+    FA_KERNEL_ROPE = 2,       /* rotary embedding */
+    FA_KERNEL_BWD_PREP = 3,   /* backward: D = rowsum(dO * O) and scaled LSE */
+    FA_KERNEL_BWD_DKDV = 4,   /* backward: dK and dV */
+    FA_KERNEL_BWD_DQ = 5,     /* backward: dQ */
+    FA_KERNEL_KINDS = 6
+} fa_kernel_kind;
+fa_status fa_timer_start(void);
+fa_status fa_timer_stop(void);
+fa_status fa_timer_read(fa_kernel_kind kind, double* total_ms, int* launches);
+
 /* A static, human-readable name for a status code. */
 const char* fa_status_string(fa_status status);
 

@@ -93,3 +93,13 @@ def test_binding_refuses_cpu_tensors(fa):
 def test_wait_selftest_rejects_bad_timeout(fa):
     assert fa.lib().fa_wait_selftest(0, None) == 1
     assert fa.lib().fa_wait_selftest(2_000_000_000, None) == 1
+
+
+def test_kernel_timer_host_checks(fa):
+    import ctypes
+
+    assert fa.lib().fa_timer_stop() == 1  # not running
+    ms, n = ctypes.c_double(), ctypes.c_int()
+    assert fa.lib().fa_timer_read(6, ctypes.byref(ms), ctypes.byref(n)) == 1
+    assert fa.lib().fa_timer_read(-1, ctypes.byref(ms), ctypes.byref(n)) == 1
+    assert fa.lib().fa_timer_read(0, None, ctypes.byref(n)) == 1

@@ -36,6 +36,44 @@ fa_status cuda_fail(cudaError_t e, const char* what) {
     return fail(FA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// ---------------------------------------------------------------------------------------------
+// Kernel timer (a measurement aid, off by default): while on, every kernel launch is bracketed
+// by a pair of CUDA events on its stream, so a caller can read the device time of each kernel
+// kind without a profiler. Events come from a pool made when the timer starts.
+// ---------------------------------------------------------------------------------------------
+struct KernelTimer {
+    static constexpr int MAX_PAIRS = 8192;
+    std::mutex mu;
+    bool on = false;
+    int used = 0;
+    bool overflow = false;
+    cudaEvent_t ev[2 * MAX_PAIRS] = {};
+    int kind[MAX_PAIRS] = {};
+    int created = 0;
+    double ms[FA_KERNEL_KINDS] = {};
+    int launches[FA_KERNEL_KINDS] = {};
+};
+KernelTimer g_timer;
+
+// Record the start event of a launch of `kind`; returns the pair index, or -1 when off.
+int timer_begin(cudaStream_t s, fa_kernel_kind kind) {
+    if (!__atomic_load_n(&g_timer.on, __ATOMIC_ACQUIRE)) return -1;
+    std::lock_guard<std::mutex> lock(g_timer.mu);
+    if (!g_timer.on) return -1;
+    if (g_timer.used >= g_timer.created / 2) {
+        g_timer.overflow = true;
+        return -1;
+    }
+    const int i = g_timer.used++;
+    g_timer.kind[i] = kind;
+    cudaEventRecord(g_timer.ev[2 * i], s);
+    return i;
+}
+
+void timer_end(cudaStream_t s, int i) {
+    if (i >= 0) cudaEventRecord(g_timer.ev[2 * i + 1], s);
+}
+
 std::mutex g_mutex;
 int* g_err_word[MAX_DEVICES] = {};         // device error word per device (16 bytes)
 int g_arch_ok[MAX_DEVICES] = {};           // 0 unknown, 1 sm_103, -1 other
@@ -168,7 +206,9 @@ fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtens
     }
     const unsigned grid = static_cast<unsigned>(p.split_begin) +
                           static_cast<unsigned>(p.split_units) * static_cast<unsigned>(p.num_splits);
+    const int ti = timer_begin(stream, FA_KERNEL_FWD);
     kernel<<<grid, fa::NUM_THREADS, smem, stream>>>(mq, mk, mv, p);
+    timer_end(stream, ti);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return FA_OK;
@@ -326,6 +366,7 @@ fa_status launch_split(const void* Q, const void* K, const void* V, void* O, flo
     const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
     const int64_t nrows = static_cast<int64_t>(rows);
     const bool bf16 = dtype == FA_BF16;
+    const int ti = timer_begin(strm, FA_KERNEL_MERGE);
     if (D == 128) {
         if (bf16) fa::fa_merge_kernel<128, true><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
         else fa::fa_merge_kernel<128, false><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
@@ -333,6 +374,7 @@ fa_status launch_split(const void* Q, const void* K, const void* V, void* O, flo
         if (bf16) fa::fa_merge_kernel<64, true><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
         else fa::fa_merge_kernel<64, false><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
     }
+    timer_end(strm, ti);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
     return FA_OK;
@@ -406,6 +448,7 @@ fa_status launch_rope(const void* X, void* Y, const float* cos_t, const float* s
     auto y = static_cast<uint16_t*>(Y);
     const bool bf16 = dtype == FA_BF16;
     const unsigned g = static_cast<unsigned>(blocks);
+    const int ti = timer_begin(strm, FA_KERNEL_ROPE);
     if (form == 0) {
         if (bf16) fa::fa_rope_kernel<true, 0><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
         else fa::fa_rope_kernel<false, 0><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
@@ -413,6 +456,7 @@ fa_status launch_rope(const void* X, void* Y, const float* cos_t, const float* s
         if (bf16) fa::fa_rope_kernel<true, 1><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
         else fa::fa_rope_kernel<false, 1><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
     }
+    timer_end(strm, ti);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "rope kernel launch");
     return FA_OK;
@@ -455,10 +499,14 @@ fa_status launch_bwd_instance(int dev, const CUtensorMap& mq, const CUtensorMap&
     }
     const unsigned nkb = static_cast<unsigned>((p.nk + 127) / 128);
     const unsigned nqb = static_cast<unsigned>((p.nq + 127) / 128);
+    int ti = timer_begin(strm, FA_KERNEL_BWD_DKDV);
     k_kv<<<nkb * static_cast<unsigned>(p.bh), fa::BWD_THREADS, smem, strm>>>(mq, mk, mv, mdo, p);
+    timer_end(strm, ti);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
+    ti = timer_begin(strm, FA_KERNEL_BWD_DQ);
     k_q<<<nqb * static_cast<unsigned>(p.bh), fa::BWD_THREADS, smem, strm>>>(mq, mk, mv, mdo, p);
+    timer_end(strm, ti);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "backward dQ launch");
     return FA_OK;
 }
@@ -660,6 +708,7 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
     {
         const int64_t warps = bh * nq_pad;
         const unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
+        const int ti = timer_begin(strm, FA_KERNEL_BWD_PREP);
         if (D == 128) {
             if (bf16) fa::fa_bwd_prep_kernel<128, true><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
             else fa::fa_bwd_prep_kernel<128, false><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
@@ -667,6 +716,7 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
             if (bf16) fa::fa_bwd_prep_kernel<64, true><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
             else fa::fa_bwd_prep_kernel<64, false><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
         }
+        timer_end(strm, ti);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "backward prep launch");
     }
@@ -757,6 +807,51 @@ fa_status fa_release_host_buffers(void) {
         g_staging[dev] = Staging{};
         if (e != cudaSuccess) return cuda_fail(e, "cudaFree(staging)");
     }
+    return FA_OK;
+}
+
+fa_status fa_timer_start(void) {
+    std::lock_guard<std::mutex> lock(g_timer.mu);
+    if (g_timer.on) return fail(FA_ERR_INVALID_ARGUMENT, "kernel timer already running");
+    while (g_timer.created < 2 * KernelTimer::MAX_PAIRS) {
+        cudaError_t e = cudaEventCreate(&g_timer.ev[g_timer.created]);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaEventCreate(kernel timer)");
+        ++g_timer.created;
+    }
+    g_timer.used = 0;
+    g_timer.overflow = false;
+    for (int k = 0; k < FA_KERNEL_KINDS; ++k) {
+        g_timer.ms[k] = 0.0;
+        g_timer.launches[k] = 0;
+    }
+    __atomic_store_n(&g_timer.on, true, __ATOMIC_RELEASE);
+    return FA_OK;
+}
+
+fa_status fa_timer_stop(void) {
+    std::lock_guard<std::mutex> lock(g_timer.mu);
+    if (!g_timer.on) return fail(FA_ERR_INVALID_ARGUMENT, "kernel timer is not running");
+    __atomic_store_n(&g_timer.on, false, __ATOMIC_RELEASE);
+    for (int i = 0; i < g_timer.used; ++i) {
+        cudaError_t e = cudaEventSynchronize(g_timer.ev[2 * i + 1]);
+        float ms = 0.f;
+        if (e == cudaSuccess) e = cudaEventElapsedTime(&ms, g_timer.ev[2 * i], g_timer.ev[2 * i + 1]);
+        if (e != cudaSuccess) return cuda_fail(e, "kernel timer events");
+        g_timer.ms[g_timer.kind[i]] += ms;
+        ++g_timer.launches[g_timer.kind[i]];
+    }
+    if (g_timer.overflow)
+        return fail(FA_ERR_UNSUPPORTED, "more than %d launches timed; the rest were not recorded",
+                    KernelTimer::MAX_PAIRS);
+    return FA_OK;
+}
+
+fa_status fa_timer_read(fa_kernel_kind kind, double* total_ms, int* launches) {
+    if (kind < 0 || kind >= FA_KERNEL_KINDS || !total_ms || !launches)
+        return fail(FA_ERR_INVALID_ARGUMENT, "bad kernel kind or null output");
+    std::lock_guard<std::mutex> lock(g_timer.mu);
+    *total_ms = g_timer.ms[kind];
+    *launches = g_timer.launches[kind];
     return FA_OK;
 }
 

@@ -17,7 +17,7 @@ EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_e
            "fa_set_rescale_threshold", "fa_get_rescale_threshold", "fa_fwd_lse",
            "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_set_tail_split", "fa_rope",
            "fa_rope_workspace_bytes", "fa_fwd_rope", "fa_bwd_workspace_bytes", "fa_bwd",
-           "fa_wait_selftest")
+           "fa_wait_selftest", "fa_timer_start", "fa_timer_stop", "fa_timer_read")
 
 
 class FaError(RuntimeError):
@@ -73,6 +73,13 @@ def lib() -> ctypes.CDLL:
     L.fa_last_device_error.restype = ctypes.c_int
     L.fa_wait_selftest.argtypes = [ctypes.c_ulonglong, vp]
     L.fa_wait_selftest.restype = ctypes.c_int
+    L.fa_timer_start.argtypes = []
+    L.fa_timer_start.restype = ctypes.c_int
+    L.fa_timer_stop.argtypes = []
+    L.fa_timer_stop.restype = ctypes.c_int
+    L.fa_timer_read.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_double),
+                                ctypes.POINTER(ctypes.c_int)]
+    L.fa_timer_read.restype = ctypes.c_int
     L.fa_status_string.argtypes = [ctypes.c_int]
     L.fa_status_string.restype = ctypes.c_char_p
     L.fa_last_error_message.argtypes = []
@@ -322,6 +329,26 @@ def last_device_error(stream=None) -> tuple[int, int]:
     site = ctypes.c_int(0)
     st = lib().fa_last_device_error(stream.cuda_stream, ctypes.byref(site))
     return st, site.value
+
+
+KERNEL_KINDS = ("fwd", "merge", "rope", "bwd_prep", "bwd_dkdv", "bwd_dq")  # fa_kernel_kind order
+
+
+def timer_start() -> None:
+    """Start the library's kernel timer: each launch from now on is bracketed by CUDA events."""
+    _raise_if(lib().fa_timer_start())
+
+
+def timer_stop() -> dict:
+    """Stop the kernel timer; {kind: (total device ms, launches)} for every kind that ran."""
+    _raise_if(lib().fa_timer_stop())
+    out = {}
+    for i, name in enumerate(KERNEL_KINDS):
+        ms, n = ctypes.c_double(0.0), ctypes.c_int(0)
+        _raise_if(lib().fa_timer_read(i, ctypes.byref(ms), ctypes.byref(n)))
+        if n.value:
+            out[name] = (ms.value, n.value)
+    return out
 
 
 def wait_selftest(timeout_ns: int, stream=None) -> None:
