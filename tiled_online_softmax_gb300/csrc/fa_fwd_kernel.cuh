@@ -20,16 +20,16 @@
 // rescaling of ithelp article 10405336, FlashAttention 保留三個狀態); l and O share the
 // reference, so O / l is unchanged and P stays <= 2^threshold.
 //
-// Warp roles (512 threads, registers rebalanced with setmaxnreg):
+// Warp roles (384 threads, registers rebalanced with setmaxnreg):
 //   warpgroup 0 (warps 0-3)  softmax of query tile 0: thread r owns row r (TMEM lane r), so row
 //                            max and sum need no shuffles. When a row of the warp moves its
 //                            reference max, the warp also rescales its rows of O_0 in TMEM.
 //   warpgroup 1 (warps 4-7)  softmax of query tile 1.
-//   warpgroup 2 (warps 8-11) epilogue: O_t / l, rounded, written to global memory.
-//   warp 12                  MMA issuer (an elected lane issues) and TMEM owner.
-//   warp 13                  TMA producer (one lane): Q_0 and Q_1 once, then K and V tiles
+//                            After its key loop each of them writes its tile: O_t / l, rounded.
+//   warp 8                   MMA issuer (an elected lane issues) and TMEM owner.
+//   warp 9                   TMA producer (one lane): Q_0 and Q_1 once, then K and V tiles
 //                            through rings of stages.
-//   warps 14-15              idle.
+//   warps 10-11              idle.
 // The MMA warp issues, per key tile j: PV_0(j) in two halves (keys 0-63 as soon as the softmax
 // releases them, then 64-127), S_0(j+1), PV_1(j) likewise, S_1(j+1). While one tile's softmax
 // runs, the tensor cores work on the other tile's products.
@@ -61,16 +61,19 @@ constexpr int BM = 128;              // query rows per tile = TMEM lanes
 constexpr int BN = 128;              // keys per tile
 constexpr int Q_TILES = 2;           // query tiles per CTA (one work unit = 256 rows)
 constexpr int UNIT_ROWS = BM * Q_TILES;
-constexpr int NUM_THREADS = 512;
-constexpr int MMA_WARP = 12;
-constexpr int LOAD_WARP = 13;
+constexpr int NUM_THREADS = 384;
+constexpr int MMA_WARP = 8;
+constexpr int LOAD_WARP = 9;
 constexpr uint32_t TMEM_COLS = 512;
 __host__ __device__ constexpr uint32_t tmem_s(int t) { return t ? 128u : 0u; }
 __host__ __device__ constexpr uint32_t tmem_o(int t) { return t ? 384u : 256u; }
 
-// Registers per thread after rebalancing; the launch gives 512 x 128.
-constexpr uint32_t REG_SOFTMAX = 184, REG_EPILOGUE = 64, REG_MISC = 72;
-static_assert(8 * 32 * REG_SOFTMAX + 4 * 32 * REG_EPILOGUE + 4 * 32 * REG_MISC <= 512 * 128,
+// Registers per thread after rebalancing. The launch gives each of the 384 threads 168 (the
+// most that fits 65536); the two softmax warpgroups then take 216 each, the MMA/TMA warpgroup
+// keeps 72.
+constexpr uint32_t REG_LAUNCH = 168, REG_SOFTMAX = 216, REG_MISC = 72;
+static_assert(NUM_THREADS * REG_LAUNCH <= 65536, "launch register file");
+static_assert(2 * 128 * REG_SOFTMAX + 128 * REG_MISC <= NUM_THREADS * REG_LAUNCH,
               "setmaxnreg split exceeds the launch's register file");
 
 // Wait-site codes written to the device error word (first timeout wins).
@@ -82,7 +85,6 @@ enum WaitSite : int {
     SITE_MMA_P_FULL = 5,
     SITE_MMA_V_FULL = 6,
     SITE_SOFTMAX_S_FULL = 7,
-    SITE_EPI_L_READY = 8,
     SITE_EPI_O_READY = 9,
     SITE_DRAIN = 10,
     SITE_SELFTEST = 30,   // fa_wait_selftest: a barrier that nothing arrives on
@@ -125,8 +127,7 @@ struct Smem {
     static constexpr int Q_OFF = 0;
     static constexpr int K_OFF = Q_OFF + Q_TILES * Q_TILE_BYTES;
     static constexpr int V_OFF = K_OFF + STAGES * KV_BYTES;
-    static constexpr int ROW_OFF = V_OFF + STAGES * KV_BYTES;   // float [3][2][128]
-    static constexpr int BAR_OFF = ROW_OFF + 3 * Q_TILES * BM * 4;
+    static constexpr int BAR_OFF = V_OFF + STAGES * KV_BYTES;
     // barrier indices
     static constexpr int B_Q_FULL = 0;                          // [2]
     static constexpr int B_K_FULL = B_Q_FULL + Q_TILES;         // [STAGES]
@@ -136,8 +137,7 @@ struct Smem {
     static constexpr int B_S_FULL = B_V_EMPTY + STAGES;         // [2] MMA -> softmax
     static constexpr int B_P_HALF = B_S_FULL + Q_TILES;         // [2] softmax -> MMA (keys 0-63)
     static constexpr int B_P_FULL = B_P_HALF + Q_TILES;         // [2] softmax -> MMA (keys 64-127)
-    static constexpr int B_L_READY = B_P_FULL + Q_TILES;        // [2] softmax -> epilogue
-    static constexpr int B_O_READY = B_L_READY + Q_TILES;       // [2] MMA -> epilogue
+    static constexpr int B_O_READY = B_P_FULL + Q_TILES;        // [2] MMA -> epilogue
     static constexpr int B_DRAIN = B_O_READY + Q_TILES;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + NUM_BARS * 8;
@@ -225,16 +225,85 @@ __device__ __forceinline__ float2 unpack2(uint32_t u) {
 }
 
 // ---------------------------------------------------------------------------------------------
+// epilogue of query tile t (its softmax warpgroup, after the key loop): O_t / l, rounded to the
+// 16-bit type, one row per thread
+// ---------------------------------------------------------------------------------------------
+template <int D, bool BF16>
+__device__ __forceinline__ void epilogue(int t, uint32_t tmem, uint32_t sbase, const Params& p,
+                                         const Ctl& ctl, int bh, int q0, int split, float l,
+                                         float m_ref) {
+    using L = Smem<D>;
+    auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
+    const int r = threadIdx.x & 127;
+    const int warp = threadIdx.x >> 5;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t o_cols = tmem + lane_base + tmem_o(t);
+    const int row = q0 + t * BM + r;
+    if (!wait_bar_warp(bar(L::B_O_READY + t), 0, ctl, SITE_EPI_O_READY)) return;
+    ptx::tc_fence_after();
+    if (split >= 0) {
+        // Partial state over this CTA's keys, merged later (split over keys).
+        const int split_rows = min(UNIT_ROWS, p.nq);
+        const int tu = bh * p.num_units + q0 / UNIT_ROWS - p.split_begin;
+        const size_t prow =
+            (static_cast<size_t>(split) * p.split_units + tu) * split_rows + (row - q0);
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            ptx::tmem_ld32(o_cols + q * 32, o);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(o);
+            if (row < p.nq) {
+                uint4* dst = reinterpret_cast<uint4*>(p.o_part + prow * D + q * 32);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
+            }
+        }
+        if (row < p.nq) reinterpret_cast<float2*>(p.ml_part)[prow] = make_float2(m_ref, l);
+        return;
+    }
+    if (p.lse != nullptr && row < p.nq) {
+        // L = m + log l in natural-log units ("Flash Attention 2", "Write the data back to
+        // HBM"): the kernel's m and l are in base 2 relative to the reference maximum.
+        p.lse[static_cast<size_t>(bh) * p.nq + row] = (m_ref + __log2f(l)) * 0.6931471805599453f;
+    }
+    const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
+    uint8_t* out_row =
+        static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.nq + row) * (D * 2);
+#pragma unroll 1
+    for (int q = 0; q < D / 32; ++q) {
+        uint32_t o[32];
+        ptx::tmem_ld32(o_cols + q * 32, o);
+        ptx::tmem_wait_ld();
+        ptx::reg_fence(o);
+        uint32_t packed[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+            packed[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
+                                    __uint_as_float(o[2 * i + 1]) * inv_l);
+        if (row < p.nq) {
+            uint4* dst = reinterpret_cast<uint4*>(out_row + q * 64);
+#pragma unroll
+            for (int v = 0; v < 4; ++v)
+                dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
+                                    packed[4 * v + 3]);
+        }
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
 // softmax of one query tile (warpgroup t)
 // ---------------------------------------------------------------------------------------------
 template <int D, bool BF16, bool CAUSAL>
-__device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbase, float* rows,
-                                             const Params& p, const Ctl& ctl, int q_tile0,
-                                             int kv0, int n_tiles) {
+__device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbase,
+                                             const Params& p, const Ctl& ctl, int bh, int q0,
+                                             int split, int kv0, int n_tiles) {
     using L = Smem<D>;
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     const int r = threadIdx.x & 127;          // row within the tile = TMEM lane
     const int warp = threadIdx.x >> 5;
+    const int q_tile0 = q0 + t * BM;
     const int row = q_tile0 + r;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t s_cols = tmem + lane_base + tmem_s(t);
@@ -244,8 +313,6 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
     const float c = (p.scale_log2 == 0.f) ? 1e-30f : p.scale_log2;
     const bool neg = c < 0.f;
     const float tau = p.rescale_threshold;
-    float* row_l = rows + (1 * Q_TILES + t) * BM;
-    float* row_m = rows + (2 * Q_TILES + t) * BM;
     float m_ref = -INFINITY;  // reference max of the scaled scores (log2 units)
     float l = 0.f;            // running denominator relative to m_ref
 
@@ -253,8 +320,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
         if (!wait_bar_warp(bar(L::B_S_FULL + t), j & 1, ctl, SITE_SOFTMAX_S_FULL)) return;
         ptx::tc_fence_after();
         uint32_t sr[4][32];
-#pragma unroll
-        for (int q = 0; q < 4; ++q) ptx::tmem_ld32(s_cols + q * 32, sr[q]);
+        ptx::tmem_ld128(s_cols, sr);
         ptx::tmem_wait_ld();
 #pragma unroll
         for (int q = 0; q < 4; ++q) ptx::reg_fence(sr[q]);
@@ -273,26 +339,29 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
                     if (q * 32 + i >= lim) sr[q][i] = hidden;
         }
 
-        // Tile maximum on the raw scores (scaling by c >= 0 is monotone; c < 0 uses the min).
+        // Tile maximum on the raw scores (scaling by c >= 0 is monotone; c < 0 uses the min),
+        // as four independent chains per block of 32 columns: chain c of block q covers columns
+        // c, c + 4, c + 8, ... so the 3-input steps of different chains overlap.
         float mx[4];
-        if (!neg) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float a = __uint_as_float(sr[q][0]);
+        for (int q = 0; q < 4; ++q) {
+            float ch[4];
 #pragma unroll
-                for (int i = 1; i < 31; i += 2)
-                    a = ptx::fmax3(a, __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]));
-                mx[q] = fmaxf(a, __uint_as_float(sr[q][31]));
-            }
-        } else {
+            for (int c = 0; c < 4; ++c) ch[c] = __uint_as_float(sr[q][c]);
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                float a = __uint_as_float(sr[q][0]);
+            for (int i = 4; i < 28; i += 8)
 #pragma unroll
-                for (int i = 1; i < 31; i += 2)
-                    a = ptx::fmin3(a, __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]));
-                mx[q] = fminf(a, __uint_as_float(sr[q][31]));
-            }
+                for (int c = 0; c < 4; ++c)
+                    ch[c] = neg ? ptx::fmin3(ch[c], __uint_as_float(sr[q][i + c]),
+                                             __uint_as_float(sr[q][i + 4 + c]))
+                                : ptx::fmax3(ch[c], __uint_as_float(sr[q][i + c]),
+                                             __uint_as_float(sr[q][i + 4 + c]));
+#pragma unroll
+            for (int c = 0; c < 4; ++c)
+                ch[c] = neg ? fminf(ch[c], __uint_as_float(sr[q][28 + c]))
+                            : fmaxf(ch[c], __uint_as_float(sr[q][28 + c]));
+            mx[q] = neg ? fminf(fminf(ch[0], ch[1]), fminf(ch[2], ch[3]))
+                        : fmaxf(fmaxf(ch[0], ch[1]), fmaxf(ch[2], ch[3]));
         }
         const float mraw = neg ? fminf(fminf(mx[0], mx[1]), fminf(mx[2], mx[3]))
                                : fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
@@ -357,85 +426,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
             ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         l = l * corr + rowsum;
     }
-    row_l[r] = l;
-    row_m[r] = m_ref;
-    ptx::mbar_arrive(bar(L::B_L_READY + t));
-}
-
-// ---------------------------------------------------------------------------------------------
-// epilogue (warpgroup 2): O_t / l, rounded to the 16-bit type, one row per thread
-// ---------------------------------------------------------------------------------------------
-template <int D, bool BF16>
-__device__ __forceinline__ void epilogue_role(uint32_t tmem, uint32_t sbase, const float* rows,
-                                              const Params& p, const Ctl& ctl, int bh, int q0,
-                                              int split) {
-    using L = Smem<D>;
-    auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
-    const int r = threadIdx.x & 127;
-    const int warp = threadIdx.x >> 5;
-    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-#pragma unroll
-    for (int t = 0; t < Q_TILES; ++t) {
-        if (!wait_bar_warp(bar(L::B_L_READY + t), 0, ctl, SITE_EPI_L_READY)) return;
-        const float l = rows[(1 * Q_TILES + t) * BM + r];
-        const int row = q0 + t * BM + r;
-        if (split >= 0) {
-            // Partial state over this CTA's keys, merged later (split over keys).
-            if (!wait_bar_warp(bar(L::B_O_READY + t), 0, ctl, SITE_EPI_O_READY)) return;
-            ptx::tc_fence_after();
-            const int split_rows = min(UNIT_ROWS, p.nq);
-            const int tu = bh * p.num_units + q0 / UNIT_ROWS - p.split_begin;
-            const size_t prow =
-                (static_cast<size_t>(split) * p.split_units + tu) * split_rows + (row - q0);
-            const uint32_t o_cols = tmem + lane_base + tmem_o(t);
-#pragma unroll 1
-            for (int q = 0; q < D / 16; ++q) {
-                uint32_t o[16];
-                ptx::tmem_ld16(o_cols + q * 16, o);
-                ptx::tmem_wait_ld();
-                ptx::reg_fence(o);
-                if (row < p.nq) {
-                    uint4* dst = reinterpret_cast<uint4*>(p.o_part + prow * D + q * 16);
-#pragma unroll
-                    for (int v = 0; v < 4; ++v)
-                        dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
-                }
-            }
-            if (row < p.nq)
-                reinterpret_cast<float2*>(p.ml_part)[prow] =
-                    make_float2(rows[(2 * Q_TILES + t) * BM + r], l);
-            continue;
-        }
-        if (p.lse != nullptr && row < p.nq) {
-            // L = m + log l in natural-log units ("Flash Attention 2", "Write the data back to
-            // HBM"): the kernel's m and l are in base 2 relative to the reference maximum.
-            const float m2 = rows[(2 * Q_TILES + t) * BM + r];
-            p.lse[static_cast<size_t>(bh) * p.nq + row] = (m2 + __log2f(l)) * 0.6931471805599453f;
-        }
-        if (!wait_bar_warp(bar(L::B_O_READY + t), 0, ctl, SITE_EPI_O_READY)) return;
-        ptx::tc_fence_after();
-        const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-        const uint32_t o_cols = tmem + lane_base + tmem_o(t);
-        uint8_t* out_row =
-            static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.nq + row) * (D * 2);
-#pragma unroll 1
-        for (int q = 0; q < D / 16; ++q) {
-            uint32_t o[16];
-            ptx::tmem_ld16(o_cols + q * 16, o);
-            ptx::tmem_wait_ld();
-            ptx::reg_fence(o);
-            uint32_t packed[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i)
-                packed[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
-                                        __uint_as_float(o[2 * i + 1]) * inv_l);
-            if (row < p.nq) {
-                uint4* dst = reinterpret_cast<uint4*>(out_row + q * 32);
-                dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-                dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
-            }
-        }
-    }
+    epilogue<D, BF16>(t, tmem, sbase, p, ctl, bh, q0, split, l, m_ref);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -454,7 +445,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::ABORT_OFF);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + L::TMEM_SLOT_OFF);
-    float* rows = reinterpret_cast<float*>(smem + L::ROW_OFF);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -493,7 +483,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(bar(L::B_S_FULL + t), 1);
             ptx::mbar_init(bar(L::B_P_HALF + t), BM);
             ptx::mbar_init(bar(L::B_P_FULL + t), BM);
-            ptx::mbar_init(bar(L::B_L_READY + t), BM);
             ptx::mbar_init(bar(L::B_O_READY + t), 1);
         }
         for (int s = 0; s < STAGES; ++s) {
@@ -521,7 +510,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const Ctl ctl{abort_flag, p.err, p.timeout_ns};
 
-    if (wg == 3) {
+    if (wg == 2) {
         ptx::regs_dec<REG_MISC>();
         if (warp == LOAD_WARP) {
             // -------------------------------------------------------------- TMA producer
@@ -654,12 +643,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             __syncwarp();
         }
-    } else if (wg == 2) {
-        ptx::regs_dec<REG_EPILOGUE>();
-        epilogue_role<D, BF16>(tmem, sbase, rows, p, ctl, bh, q0, split);
     } else {
         ptx::regs_inc<REG_SOFTMAX>();
-        softmax_role<D, BF16, CAUSAL>(wg, tmem, sbase, rows, p, ctl, q0 + wg * BM, kv0, n_tiles[wg]);
+        softmax_role<D, BF16, CAUSAL>(wg, tmem, sbase, p, ctl, bh, q0, split, kv0, n_tiles[wg]);
         ptx::tmem_wait_st();  // no TMEM store of this warp may be pending at dealloc
     }
 
