@@ -113,3 +113,36 @@ def test_last_wave_split_matches_oracle_and_unsplit(fa):
     diff = np.abs(inputs.bits_to_f64(got, "bf16") - inputs.bits_to_f64(inputs.from_torch(o_plain), "bf16"))
     assert diff[0, :38].max() == 0.0  # whole units: identical bits
     assert diff.max() <= 2e-2
+
+
+def test_last_wave_split_workspace_is_reused_across_calls(fa):
+    """The split last wave's partial states live in a workspace shared by every call: calls of
+    two shapes interleaved (ragged rows, both head dims, both dtypes) give the same bits every
+    time and match the unsplit launch and the oracle."""
+    shapes = [inputs.Workload("tail_a", 1, 40, 2048, 1024, 64, "bf16", False, seed=58),
+              inputs.Workload("tail_b", 1, 10, 4000, 2000, 128, "f16", False, seed=59)]
+    data = []
+    for w in shapes:
+        bits = inputs.draw(w)
+        q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+        try:
+            fa.set_tail_split(False)
+            plain = inputs.from_torch(fa.forward(q, k, v, scale=w.scale))
+        finally:
+            fa.set_tail_split(True)
+        data.append((w, bits, (q, k, v), plain))
+    first = {}
+    for rep in range(3):
+        for w, bits, (q, k, v), plain in data:
+            got = inputs.from_torch(fa.forward(q, k, v, scale=w.scale))
+            assert fa.last_device_error() == (0, 0)
+            if w.name in first:
+                assert np.array_equal(got, first[w.name]), f"{w.name} changed on call {rep}"
+                continue
+            first[w.name] = got
+            diff = np.abs(inputs.bits_to_f64(got, w.dtype) - inputs.bits_to_f64(plain, w.dtype))
+            assert diff.max() <= 2e-2
+            h = w.H - 1  # the last head's units are in the split wave
+            ref = oracle.attention(*(inputs.bits_to_f64(bits[n][0, h], w.dtype) for n in "qkv"),
+                                   w.scale, False)
+            parity.assert_parity(parity.compare(got[0, h], ref, w.dtype), True, f"{w.name} head {h}")

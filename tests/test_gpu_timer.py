@@ -18,19 +18,21 @@ def fa():
 
 
 def test_timer_counts_launches_by_kind(fa):
-    # 40 slices x 8 units of 256 rows = 320 units: 2 full waves of 152 and a last wave of 16,
-    # which is split over keys, so each forward call is an attention launch and a merge.
-    w = inputs.Workload("timer", 1, 40, 2048, 1024, 64, "bf16", False, seed=91)
+    # A decoding shape split over keys: each call is an attention launch and a merge launch.
+    w = inputs.Workload("timer", 1, 4, 64, 4096, 64, "bf16", False, seed=91)
     bits = inputs.draw(w)
     q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
-    fa.forward(q, k, v, scale=w.scale)
+    ws = torch.empty(fa.splitkv_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.D, 8), dtype=torch.uint8,
+                     device="cuda")
+    run = lambda: fa.forward_splitkv(q, k, v, num_splits=8, scale=w.scale, workspace=ws)
+    run()
     torch.cuda.synchronize()
     stream = torch.cuda.current_stream()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     fa.timer_start()
     e0.record(stream)
     for _ in range(5):
-        fa.forward(q, k, v, scale=w.scale)
+        run()
     e1.record(stream)
     torch.cuda.synchronize()
     kernels = fa.timer_stop()
@@ -41,7 +43,7 @@ def test_timer_counts_launches_by_kind(fa):
     assert 0 < timed <= total * 1.001
     assert kernels["fwd"][0] > kernels["merge"][0]
     # Stopped: further launches are not counted, and a second stop is an error.
-    fa.forward(q, k, v, scale=w.scale)
+    run()
     with pytest.raises(fa.FaError):
         fa.timer_stop()
     assert fa.last_device_error() == (0, 0)
