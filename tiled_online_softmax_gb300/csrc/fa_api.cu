@@ -193,7 +193,8 @@ fa_status device_state(int* dev_out, int** err_out) {
 
 template <int D, bool BF16, bool CAUSAL>
 fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtensorMap& mk,
-                          const CUtensorMap& mv, const fa::Params& p, cudaStream_t stream) {
+                          const CUtensorMap& mv, const CUtensorMap& mo, const fa::Params& p,
+                          cudaStream_t stream) {
     auto kernel = fa::fa_fwd_kernel<D, BF16, CAUSAL>;
     constexpr int smem = fa::Smem<D>::ALLOC_BYTES;
     {
@@ -207,7 +208,7 @@ fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtens
     const unsigned grid = static_cast<unsigned>(p.split_begin) +
                           static_cast<unsigned>(p.split_units) * static_cast<unsigned>(p.num_splits);
     const int ti = timer_begin(stream, FA_KERNEL_FWD);
-    kernel<<<grid, fa::NUM_THREADS, smem, stream>>>(mq, mk, mv, p);
+    kernel<<<grid, fa::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, p);
     timer_end(stream, ti);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
@@ -233,10 +234,11 @@ fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LS
     fa_status s = device_state(&dev, &err);
     if (s != FA_OK) return s;
     const int64_t bh = B * H;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if ((s = encode_map(&mq, Q, bh, Nq, D, dtype)) != FA_OK) return s;
     if ((s = encode_map(&mk, K, bh, Nk, D, dtype)) != FA_OK) return s;
     if ((s = encode_map(&mv, V, bh, Nk, D, dtype)) != FA_OK) return s;
+    if ((s = encode_map(&mo, O, bh, Nq, D, dtype)) != FA_OK) return s;
     fa::Params p{};
     p.o = O;
     p.lse = LSE;
@@ -260,14 +262,14 @@ fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LS
     const bool bf16 = dtype == FA_BF16;
     const int inst = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
     switch (inst) {
-        case 0: return launch_instance<64, false, false>(dev, inst, mq, mk, mv, p, stream);
-        case 1: return launch_instance<64, false, true>(dev, inst, mq, mk, mv, p, stream);
-        case 2: return launch_instance<64, true, false>(dev, inst, mq, mk, mv, p, stream);
-        case 3: return launch_instance<64, true, true>(dev, inst, mq, mk, mv, p, stream);
-        case 4: return launch_instance<128, false, false>(dev, inst, mq, mk, mv, p, stream);
-        case 5: return launch_instance<128, false, true>(dev, inst, mq, mk, mv, p, stream);
-        case 6: return launch_instance<128, true, false>(dev, inst, mq, mk, mv, p, stream);
-        default: return launch_instance<128, true, true>(dev, inst, mq, mk, mv, p, stream);
+        case 0: return launch_instance<64, false, false>(dev, inst, mq, mk, mv, mo, p, stream);
+        case 1: return launch_instance<64, false, true>(dev, inst, mq, mk, mv, mo, p, stream);
+        case 2: return launch_instance<64, true, false>(dev, inst, mq, mk, mv, mo, p, stream);
+        case 3: return launch_instance<64, true, true>(dev, inst, mq, mk, mv, mo, p, stream);
+        case 4: return launch_instance<128, false, false>(dev, inst, mq, mk, mv, mo, p, stream);
+        case 5: return launch_instance<128, false, true>(dev, inst, mq, mk, mv, mo, p, stream);
+        case 6: return launch_instance<128, true, false>(dev, inst, mq, mk, mv, mo, p, stream);
+        default: return launch_instance<128, true, true>(dev, inst, mq, mk, mv, mo, p, stream);
     }
 }
 
@@ -530,10 +532,11 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, i
     cudaError_t e = cudaMemsetAsync(scratch, 0, NOALLOC_RECORD_BYTES, strm);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync(scratch)");
     const int64_t bh = B * H;
-    CUtensorMap mq, mk, mv;
+    CUtensorMap mq, mk, mv, mo;
     if ((s = encode_map(&mq, Q, bh, Nq, D, int(dtype))) != FA_OK) return s;
     if ((s = encode_map(&mk, K, bh, Nk, D, int(dtype))) != FA_OK) return s;
     if ((s = encode_map(&mv, V, bh, Nk, D, int(dtype))) != FA_OK) return s;
+    if ((s = encode_map(&mo, O, bh, Nq, D, int(dtype))) != FA_OK) return s;
     fa::Params p{};
     p.o = O;
     p.lse = nullptr;
@@ -551,14 +554,14 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, i
     p.timeout_ns = wait_timeout_ns();
     const int inst = (D == 128 ? 4 : 0) + (dtype == FA_BF16 ? 2 : 0) + (causal ? 1 : 0);
     switch (inst) {
-        case 0: return launch_instance<64, false, false>(dev, inst, mq, mk, mv, p, strm);
-        case 1: return launch_instance<64, false, true>(dev, inst, mq, mk, mv, p, strm);
-        case 2: return launch_instance<64, true, false>(dev, inst, mq, mk, mv, p, strm);
-        case 3: return launch_instance<64, true, true>(dev, inst, mq, mk, mv, p, strm);
-        case 4: return launch_instance<128, false, false>(dev, inst, mq, mk, mv, p, strm);
-        case 5: return launch_instance<128, false, true>(dev, inst, mq, mk, mv, p, strm);
-        case 6: return launch_instance<128, true, false>(dev, inst, mq, mk, mv, p, strm);
-        default: return launch_instance<128, true, true>(dev, inst, mq, mk, mv, p, strm);
+        case 0: return launch_instance<64, false, false>(dev, inst, mq, mk, mv, mo, p, strm);
+        case 1: return launch_instance<64, false, true>(dev, inst, mq, mk, mv, mo, p, strm);
+        case 2: return launch_instance<64, true, false>(dev, inst, mq, mk, mv, mo, p, strm);
+        case 3: return launch_instance<64, true, true>(dev, inst, mq, mk, mv, mo, p, strm);
+        case 4: return launch_instance<128, false, false>(dev, inst, mq, mk, mv, mo, p, strm);
+        case 5: return launch_instance<128, false, true>(dev, inst, mq, mk, mv, mo, p, strm);
+        case 6: return launch_instance<128, true, false>(dev, inst, mq, mk, mv, mo, p, strm);
+        default: return launch_instance<128, true, true>(dev, inst, mq, mk, mv, mo, p, strm);
     }
 }
 

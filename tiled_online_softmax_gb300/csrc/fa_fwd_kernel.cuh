@@ -87,6 +87,7 @@ enum WaitSite : int {
     SITE_SOFTMAX_S_FULL = 7,
     SITE_EPI_O_READY = 9,
     SITE_DRAIN = 10,
+    SITE_EPI_O_STAGED = 14,
     SITE_SELFTEST = 30,   // fa_wait_selftest: a barrier that nothing arrives on
 };
 
@@ -138,7 +139,8 @@ struct Smem {
     static constexpr int B_P_HALF = B_S_FULL + Q_TILES;         // [2] softmax -> MMA (keys 0-63)
     static constexpr int B_P_FULL = B_P_HALF + Q_TILES;         // [2] softmax -> MMA (keys 64-127)
     static constexpr int B_O_READY = B_P_FULL + Q_TILES;        // [2] MMA -> epilogue
-    static constexpr int B_DRAIN = B_O_READY + Q_TILES;
+    static constexpr int B_O_STAGED = B_O_READY + Q_TILES;      // [2] O_t in smem (4 warps)
+    static constexpr int B_DRAIN = B_O_STAGED + Q_TILES;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
@@ -231,7 +233,7 @@ __device__ __forceinline__ float2 unpack2(uint32_t u) {
 template <int D, bool BF16>
 __device__ __forceinline__ void epilogue(int t, uint32_t tmem, uint32_t sbase, const Params& p,
                                          const Ctl& ctl, int bh, int q0, int split, float l,
-                                         float m_ref) {
+                                         float m_ref, const CUtensorMap* tm_o) {
     using L = Smem<D>;
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     const int r = threadIdx.x & 127;
@@ -268,9 +270,11 @@ __device__ __forceinline__ void epilogue(int t, uint32_t tmem, uint32_t sbase, c
         // HBM"): the kernel's m and l are in base 2 relative to the reference maximum.
         p.lse[static_cast<size_t>(bh) * p.nq + row] = (m_ref + __log2f(l)) * 0.6931471805599453f;
     }
+    // O_t / l, rounded, staged in shared memory over Q_t (whose last reader, S_t of the last key
+    // tile, finished before O_READY_t) in the 128-byte-swizzled layout of the tensor map, then
+    // written by TMA: whole 128-byte row segments instead of one 16-byte store per row.
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
-    uint8_t* out_row =
-        static_cast<uint8_t*>(p.o) + (static_cast<size_t>(bh) * p.nq + row) * (D * 2);
+    const uint32_t stage = sbase + L::Q_OFF + t * L::Q_TILE_BYTES;
 #pragma unroll 1
     for (int q = 0; q < D / 32; ++q) {
         uint32_t o[32];
@@ -282,13 +286,26 @@ __device__ __forceinline__ void epilogue(int t, uint32_t tmem, uint32_t sbase, c
         for (int i = 0; i < 16; ++i)
             packed[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
                                     __uint_as_float(o[2 * i + 1]) * inv_l);
-        if (row < p.nq) {
-            uint4* dst = reinterpret_cast<uint4*>(out_row + q * 64);
+        // 32 columns = 4 chunks of 16 bytes in column block q / 2, chunks 4 (q % 2) + v of the
+        // row; chunk c of row r sits at chunk position c ^ (r % 8).
+        const uint32_t row_base = stage + (q / 2) * (BM * 128) + r * 128;
 #pragma unroll
-            for (int v = 0; v < 4; ++v)
-                dst[v] = make_uint4(packed[4 * v], packed[4 * v + 1], packed[4 * v + 2],
-                                    packed[4 * v + 3]);
+        for (int v = 0; v < 4; ++v) {
+            const uint32_t c = (q % 2) * 4 + v;
+            ptx::st_shared_v4(row_base + ((c ^ (r & 7)) << 4), packed[4 * v], packed[4 * v + 1],
+                              packed[4 * v + 2], packed[4 * v + 3]);
         }
+    }
+    ptx::fence_proxy_async_smem();  // the TMA store reads what these threads wrote
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar(L::B_O_STAGED + t));
+    if (r == 0) {
+        if (!wait_bar(bar(L::B_O_STAGED + t), 0, ctl, SITE_EPI_O_STAGED)) return;
+#pragma unroll
+        for (int cb = 0; cb < D / 64; ++cb)
+            ptx::tma_store_3d(tm_o, stage + cb * (BM * 128), cb * 64, q0 + t * BM, bh);
+        ptx::bulk_commit_group();
+        ptx::bulk_wait_group_read0();  // shared memory stays allocated until the copy has read it
     }
 }
 
@@ -298,7 +315,8 @@ __device__ __forceinline__ void epilogue(int t, uint32_t tmem, uint32_t sbase, c
 template <int D, bool BF16, bool CAUSAL>
 __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbase,
                                              const Params& p, const Ctl& ctl, int bh, int q0,
-                                             int split, int kv0, int n_tiles) {
+                                             int split, int kv0, int n_tiles,
+                                             const CUtensorMap* tm_o) {
     using L = Smem<D>;
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     const int r = threadIdx.x & 127;          // row within the tile = TMEM lane
@@ -426,7 +444,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
             ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
         l = l * corr + rowsum;
     }
-    epilogue<D, BF16>(t, tmem, sbase, p, ctl, bh, q0, split, l, m_ref);
+    epilogue<D, BF16>(t, tmem, sbase, p, ctl, bh, q0, split, l, m_ref, tm_o);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -435,7 +453,8 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     fa_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
-                  const __grid_constant__ CUtensorMap tm_v, const Params p) {
+                  const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_o,
+                  const Params p) {
     using L = Smem<D>;
     constexpr int STAGES = L::STAGES;
     extern __shared__ uint8_t smem_raw[];
@@ -484,6 +503,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(bar(L::B_P_HALF + t), BM);
             ptx::mbar_init(bar(L::B_P_FULL + t), BM);
             ptx::mbar_init(bar(L::B_O_READY + t), 1);
+            ptx::mbar_init(bar(L::B_O_STAGED + t), 4);
         }
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar(L::B_K_FULL + s), 1);
@@ -499,6 +519,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tensormap(&tm_q);
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
+        ptx::prefetch_tensormap(&tm_o);
     }
     if (warp == MMA_WARP) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
@@ -645,7 +666,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         ptx::regs_inc<REG_SOFTMAX>();
-        softmax_role<D, BF16, CAUSAL>(wg, tmem, sbase, p, ctl, bh, q0, split, kv0, n_tiles[wg]);
+        softmax_role<D, BF16, CAUSAL>(wg, tmem, sbase, p, ctl, bh, q0, split, kv0, n_tiles[wg],
+                                      &tm_o);
         ptx::tmem_wait_st();  // no TMEM store of this warp may be pending at dealloc
     }
 
