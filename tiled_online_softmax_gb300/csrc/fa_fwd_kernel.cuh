@@ -94,6 +94,9 @@ enum WaitSite : int {
 // Floor of the time limit of drain waits (for copies and MMAs this CTA started, which always
 // complete): a short limit for the ordinary waits never lets a CTA exit with copies in flight.
 constexpr unsigned long long DRAIN_FLOOR_NS = 1000000000ull;
+// Longest sleep of one try inside a bounded wait (the waiting thread wakes as soon as the phase
+// completes); the time limit is checked every 32 tries.
+constexpr uint32_t WAIT_SLEEP_NS = 2000;
 
 struct Params {
     void* o;                   // output [bh][nq][D]
@@ -170,7 +173,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, const Ct
     const uint64_t limit =
         honor_abort || ctl.timeout_ns >= DRAIN_FLOOR_NS ? ctl.timeout_ns : DRAIN_FLOOR_NS;
     for (uint32_t it = 1;; ++it) {
-        if (ptx::mbar_try_wait(bar, parity)) return true;
+        if (ptx::mbar_try_wait_sleep(bar, parity, WAIT_SLEEP_NS)) return true;
         if ((it & 31u) == 0) {
             if (honor_abort && *ctl.abort) return false;
             if (ptx::globaltimer_ns() - t0 > limit) {
