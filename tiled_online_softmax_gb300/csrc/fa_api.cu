@@ -368,16 +368,32 @@ fa_status launch_split(const void* Q, const void* K, const void* V, void* O, flo
     const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
     const int64_t nrows = static_cast<int64_t>(rows);
     const bool bf16 = dtype == FA_BF16;
+    // Programmatic dependent launch: the merge grid may be scheduled while the attention kernel's
+    // last CTAs still run (they signal it at their start); each merge block first waits, in
+    // griddepcontrol.wait, for the attention kernel to complete and its writes to be visible.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(blocks);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = strm;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const float* op = sp.o_part;
+    const float* mp = sp.ml_part;
+    const int ns = plan.num_splits;
     const int ti = timer_begin(strm, FA_KERNEL_MERGE);
-    if (D == 128) {
-        if (bf16) fa::fa_merge_kernel<128, true><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
-        else fa::fa_merge_kernel<128, false><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
-    } else {
-        if (bf16) fa::fa_merge_kernel<64, true><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
-        else fa::fa_merge_kernel<64, false><<<blocks, 256, 0, strm>>>(sp.o_part, sp.ml_part, O, LSE, nrows, plan.num_splits, map);
-    }
+    cudaError_t e;
+    if (D == 128)
+        e = bf16 ? cudaLaunchKernelEx(&cfg, fa::fa_merge_kernel<128, true>, op, mp, O, LSE, nrows, ns, map)
+                 : cudaLaunchKernelEx(&cfg, fa::fa_merge_kernel<128, false>, op, mp, O, LSE, nrows, ns, map);
+    else
+        e = bf16 ? cudaLaunchKernelEx(&cfg, fa::fa_merge_kernel<64, true>, op, mp, O, LSE, nrows, ns, map)
+                 : cudaLaunchKernelEx(&cfg, fa::fa_merge_kernel<64, false>, op, mp, O, LSE, nrows, ns, map);
     timer_end(strm, ti);
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "merge kernel launch");
     return FA_OK;
 }

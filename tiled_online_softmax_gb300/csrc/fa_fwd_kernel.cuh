@@ -533,6 +533,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Ctl ctl{abort_flag, p.err, p.timeout_ns};
+    // A grid launched after this one as a programmatic dependent (the merge of split key ranges)
+    // may be scheduled once every CTA of this grid has started; it still waits for this grid to
+    // complete before reading anything.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (wg == 2) {
         ptx::regs_dec<REG_MISC>();

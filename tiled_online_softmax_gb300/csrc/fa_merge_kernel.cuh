@@ -31,6 +31,9 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__
                                                        void* __restrict__ o, float* __restrict__ lse,
                                                        int64_t rows, int num_splits, MergeMap map) {
     constexpr int E = D / 32;
+    // Launched as a programmatic dependent of the attention kernel: wait until that grid has
+    // completed and its partial states are visible (a no-op for an ordinary launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // 32-bit index arithmetic: rows, units and query rows all fit in int (checked on the host).
     const int row = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
