@@ -502,6 +502,7 @@ fa_status launch_bwd_instance(int dev, const CUtensorMap& mq, const CUtensorMap&
                               const CUtensorMap& mv, const CUtensorMap& mdo, const fa::BwdParams& p,
                               cudaStream_t strm) {
     constexpr int smem = fa::BwdSmem<D>::ALLOC_BYTES;
+    constexpr int smem_q = fa::DqSmem<D>::ALLOC_BYTES;
     auto k_kv = fa::fa_bwd_dkdv_kernel<D, BF16, CAUSAL>;
     auto k_q = fa::fa_bwd_dq_kernel<D, BF16, CAUSAL>;
     static unsigned attr_set[MAX_DEVICES] = {};  // one per template instance
@@ -510,7 +511,7 @@ fa_status launch_bwd_instance(int dev, const CUtensorMap& mq, const CUtensorMap&
         if (!attr_set[dev]) {
             cudaError_t e;
             if ((e = cudaFuncSetAttribute(k_kv, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess ||
-                (e = cudaFuncSetAttribute(k_q, cudaFuncAttributeMaxDynamicSharedMemorySize, smem)) != cudaSuccess)
+                (e = cudaFuncSetAttribute(k_q, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_q)) != cudaSuccess)
                 return cuda_fail(e, "cudaFuncSetAttribute(backward)");
             attr_set[dev] = 1;
         }
@@ -523,7 +524,7 @@ fa_status launch_bwd_instance(int dev, const CUtensorMap& mq, const CUtensorMap&
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
     ti = timer_begin(strm, FA_KERNEL_BWD_DQ);
-    k_q<<<nqb * static_cast<unsigned>(p.bh), fa::BWD_THREADS, smem, strm>>>(mq, mk, mv, mdo, p);
+    k_q<<<nqb * static_cast<unsigned>(p.bh), fa::BWD_THREADS, smem_q, strm>>>(mq, mk, mv, mdo, p);
     timer_end(strm, ti);
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "backward dQ launch");
     return FA_OK;

@@ -11,8 +11,8 @@
 //   fa_bwd_dkdv_kernel  one CTA per 128 keys: S^T = K Q_i^T and dP^T = V dO_i^T into TMEM,
 //                       P^T and dS^T rounded to 16 bits over them, dV += P^T dO_i and
 //                       dK += dS^T Q_i accumulating in TMEM, over every query block i.
-//   fa_bwd_dq_kernel    one CTA per 128 queries: S = Q K_j^T and dP = dO V_j^T, dS over S,
-//                       dQ += dS K_j, over every key block j.
+//   fa_bwd_dq_kernel    one CTA per 128 queries: S = Q K_j^T (two TMEM buffers, computed ahead)
+//                       and dP = dO V_j^T, dS over S, dQ += dS K_j, over every key block j.
 // Warp roles (192 threads): warps 0-3 compute (thread r owns TMEM lane r: a key row in the
 // first kernel, a query row in the second), warp 4 issues MMAs (an elected lane) and owns TMEM,
 // warp 5 issues TMA copies. Every wait is bounded as in the forward kernel.
@@ -417,15 +417,47 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 }
 
 // ---------------------------------------------------------------------------------------------
-// dQ: one CTA per (slice, 128 queries); resident Q (R0) and dO (R1); ring A = K_j, ring B = V_j
+// dQ: one CTA per (slice, 128 queries); resident Q and dO; a ring of K tiles, a ring of V tiles
 // ---------------------------------------------------------------------------------------------
+// S_j = Q K_j^T alternates between two TMEM buffers (columns 0-127 and 384-511), so S_{j+1} and
+// S_{j+2} are computed while the compute warps turn S_j and dP_j into dS_j. MMA order:
+//   S_0, dP_0, S_1,  then per j: dQ += dS_j K_j, dP_{j+1}, S_{j+2} (over dS_j's buffer).
+// K_j serves S_j and the dQ product of block j, so the K ring holds three tiles.
+template <int D>
+struct DqSmem {
+    static constexpr int TILE = 128 * D * 2;
+    static constexpr int K_STAGES = 3, V_STAGES = 2;
+    static constexpr int Q_OFF = 0;
+    static constexpr int DO_OFF = TILE;
+    static constexpr int K_OFF = 2 * TILE;
+    static constexpr int V_OFF = K_OFF + K_STAGES * TILE;
+    static constexpr int BAR_OFF = V_OFF + V_STAGES * TILE;
+    static constexpr int B_RES_FULL = 0;
+    static constexpr int B_K_FULL = 1;                         // [K_STAGES]
+    static constexpr int B_K_EMPTY = B_K_FULL + K_STAGES;      // [K_STAGES]
+    static constexpr int B_V_FULL = B_K_EMPTY + K_STAGES;      // [V_STAGES]
+    static constexpr int B_V_EMPTY = B_V_FULL + V_STAGES;      // [V_STAGES]
+    static constexpr int B_S_FULL = B_V_EMPTY + V_STAGES;      // [2] per S buffer
+    static constexpr int B_DP_FULL = B_S_FULL + 2;
+    static constexpr int B_DS_FULL = B_DP_FULL + 1;
+    static constexpr int B_MMA_DONE = B_DS_FULL + 1;
+    static constexpr int B_DRAIN = B_MMA_DONE + 1;
+    static constexpr int NUM_BARS = B_DRAIN + 1;
+    static constexpr int TMEM_SLOT_OFF = BAR_OFF + NUM_BARS * 8;
+    static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
+    static constexpr int BYTES = ABORT_OFF + 4;
+    static constexpr int ALLOC_BYTES = (BYTES + 1024 > 116 * 1024) ? BYTES + 1024 : 116 * 1024;
+    static_assert(ALLOC_BYTES <= 232448, "shared memory budget");
+};
+constexpr uint32_t DQ_TMEM_S0 = 0, DQ_TMEM_DP = 128, DQ_TMEM_DQ = 256, DQ_TMEM_S1 = 384;
+
 template <int D, bool BF16, bool CAUSAL>
 __global__ void __launch_bounds__(BWD_THREADS, 1)
     fa_bwd_dq_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                      const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                      const BwdParams p) {
-    using L = BwdSmem<D>;
-    constexpr int STAGES = L::STAGES;
+    using L = DqSmem<D>;
+    constexpr int KS = L::K_STAGES, VS = L::V_STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
     uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
@@ -439,30 +471,62 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int bh = blockIdx.x / nqb, qb = blockIdx.x % nqb;
     const int q0 = qb * 128;
     const int n = CAUSAL ? min(nkb, qb + 1) : nkb;  // key blocks up to the diagonal
-    const uint32_t tmem = bwd_setup<D>(smem, sbase, ptx::smem_u32(tmem_slot), tmem_slot, abort_flag, 1);
+
+    if (threadIdx.x == 0) {
+        *abort_flag = 0;
+        ptx::mbar_init(bar(L::B_RES_FULL), 1);
+        for (int s = 0; s < KS; ++s) {
+            ptx::mbar_init(bar(L::B_K_FULL + s), 1);
+            ptx::mbar_init(bar(L::B_K_EMPTY + s), 1);
+        }
+        for (int s = 0; s < VS; ++s) {
+            ptx::mbar_init(bar(L::B_V_FULL + s), 1);
+            ptx::mbar_init(bar(L::B_V_EMPTY + s), 1);
+        }
+        ptx::mbar_init(bar(L::B_S_FULL + 0), 1);
+        ptx::mbar_init(bar(L::B_S_FULL + 1), 1);
+        ptx::mbar_init(bar(L::B_DP_FULL), 1);
+        ptx::mbar_init(bar(L::B_DS_FULL), 128);
+        ptx::mbar_init(bar(L::B_MMA_DONE), 1);
+        ptx::mbar_init(bar(L::B_DRAIN), 1);
+        ptx::fence_barrier_init();
+        ptx::fence_proxy_async_smem();
+    }
+    if (warp == BWD_MMA_WARP) {
+        ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
     const Ctl ctl{abort_flag, p.err, p.timeout_ns};
+    auto s_buf = [](int j) { return (j & 1) ? DQ_TMEM_S1 : DQ_TMEM_S0; };
 
     if (warp == BWD_LOAD_WARP) {
         if (lane == 0) {
             ptx::mbar_arrive_expect_tx(bar(L::B_RES_FULL), 2 * L::TILE);
-            tma_tile<D>(sbase + L::R0_OFF, &tm_q, q0, bh, bar(L::B_RES_FULL));
-            tma_tile<D>(sbase + L::R1_OFF, &tm_do, q0, bh, bar(L::B_RES_FULL));
-            int issued = 0;
+            tma_tile<D>(sbase + L::Q_OFF, &tm_q, q0, bh, bar(L::B_RES_FULL));
+            tma_tile<D>(sbase + L::DO_OFF, &tm_do, q0, bh, bar(L::B_RES_FULL));
+            int k_issued = 0, v_issued = 0;
             for (int j = 0; j < n; ++j) {
-                const int st = j % STAGES;
-                if (!wait_bar(bar(L::B_EMPTY + st), ((j / STAGES) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
-                ptx::mbar_arrive_expect_tx(bar(L::B_A_FULL + st), L::TILE);
-                tma_tile<D>(sbase + L::A_OFF + st * L::TILE, &tm_k, j * 128, bh, bar(L::B_A_FULL + st));
-                ptx::mbar_arrive_expect_tx(bar(L::B_B_FULL + st), L::TILE);
-                tma_tile<D>(sbase + L::B_OFF + st * L::TILE, &tm_v, j * 128, bh, bar(L::B_B_FULL + st));
-                issued = j + 1;
+                const int ks = j % KS, vs = j % VS;
+                if (!wait_bar(bar(L::B_K_EMPTY + ks), ((j / KS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
+                ptx::mbar_arrive_expect_tx(bar(L::B_K_FULL + ks), L::TILE);
+                tma_tile<D>(sbase + L::K_OFF + ks * L::TILE, &tm_k, j * 128, bh, bar(L::B_K_FULL + ks));
+                k_issued = j + 1;
+                if (!wait_bar(bar(L::B_V_EMPTY + vs), ((j / VS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
+                ptx::mbar_arrive_expect_tx(bar(L::B_V_FULL + vs), L::TILE);
+                tma_tile<D>(sbase + L::V_OFF + vs * L::TILE, &tm_v, j * 128, bh, bar(L::B_V_FULL + vs));
+                v_issued = j + 1;
             }
             if (*abort_flag) {
+                // Drain: the newest copy into each stage is its barrier's newest phase.
                 wait_bar(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_DRAIN, false);
-                for (int j = (issued > STAGES ? issued - STAGES : 0); j < issued; ++j) {
-                    wait_bar(bar(L::B_A_FULL + j % STAGES), (j / STAGES) & 1, ctl, SITE_BWD_DRAIN, false);
-                    wait_bar(bar(L::B_B_FULL + j % STAGES), (j / STAGES) & 1, ctl, SITE_BWD_DRAIN, false);
-                }
+                for (int j = (k_issued > KS ? k_issued - KS : 0); j < k_issued; ++j)
+                    wait_bar(bar(L::B_K_FULL + j % KS), (j / KS) & 1, ctl, SITE_BWD_DRAIN, false);
+                for (int j = (v_issued > VS ? v_issued - VS : 0); j < v_issued; ++j)
+                    wait_bar(bar(L::B_V_FULL + j % VS), (j / VS) & 1, ctl, SITE_BWD_DRAIN, false);
             }
         }
         __syncwarp();
@@ -470,34 +534,51 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const uint32_t leader = elect_leader();
         constexpr uint32_t IDESC_SQ = ptx::idesc_f16(BF16, 128, 128, false, false);
         constexpr uint32_t IDESC_OD = ptx::idesc_f16(BF16, 128, D, false, true);
-        const uint32_t d_s = tmem + BWD_TMEM_S, d_dp = tmem + BWD_TMEM_DP, d_dq = tmem + BWD_TMEM_A;
+        const uint32_t d_dp = tmem + DQ_TMEM_DP, d_dq = tmem + DQ_TMEM_DQ;
         auto commit = [&](int b) {
             if (leader) ptx::mma_commit(bar(b));
             __syncwarp();
         };
-        bool ok = wait_bar_warp(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_MMA);
-        for (int j = 0; ok && j < n; ++j) {
-            const int st = j % STAGES;
-            const uint32_t ph = (j / STAGES) & 1;
-            const uint32_t k_tile = sbase + L::A_OFF + st * L::TILE, v_tile = sbase + L::B_OFF + st * L::TILE;
-            if (!(ok = wait_bar_warp(bar(L::B_A_FULL + st), ph, ctl, SITE_BWD_MMA))) break;
+        auto k_tile = [&](int j) { return sbase + L::K_OFF + (j % KS) * L::TILE; };
+        auto v_tile = [&](int j) { return sbase + L::V_OFF + (j % VS) * L::TILE; };
+        // S_j = Q K_j^T into the buffer of block j.
+        auto issue_s = [&](int j) -> bool {
+            if (!wait_bar_warp(bar(L::B_K_FULL + j % KS), (j / KS) & 1, ctl, SITE_BWD_MMA)) return false;
             ptx::tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)  // S = Q K_j^T
-                if (leader) ptx::mma_ss(d_s, kmajor_desc(sbase + L::R0_OFF, kk), kmajor_desc(k_tile, kk), IDESC_SQ, kk > 0);
-            commit(L::B_S_FULL);
-            if (!(ok = wait_bar_warp(bar(L::B_B_FULL + st), ph, ctl, SITE_BWD_MMA))) break;
+            for (int kk = 0; kk < D / 16; ++kk)
+                if (leader)
+                    ptx::mma_ss(tmem + s_buf(j), kmajor_desc(sbase + L::Q_OFF, kk),
+                                kmajor_desc(k_tile(j), kk), IDESC_SQ, kk > 0);
+            commit(L::B_S_FULL + (j & 1));
+            return true;
+        };
+        // dP_j = dO V_j^T; V_j is then free.
+        auto issue_dp = [&](int j) -> bool {
+            if (!wait_bar_warp(bar(L::B_V_FULL + j % VS), (j / VS) & 1, ctl, SITE_BWD_MMA)) return false;
             ptx::tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk)  // dP = dO V_j^T
-                if (leader) ptx::mma_ss(d_dp, kmajor_desc(sbase + L::R1_OFF, kk), kmajor_desc(v_tile, kk), IDESC_SQ, kk > 0);
+            for (int kk = 0; kk < D / 16; ++kk)
+                if (leader)
+                    ptx::mma_ss(d_dp, kmajor_desc(sbase + L::DO_OFF, kk), kmajor_desc(v_tile(j), kk),
+                                IDESC_SQ, kk > 0);
             commit(L::B_DP_FULL);
+            commit(L::B_V_EMPTY + j % VS);
+            return true;
+        };
+        bool ok = wait_bar_warp(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_MMA);
+        ok = ok && issue_s(0) && issue_dp(0) && (n < 2 || issue_s(1));
+        for (int j = 0; ok && j < n; ++j) {
             if (!(ok = wait_bar_warp(bar(L::B_DS_FULL), j & 1, ctl, SITE_BWD_MMA))) break;
             ptx::tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)  // dQ += dS K_j (dS over the S columns)
-                if (leader) ptx::mma_ts(d_dq, d_s + kk * 8, mnmajor_desc(k_tile, kk), IDESC_OD, (j > 0 || kk > 0));
-            commit(L::B_EMPTY + st);
+            for (int kk = 0; kk < 8; ++kk)  // dQ += dS_j K_j (dS_j over its S buffer)
+                if (leader)
+                    ptx::mma_ts(d_dq, tmem + s_buf(j) + kk * 8, mnmajor_desc(k_tile(j), kk), IDESC_OD,
+                                (j > 0 || kk > 0));
+            commit(L::B_K_EMPTY + j % KS);
+            if (j + 1 < n && !(ok = issue_dp(j + 1))) break;
+            if (j + 2 < n && !(ok = issue_s(j + 2))) break;
         }
         if (ok) commit(L::B_MMA_DONE);
         if (*abort_flag) {
@@ -510,13 +591,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const int r = threadIdx.x;
         const int row = q0 + r;
         const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
-        const uint32_t s_cols = tmem + lanes + BWD_TMEM_S, dp_cols = tmem + lanes + BWD_TMEM_DP;
+        const uint32_t dp_cols = tmem + lanes + DQ_TMEM_DP;
         const float c = p.scale_log2;
         const size_t vo = static_cast<size_t>(bh) * p.nq_pad + row;  // row < nq_pad always
         const float lse2 = p.lse2[vo], dlt = p.delta[vo];
         bool ok = true;
         for (int j = 0; j < n; ++j) {
-            if (!(ok = wait_bar_warp(bar(L::B_S_FULL), j & 1, ctl, SITE_BWD_COMPUTE))) break;
+            const uint32_t s_cols = tmem + lanes + s_buf(j);
+            if (!(ok = wait_bar_warp(bar(L::B_S_FULL + (j & 1)), (j >> 1) & 1, ctl, SITE_BWD_COMPUTE))) break;
             ptx::tc_fence_after();
             uint32_t sr[4][32];
 #pragma unroll
@@ -540,7 +622,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 }
             if (!(ok = wait_bar_warp(bar(L::B_DP_FULL), j & 1, ctl, SITE_BWD_COMPUTE))) break;
             ptx::tc_fence_after();
-            // dS = P (dP - D), written over the S columns (all of S is already in registers).
+            // dS = P (dP - D), written over this block's S buffer (all of S is in registers).
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
                 uint32_t dr[32];
@@ -560,7 +642,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
         if (ok && n > 0 && wait_bar_warp(bar(L::B_MMA_DONE), 0, ctl, SITE_BWD_COMPUTE)) {
             ptx::tc_fence_after();
-            store_row<D, BF16>(tmem + lanes + BWD_TMEM_A, p.scale,
+            store_row<D, BF16>(tmem + lanes + DQ_TMEM_DQ, p.scale,
                                static_cast<uint8_t*>(p.dq) + (static_cast<size_t>(bh) * p.nq + row) * D * 2,
                                row < p.nq);
         }
