@@ -523,9 +523,23 @@ fa_status launch_bwd_instance(int dev, const CUtensorMap& mq, const CUtensorMap&
     timer_end(strm, ti);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
+    // dQ depends only on the preprocessing (complete before the dK/dV kernel started), not on
+    // dK/dV: a programmatic dependent launch lets its CTAs fill the SMs the dK/dV kernel's last
+    // wave leaves idle.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(nqb * static_cast<unsigned>(p.bh));
+    cfg.blockDim = dim3(fa::BWD_THREADS);
+    cfg.dynamicSmemBytes = smem_q;
+    cfg.stream = strm;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     ti = timer_begin(strm, FA_KERNEL_BWD_DQ);
-    k_q<<<nqb * static_cast<unsigned>(p.bh), fa::BWD_THREADS, smem_q, strm>>>(mq, mk, mv, mdo, p);
+    e = cudaLaunchKernelEx(&cfg, k_q, mq, mk, mv, mdo, p);
     timer_end(strm, ti);
+    if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
     if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "backward dQ launch");
     return FA_OK;
 }
@@ -726,8 +740,8 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
     auto strm = static_cast<cudaStream_t>(stream);
     const bool bf16 = dtype == FA_BF16;
     {
-        const int64_t warps = bh * nq_pad;
-        const unsigned blocks = static_cast<unsigned>((warps * 32 + 255) / 256);
+        const int64_t threads = bh * nq_pad * (D / 8);
+        const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
         const int ti = timer_begin(strm, FA_KERNEL_BWD_PREP);
         if (D == 128) {
             if (bf16) fa::fa_bwd_prep_kernel<128, true><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));

@@ -48,7 +48,7 @@ enum BwdSite : int {
 };
 
 // ---------------------------------------------------------------------------------------------
-// D_i and LSE2_i: one warp per (padded) query row
+// D_i and LSE2_i: D / 8 threads per (padded) query row, 16-byte loads of O and dO
 // ---------------------------------------------------------------------------------------------
 template <int D, bool BF16>
 __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const void* __restrict__ o,
@@ -57,34 +57,35 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const void* __restrict
                                                           float* __restrict__ lse2,
                                                           float* __restrict__ delta, int bh,
                                                           int nq, int nq_pad) {
-    constexpr int E = D / 32;
-    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5;
-    const int lane = threadIdx.x & 31;
-    if (w >= static_cast<int64_t>(bh) * nq_pad) return;
-    const int64_t h = w / nq_pad, r = w % nq_pad;
-    if (r >= nq) {
-        if (lane == 0) {
+    constexpr int TPR = D / 8;  // threads per row, 8 elements each
+    const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / TPR;
+    const int sub = threadIdx.x % TPR;
+    const bool live = w < static_cast<int64_t>(bh) * nq_pad;
+    const int64_t h = live ? w / nq_pad : 0, r = live ? w % nq_pad : 0;
+    float acc = 0.f;
+    if (live && r < nq) {
+        const int64_t src = (h * nq + r) * D + sub * 8;
+        const uint4 a = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(o) + src);
+        const uint4 b = *reinterpret_cast<const uint4*>(static_cast<const uint16_t*>(dout) + src);
+        const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float2 x = unpack2<BF16>(av[e]), y = unpack2<BF16>(bv[e]);
+            acc = fmaf(x.x, y.x, acc);
+            acc = fmaf(x.y, y.y, acc);
+        }
+    }
+    // Sum over the TPR threads of the row (aligned groups within the warp).
+#pragma unroll
+    for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
+    if (live && sub == 0) {
+        if (r < nq) {
+            delta[w] = acc;
+            lse2[w] = lse[h * nq + r] * 1.4426950408889634f;
+        } else {
             lse2[w] = INFINITY;
             delta[w] = 0.f;
         }
-        return;
-    }
-    const int64_t src = (h * nq + r) * D + lane * E;
-    const uint16_t* op = static_cast<const uint16_t*>(o) + src;
-    const uint16_t* dp = static_cast<const uint16_t*>(dout) + src;
-    float acc = 0.f;
-#pragma unroll
-    for (int e = 0; e < E; e += 2) {
-        const float2 a = unpack2<BF16>(*reinterpret_cast<const uint32_t*>(op + e));
-        const float2 b = unpack2<BF16>(*reinterpret_cast<const uint32_t*>(dp + e));
-        acc = fmaf(a.x, b.x, acc);
-        acc = fmaf(a.y, b.y, acc);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (lane == 0) {
-        delta[w] = acc;
-        lse2[w] = lse[h * nq + r] * 1.4426950408889634f;
     }
 }
 
@@ -242,6 +243,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int n = nqb > i_begin ? nqb - i_begin : 0;
     const uint32_t tmem = bwd_setup<D>(smem, sbase, ptx::smem_u32(tmem_slot), tmem_slot, abort_flag, 1);
     const Ctl ctl{abort_flag, p.err, p.timeout_ns};
+    // The dQ kernel is launched as a programmatic dependent of this one and reads nothing this
+    // kernel writes, so it may take SMs as soon as every CTA here has started.
+    if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == BWD_LOAD_WARP) {
         if (lane == 0 && n > 0) {
