@@ -111,7 +111,8 @@ struct BwdSmem {
     static constexpr int B_EMPTY = B_B_FULL + STAGES;   // [STAGES]
     static constexpr int B_S_FULL = B_EMPTY + STAGES;
     static constexpr int B_DP_FULL = B_S_FULL + 1;
-    static constexpr int B_P_FULL = B_DP_FULL + 1;
+    static constexpr int B_P_HALF = B_DP_FULL + 1;      // P^T of queries 0-63 stored
+    static constexpr int B_P_FULL = B_P_HALF + 1;
     static constexpr int B_DS_FULL = B_P_FULL + 1;
     static constexpr int B_MMA_DONE = B_DS_FULL + 1;
     static constexpr int B_DRAIN = B_MMA_DONE + 1;
@@ -193,6 +194,7 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t sbase, uin
         }
         ptx::mbar_init(bar(L::B_S_FULL), 1);
         ptx::mbar_init(bar(L::B_DP_FULL), 1);
+        ptx::mbar_init(bar(L::B_P_HALF), 128);
         ptx::mbar_init(bar(L::B_P_FULL), 128);
         ptx::mbar_init(bar(L::B_DS_FULL), 128);
         ptx::mbar_init(bar(L::B_MMA_DONE), 1);
@@ -304,12 +306,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             commit(L::B_DP_FULL);
         }
         for (int it = 0; ok && it < n; ++it) {
-            // dV += P^T dO_i (P^T over the S^T columns)
-            if (!(ok = wait_bar_warp(bar(L::B_P_FULL), it & 1, ctl, SITE_BWD_MMA))) break;
-            ptx::tc_fence_after();
+            // dV += P^T dO_i (P^T over the S^T columns), queries 0-63 as soon as they are stored
+            for (int h = 0; h < 2 && ok; ++h) {
+                if (!(ok = wait_bar_warp(bar(h == 0 ? L::B_P_HALF : L::B_P_FULL), it & 1, ctl, SITE_BWD_MMA)))
+                    break;
+                ptx::tc_fence_after();
 #pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-                if (leader) ptx::mma_ts(d_dv, d_s + kk * 8, mnmajor_desc(stage_do(it), kk), IDESC_OD, (it > 0 || kk > 0));
+                for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
+                    if (leader)
+                        ptx::mma_ts(d_dv, d_s + kk * 8, mnmajor_desc(stage_do(it), kk), IDESC_OD,
+                                    (it > 0 || kk > 0));
+            }
+            if (!ok) break;
             if (it + 1 < n) {  // S^T of the next block may overwrite P^T now (MMAs run in order)
                 if (!(ok = wait_bar_warp(bar(L::B_A_FULL + (it + 1) % STAGES), ((it + 1) / STAGES) & 1, ctl, SITE_BWD_MMA))) break;
                 ptx::tc_fence_after();
@@ -357,25 +365,26 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             // On the diagonal block a query before this key (q < k) does not see it.
             const bool diag = CAUSAL && (i == kb);
             float pf[128];
+            // P^T in two halves of 64 queries, each released to the dV product once stored.
 #pragma unroll
-            for (int q = 0; q < 4; ++q)
+            for (int h = 0; h < 2; ++h) {
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    const int col = q * 32 + e;
-                    float pv = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -vec[col]));
-                    if (diag && i * 128 + col < kr) pv = 0.f;
-                    pf[col] = pv;
-                }
-            uint32_t pk[2][32];
+                for (int qq = 0; qq < 2; ++qq)
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
+                    for (int e = 0; e < 32; ++e) {
+                        const int q = 2 * h + qq, col = q * 32 + e;
+                        float pv = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -vec[col]));
+                        if (diag && i * 128 + col < kr) pv = 0.f;
+                        pf[col] = pv;
+                    }
+                uint32_t pk[32];
 #pragma unroll
-                for (int w = 0; w < 32; ++w) pk[h][w] = pack2<BF16>(pf[h * 64 + 2 * w], pf[h * 64 + 2 * w + 1]);
-            ptx::tmem_st32(s_cols, pk[0]);
-            ptx::tmem_st32(s_cols + 32, pk[1]);
-            ptx::tmem_wait_st();
-            ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(L::B_P_FULL));
+                for (int w = 0; w < 32; ++w) pk[w] = pack2<BF16>(pf[h * 64 + 2 * w], pf[h * 64 + 2 * w + 1]);
+                ptx::tmem_st32(s_cols + 32 * h, pk);
+                ptx::tmem_wait_st();
+                ptx::tc_fence_before();
+                ptx::mbar_arrive(bar(h == 0 ? L::B_P_HALF : L::B_P_FULL));
+            }
             // dS^T[r][col] = P^T (dP^T - D[col]), written over the dP^T columns chunk by chunk
             // (chunk q of fp32 columns 32q.. becomes 16-bit pairs at 16q.., already read).
             if (!(ok = wait_bar_warp(bar(L::B_DP_FULL), it & 1, ctl, SITE_BWD_COMPUTE))) break;
