@@ -182,11 +182,15 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
 /*
  * fa_fwd_host -- the same operation on HOST buffers, synchronous.
  *
- * Q, K, V, O are host pointers with the layout above (pinned memory gives full copy speed).
- * The call copies Q, K, V to device memory owned by libfa, runs fa_fwd on `stream`, copies O
- * back and waits for the stream. The device staging buffers grow to the largest request seen
- * and are kept until process exit (or fa_release_host_buffers). Not thread-safe: concurrent
- * calls from several host threads must be serialised by the caller.
+ * Q, K, V, O are host pointers with the layout above (pinned memory gives full copy speed and
+ * lets copies overlap the computation). The call copies Q, K, V to device memory owned by
+ * libfa, computes, copies O back and returns when O is complete. The (batch, head) slices are
+ * processed in up to 8 chunks on three libfa-owned streams, ordered after the work already on
+ * `stream`: while one chunk computes, the next is copied in and the previous copied out. Each
+ * chunk is one attention launch (no last-wave split). The device staging buffers grow to the
+ * largest request seen and are kept until process exit (or fa_release_host_buffers); the
+ * streams live until process exit. Not thread-safe: concurrent calls from several host
+ * threads must be serialised by the caller. On an error the contents of O are undefined.
  */
 fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int64_t B,
                       int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,

@@ -280,6 +280,33 @@ struct Staging {
 };
 Staging g_staging[MAX_DEVICES];
 
+// Streams and events of fa_fwd_host's copy/compute pipeline, per device, made on first use.
+constexpr int HOST_PIPE_STREAMS = 3;
+struct HostPipe {
+    bool ready = false;
+    cudaStream_t s[HOST_PIPE_STREAMS] = {};
+    cudaEvent_t start = nullptr;
+    cudaEvent_t done[HOST_PIPE_STREAMS] = {};
+};
+HostPipe g_host_pipe[MAX_DEVICES];
+
+fa_status host_pipe(int dev, HostPipe** out) {
+    HostPipe& hp = g_host_pipe[dev];
+    if (!hp.ready) {
+        cudaError_t e;
+        for (int i = 0; i < HOST_PIPE_STREAMS; ++i) {
+            if ((e = cudaStreamCreateWithFlags(&hp.s[i], cudaStreamNonBlocking)) != cudaSuccess ||
+                (e = cudaEventCreateWithFlags(&hp.done[i], cudaEventDisableTiming)) != cudaSuccess)
+                return cuda_fail(e, "host pipeline streams");
+        }
+        if ((e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming)) != cudaSuccess)
+            return cuda_fail(e, "host pipeline event");
+        hp.ready = true;
+    }
+    *out = &hp;
+    return FA_OK;
+}
+
 // ---------------------------------------------------------------------------------------------
 // Allocation-free variant (fa_fwd_noalloc): the kernel's error record lives in this file-scope
 // device array instead of device memory from cudaMalloc. Host code must not pass the symbol
@@ -815,19 +842,53 @@ fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int6
         st.bytes = need;
     }
     auto* base = static_cast<uint8_t*>(st.buf);
-    void* dq = base;
-    void* dk = base + round_up(q_bytes);
-    void* dv = base + round_up(q_bytes) + round_up(kv_bytes);
-    void* dout = base + round_up(q_bytes) + 2 * round_up(kv_bytes);
+    auto* dq = base;
+    auto* dk = base + round_up(q_bytes);
+    auto* dv = base + round_up(q_bytes) + round_up(kv_bytes);
+    auto* dout = base + round_up(q_bytes) + 2 * round_up(kv_bytes);
     auto strm = static_cast<cudaStream_t>(stream);
-    if ((e = cudaMemcpyAsync(dq, Q, q_bytes, cudaMemcpyHostToDevice, strm)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(dk, K, kv_bytes, cudaMemcpyHostToDevice, strm)) != cudaSuccess ||
-        (e = cudaMemcpyAsync(dv, V, kv_bytes, cudaMemcpyHostToDevice, strm)) != cudaSuccess)
-        return cuda_fail(e, "cudaMemcpyAsync(host to device)");
-    s = forward(dq, dk, dv, dout, nullptr, B, H, Nq, Nk, D, scale, causal, int(dtype), strm);
-    if (s != FA_OK) return s;
-    if ((e = cudaMemcpyAsync(O, dout, q_bytes, cudaMemcpyDeviceToHost, strm)) != cudaSuccess)
-        return cuda_fail(e, "cudaMemcpyAsync(device to host)");
+    HostPipe* hp = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        if ((s = host_pipe(dev, &hp)) != FA_OK) return s;
+    }
+    // The (batch, head) slices are independent: in chunks of slices, the copy of chunk c + 1 in,
+    // the attention on chunk c and the copy of chunk c - 1 out run at the same time (the copy
+    // engines of the two directions and the SMs work in parallel). Chunks go round-robin over
+    // three streams; each stream copies in, computes and copies out its chunks in order.
+    const int64_t bh = B * H;
+    const int64_t chunks = bh < 8 ? bh : 8;
+    const int64_t per = (bh + chunks - 1) / chunks;
+    const size_t q_slice = size_t(Nq) * size_t(D) * 2, kv_slice = size_t(Nk) * size_t(D) * 2;
+    auto* hq = static_cast<const uint8_t*>(Q);
+    auto* hk = static_cast<const uint8_t*>(K);
+    auto* hv = static_cast<const uint8_t*>(V);
+    auto* ho = static_cast<uint8_t*>(O);
+    if ((e = cudaEventRecord(hp->start, strm)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    for (int i = 0; i < HOST_PIPE_STREAMS; ++i)
+        if ((e = cudaStreamWaitEvent(hp->s[i], hp->start, 0)) != cudaSuccess)
+            return cuda_fail(e, "cudaStreamWaitEvent");
+    for (int64_t c0 = 0, c = 0; c0 < bh; c0 += per, ++c) {
+        const int64_t n = (bh - c0 < per) ? bh - c0 : per;
+        cudaStream_t x = hp->s[c % HOST_PIPE_STREAMS];
+        const size_t qo = size_t(c0) * q_slice, ko = size_t(c0) * kv_slice;
+        if ((e = cudaMemcpyAsync(dq + qo, hq + qo, size_t(n) * q_slice, cudaMemcpyHostToDevice, x)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(dk + ko, hk + ko, size_t(n) * kv_slice, cudaMemcpyHostToDevice, x)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(dv + ko, hv + ko, size_t(n) * kv_slice, cudaMemcpyHostToDevice, x)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyAsync(host to device)");
+        // One launch per chunk, without the last-wave split (its workspace is shared, and the
+        // chunks run concurrently).
+        s = launch(dq + qo, dk + ko, dv + ko, dout + qo, nullptr, 1, n, Nq, Nk, D, scale, causal,
+                   int(dtype), x);
+        if (s != FA_OK) return s;
+        if ((e = cudaMemcpyAsync(ho + qo, dout + qo, size_t(n) * q_slice, cudaMemcpyDeviceToHost, x)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyAsync(device to host)");
+    }
+    for (int i = 0; i < HOST_PIPE_STREAMS; ++i) {
+        if ((e = cudaEventRecord(hp->done[i], hp->s[i])) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(strm, hp->done[i], 0)) != cudaSuccess)
+            return cuda_fail(e, "host pipeline join");
+    }
     if ((e = cudaStreamSynchronize(strm)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     return FA_OK;
 }
