@@ -434,7 +434,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 // ---------------------------------------------------------------------------------------------
 // S_j = Q K_j^T alternates between two TMEM buffers (columns 0-127 and 384-511), so S_{j+1} and
 // S_{j+2} are computed while the compute warps turn S_j and dP_j into dS_j. MMA order:
-//   S_0, dP_0, S_1,  then per j: dQ += dS_j K_j, dP_{j+1}, S_{j+2} (over dS_j's buffer).
+//   S_0, dP_0, S_1,  then per j: dP_{j+1}, dQ += dS_j K_j, S_{j+2} (over dS_j's buffer).
 // K_j serves S_j and the dQ product of block j, so the K ring holds three tiles.
 template <int D>
 struct DqSmem {
@@ -583,6 +583,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ok = ok && issue_s(0) && issue_dp(0) && (n < 2 || issue_s(1));
         for (int j = 0; ok && j < n; ++j) {
             if (!(ok = wait_bar_warp(bar(L::B_DS_FULL), j & 1, ctl, SITE_BWD_MMA))) break;
+            // dP_{j+1} first: the compute warps are done with dP_j, and dS_{j+1} then overlaps
+            // the dQ product of block j instead of waiting behind it.
+            if (j + 1 < n && !(ok = issue_dp(j + 1))) break;
             ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // dQ += dS_j K_j (dS_j over its S buffer)
@@ -590,7 +593,6 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                     ptx::mma_ts(d_dq, tmem + s_buf(j) + kk * 8, mnmajor_desc(k_tile(j), kk), IDESC_OD,
                                 (j > 0 || kk > 0));
             commit(L::B_K_EMPTY + j % KS);
-            if (j + 1 < n && !(ok = issue_dp(j + 1))) break;
             if (j + 2 < n && !(ok = issue_s(j + 2))) break;
         }
         if (ok) commit(L::B_MMA_DONE);
