@@ -236,3 +236,48 @@ def test_rescale_threshold_setter_validates(fa):
         with pytest.raises(fa.FaError):
             fa.set_rescale_threshold(bad)
     assert fa.get_rescale_threshold() == old
+
+
+def test_host_buffer_pipeline_uneven_chunks(fa):
+    """The host entry copies and computes in chunks of slices on several streams: 37 slices make
+    chunks of 5 and a last one of 2. The result equals the device entry's bit for bit."""
+    w = inputs.Workload("host_chunks", 1, 37, 300, 500, 64, "f16", True, seed=13)
+    bits = inputs.draw(w)
+    dev = inputs.from_torch(run_gpu(fa, bits, w))
+    qh, kh, vh = (inputs.to_torch(bits[n], w.dtype).pin_memory() for n in "qkv")
+    oh = torch.full_like(qh, 5.0).pin_memory()
+    fa.forward_host(qh, kh, vh, oh, causal=True, scale=w.scale)
+    assert np.array_equal(inputs.from_torch(oh), dev)
+
+
+def test_long_context_chunk_full_size(fa, orc):
+    """128 queries against 65536 keys (split over keys, then merged): sampled rows of two heads
+    against the oracle, from both the split-KV entry and the single launch."""
+    w = inputs.WORKLOADS["long_context_chunk"]
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    outs = {"split": fa.forward_splitkv(q, k, v, scale=w.scale),
+            "single": fa.forward(q, k, v, scale=w.scale)}
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == (0, 0)
+    rows = np.array([0, 1, 63, 64, 127])
+    for h in (0, w.H - 1):
+        ref = orc.attention_rows(inputs.bits_to_f64(bits["q"][0, h, rows], w.dtype), rows,
+                                 inputs.bits_to_f64(bits["k"][0, h], w.dtype),
+                                 inputs.bits_to_f64(bits["v"][0, h], w.dtype), w.scale, False)
+        for name, o in outs.items():
+            got = inputs.from_torch(o)[0, h, rows]
+            parity.assert_parity(parity.compare(got, ref, w.dtype), True, f"{name} head {h}")
+
+
+def test_many_slices_with_split_last_wave(fa, orc):
+    """2048 slices of 128 queries against 1024 keys: 2048 units leave a last wave of 72, whose
+    keys are split in two (slices 1976 and up). Whole-unit slices and split ones both match
+    the oracle."""
+    w = inputs.Workload("many_slices", 64, 32, 128, 1024, 64, "bf16", False, seed=14)
+    bits = inputs.draw(w)
+    o = inputs.from_torch(run_gpu(fa, bits, w))
+    for b, h in ((0, 0), (31, 7), (62, 31), (63, 30), (63, 31)):
+        ref = orc.attention(*(inputs.bits_to_f64(bits[n][b, h], w.dtype) for n in "qkv"),
+                            w.scale, False)
+        parity.assert_parity(parity.compare(o[b, h], ref, w.dtype), True, f"slice ({b},{h})")
