@@ -73,6 +73,8 @@ WORKLOADS = {
         # a 128-token chunk against a 64K-token context: one query block per head, so the keys
         # are split across CTAs (flash-decoding)
         Workload("long_context_chunk", 1, 8, 128, 65536, 128, "bf16", False, seed=7),
+        # the headline shape at head dim 64 (the ragged and single-head configs' D)
+        Workload("headline_d64", 1, 32, 4096, 4096, 64, "f16", False, seed=8),
     ]
 }
 
