@@ -602,8 +602,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4;
-                    if (leader)
-                        ptx::mma_ss(tmem + tmem_s(t), a0 + off, b0 + off, IDESC_S, kk > 0 ? 1u : 0u);
+                    ptx::mma_ss_if(leader, tmem + tmem_s(t), a0 + off, b0 + off, IDESC_S, kk > 0 ? 1u : 0u);
                 }
             };
             // O_t += P_t V_j over keys [64 half, 64 half + 64): P_t is the A operand from TMEM
@@ -613,14 +612,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const uint64_t b0 = ptx::sdesc_sw128(sv + (j % STAGES) * L::KV_BYTES, BN * 128, 1024);
 #pragma unroll
                 for (int kk = half * (BN / 32); kk < (half + 1) * (BN / 32); ++kk)
-                    if (leader)
-                        ptx::mma_ts(tmem + tmem_o(t), tmem + tmem_s(t) + kk * 8,
-                                    b0 + ((kk * 16 * 128) >> 4), IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
+                    ptx::mma_ts_if(leader, tmem + tmem_o(t), tmem + tmem_s(t) + kk * 8,
+                                   b0 + ((kk * 16 * 128) >> 4), IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
             };
-            auto commit = [&](int b) {
-                if (leader) ptx::mma_commit(bar(b));
-                __syncwarp();
-            };
+            auto commit = [&](int b) { ptx::mma_commit_if(leader, bar(b)); };
             // Per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1). S_t(j+1) overwrites the TMEM
             // columns P_t(j) occupies, so it follows PV_t(j) (MMAs of one thread run in order).
             const int n0 = n_tiles[0], n1 = n_tiles[Q_TILES - 1];
