@@ -285,17 +285,14 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         auto issue_s = [&](int it) {  // S^T = K Q_i^T
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                if (leader) ptx::mma_ss(d_s, kmajor_desc(sbase + L::R0_OFF, kk), kmajor_desc(stage_q(it), kk), IDESC_SQ, kk > 0);
+                ptx::mma_ss_if(leader, d_s, kmajor_desc(sbase + L::R0_OFF, kk), kmajor_desc(stage_q(it), kk), IDESC_SQ, kk > 0);
         };
         auto issue_dp = [&](int it) {  // dP^T = V dO_i^T
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                if (leader) ptx::mma_ss(d_dp, kmajor_desc(sbase + L::R1_OFF, kk), kmajor_desc(stage_do(it), kk), IDESC_SQ, kk > 0);
+                ptx::mma_ss_if(leader, d_dp, kmajor_desc(sbase + L::R1_OFF, kk), kmajor_desc(stage_do(it), kk), IDESC_SQ, kk > 0);
         };
-        auto commit = [&](int b) {
-            if (leader) ptx::mma_commit(bar(b));
-            __syncwarp();
-        };
+        auto commit = [&](int b) { ptx::mma_commit_if(leader, bar(b)); };
         bool ok = n > 0 && wait_bar_warp(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_MMA) &&
                   wait_bar_warp(bar(L::B_A_FULL + 0), 0, ctl, SITE_BWD_MMA);
         if (ok) {
@@ -313,8 +310,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 ptx::tc_fence_after();
 #pragma unroll
                 for (int kk = 4 * h; kk < 4 * h + 4; ++kk)
-                    if (leader)
-                        ptx::mma_ts(d_dv, d_s + kk * 8, mnmajor_desc(stage_do(it), kk), IDESC_OD,
+                    ptx::mma_ts_if(leader, d_dv, d_s + kk * 8, mnmajor_desc(stage_do(it), kk), IDESC_OD,
                                     (it > 0 || kk > 0));
             }
             if (!ok) break;
@@ -329,7 +325,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
-                if (leader) ptx::mma_ts(d_dk, d_dp + kk * 8, mnmajor_desc(stage_q(it), kk), IDESC_OD, (it > 0 || kk > 0));
+                ptx::mma_ts_if(leader, d_dk, d_dp + kk * 8, mnmajor_desc(stage_q(it), kk), IDESC_OD, (it > 0 || kk > 0));
             commit(L::B_EMPTY + it % STAGES);
             if (it + 1 < n) {
                 issue_dp(it + 1);
@@ -548,10 +544,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         constexpr uint32_t IDESC_SQ = ptx::idesc_f16(BF16, 128, 128, false, false);
         constexpr uint32_t IDESC_OD = ptx::idesc_f16(BF16, 128, D, false, true);
         const uint32_t d_dp = tmem + DQ_TMEM_DP, d_dq = tmem + DQ_TMEM_DQ;
-        auto commit = [&](int b) {
-            if (leader) ptx::mma_commit(bar(b));
-            __syncwarp();
-        };
+        auto commit = [&](int b) { ptx::mma_commit_if(leader, bar(b)); };
         auto k_tile = [&](int j) { return sbase + L::K_OFF + (j % KS) * L::TILE; };
         auto v_tile = [&](int j) { return sbase + L::V_OFF + (j % VS) * L::TILE; };
         // S_j = Q K_j^T into the buffer of block j.
@@ -560,8 +553,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                if (leader)
-                    ptx::mma_ss(tmem + s_buf(j), kmajor_desc(sbase + L::Q_OFF, kk),
+                ptx::mma_ss_if(leader, tmem + s_buf(j), kmajor_desc(sbase + L::Q_OFF, kk),
                                 kmajor_desc(k_tile(j), kk), IDESC_SQ, kk > 0);
             commit(L::B_S_FULL + (j & 1));
             return true;
@@ -572,8 +564,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
-                if (leader)
-                    ptx::mma_ss(d_dp, kmajor_desc(sbase + L::DO_OFF, kk), kmajor_desc(v_tile(j), kk),
+                ptx::mma_ss_if(leader, d_dp, kmajor_desc(sbase + L::DO_OFF, kk), kmajor_desc(v_tile(j), kk),
                                 IDESC_SQ, kk > 0);
             commit(L::B_DP_FULL);
             commit(L::B_V_EMPTY + j % VS);
@@ -589,8 +580,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::tc_fence_after();
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)  // dQ += dS_j K_j (dS_j over its S buffer)
-                if (leader)
-                    ptx::mma_ts(d_dq, tmem + s_buf(j) + kk * 8, mnmajor_desc(k_tile(j), kk), IDESC_OD,
+                ptx::mma_ts_if(leader, d_dq, tmem + s_buf(j) + kk * 8, mnmajor_desc(k_tile(j), kk), IDESC_OD,
                                 (j > 0 || kk > 0));
             commit(L::B_K_EMPTY + j % KS);
             if (j + 2 < n && !(ok = issue_s(j + 2))) break;
