@@ -310,7 +310,8 @@ def main():
                     help="fwd: the forward pass (the headline metric); bwd: fa_bwd after one "
                          "forward; rope: the rotary-embedding pass over Q and K")
     ap.add_argument("--splits", type=int, default=0,
-                    help="key splits for workloads with few query blocks (0: automatic)")
+                    help="N > 1: time the split-KV entry with N key ranges (non-causal); "
+                         "0: fa_fwd, which splits few-unit shapes over keys by itself")
     ap.add_argument("--ref-seconds", type=float, default=12.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile", action="store_true",
@@ -355,9 +356,9 @@ def main():
         sets.append((q, k, v, torch.empty_like(q)))
     stream = torch.cuda.current_stream(dev)
 
-    # Few query blocks per slice (a short chunk against a long context): split the keys across
-    # CTAs and merge (two launches per step).
-    use_split = (not w.causal) and w.B * w.H * -(-w.Nq // 256) < 152 and args.splits != 1
+    # fa_fwd balances work by itself (few units: every unit split over keys, then merged). An
+    # explicit --splits N > 1 times the split-KV entry with N key ranges instead.
+    use_split = (not w.causal) and args.splits > 1
     workspace = None
     if use_split:
         workspace = torch.empty(max(1, fa.splitkv_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.D,
@@ -468,7 +469,7 @@ def main():
                    "l2": f"{n_sets} rotating input sets of {set_bytes / 2**20:.0f} MiB "
                          f"(> L2 between consecutive steps)",
                    "pct_of_measured_peak": 100 * achieved / peak,
-                   "key_splits": "auto" if use_split and args.splits == 0 else (args.splits if use_split else 1)},
+                   "key_splits": args.splits if use_split else "auto"},
         "roofline": roofline,
         "cpu_baseline": cpu,
         "e2e": {"value": job_throughput(w.flops, world, e2e_s), "unit": "TFLOP/s",

@@ -75,13 +75,20 @@ typedef enum fa_status {
  * The first call on a device allocates one 16-byte device word for kernel error reports
  * (kept until process exit); make that first call outside any stream capture.
  *
- * Last-wave balancing (non-causal): when the 256-row work units leave a last wave that fills at
- * most half of the 152 SMs, those units are split over keys into 2-4 ranges and merged as in
- * fa_fwd_splitkv (two launches). The partial states live in a device workspace owned by libfa:
+ * Work balancing (non-causal), by splitting 256-row work units over keys and merging them as in
+ * fa_fwd_splitkv (two launches):
+ *   - at most 76 units (half of the 152 SMs): each unit is split into floor(152 / units) key
+ *     ranges of at least 2 key tiles (256 keys), so that one wave covers nearly all SMs;
+ *   - more than 152 units whose last wave fills at most half of the SMs: the units of that
+ *     wave are split into 2-4 ranges.
+ * Shapes with fewer than 4 key tiles (Nk <= 384), and causal launches, always run as one
+ * launch.
+ * The partial states live in a device workspace owned by libfa:
  * allocated the first time a shape needs it, grown when a later shape needs more, kept until
  * process exit. Calls that might grow it must not run under stream capture; all calls on one
  * device share it, so fa_fwd calls on different streams must be ordered. fa_set_tail_split(0)
- * turns the balancing off (one launch, no workspace).
+ * turns the balancing off (one launch, no workspace). Split units' rows differ from the single
+ * launch's only by rounding.
  */
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H,
                  int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, fa_dtype dtype,
@@ -187,7 +194,7 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
  * libfa, computes, copies O back and returns when O is complete. The (batch, head) slices are
  * processed in up to 8 chunks on three libfa-owned streams, ordered after the work already on
  * `stream`: while one chunk computes, the next is copied in and the previous copied out. Each
- * chunk is one attention launch (no last-wave split). The device staging buffers grow to the
+ * chunk is one attention launch (no key split). The device staging buffers grow to the
  * largest request seen and are kept until process exit (or fa_release_host_buffers); the
  * streams live until process exit. Not thread-safe: concurrent calls from several host
  * threads must be serialised by the caller. On an error the contents of O are undefined.
@@ -261,7 +268,8 @@ fa_status fa_wait_selftest(unsigned long long timeout_ns, void* stream);
 fa_status fa_set_rescale_threshold(float log2_threshold);
 float fa_get_rescale_threshold(void);
 
-/* Turn fa_fwd's last-wave balancing on (1, the default) or off (0). Process-wide. */
+/* Turn fa_fwd's work balancing (key splits, see fa_fwd) on (1, the default) or off (0).
+ * Process-wide. */
 fa_status fa_set_tail_split(int enable);
 
 /*

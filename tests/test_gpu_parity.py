@@ -251,13 +251,19 @@ def test_host_buffer_pipeline_uneven_chunks(fa):
 
 
 def test_long_context_chunk_full_size(fa, orc):
-    """128 queries against 65536 keys (split over keys, then merged): sampled rows of two heads
-    against the oracle, from both the split-KV entry and the single launch."""
+    """128 queries against 65536 keys: sampled rows of two heads against the oracle, from the
+    split-KV entry, from the default entry (which splits the 8 units over keys by itself) and
+    from one unsplit launch."""
     w = inputs.WORKLOADS["long_context_chunk"]
     bits = inputs.draw(w)
     q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
     outs = {"split": fa.forward_splitkv(q, k, v, scale=w.scale),
-            "single": fa.forward(q, k, v, scale=w.scale)}
+            "balanced": fa.forward(q, k, v, scale=w.scale)}
+    try:
+        fa.set_tail_split(False)
+        outs["single"] = fa.forward(q, k, v, scale=w.scale)
+    finally:
+        fa.set_tail_split(True)
     torch.cuda.synchronize()
     assert fa.last_device_error() == (0, 0)
     rows = np.array([0, 1, 63, 64, 127])

@@ -64,11 +64,16 @@ def test_long_context_chunk_full_size(fa):
 
 
 def test_one_split_is_fa_fwd(fa):
+    """One key range is fa_fwd's single launch (work balancing off), bit for bit."""
     w = inputs.Workload("one_split", 1, 2, 200, 500, 128, "bf16", False, seed=56)
     bits = inputs.draw(w)
     q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
     a = fa.forward_splitkv(q, k, v, num_splits=1, scale=w.scale)
-    b = fa.forward(q, k, v, scale=w.scale)
+    try:
+        fa.set_tail_split(False)
+        b = fa.forward(q, k, v, scale=w.scale)
+    finally:
+        fa.set_tail_split(True)
     torch.cuda.synchronize()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
@@ -113,6 +118,46 @@ def test_last_wave_split_matches_oracle_and_unsplit(fa):
     diff = np.abs(inputs.bits_to_f64(got, "bf16") - inputs.bits_to_f64(inputs.from_torch(o_plain), "bf16"))
     assert diff[0, :38].max() == 0.0  # whole units: identical bits
     assert diff.max() <= 2e-2
+
+
+@pytest.mark.parametrize("w,splits", [
+    # 4 units, 24 key tiles: each unit split into min(152 // 4, 24 // 2) = 12 ranges.
+    (inputs.Workload("few_units", 1, 2, 300, 3000, 128, "bf16", False, seed=60), 12),
+    # 2 units, 3 key tiles: ranges would be shorter than 2 tiles, so one launch.
+    (inputs.Workload("few_keys", 1, 2, 200, 380, 64, "f16", False, seed=61), 1),
+], ids=lambda x: getattr(x, "name", str(x)))
+def test_few_units_split_over_keys(fa, w, splits):
+    """When the units cannot fill half the SMs, the default entry splits every unit over keys
+    (one attention launch and one merge launch) unless the key ranges would be too short. Either
+    way the result matches the oracle, and the unsplit launch up to rounding."""
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    lse = torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device="cuda")
+    fa.forward_lse(q, k, v, scale=w.scale, lse=lse)
+    torch.cuda.synchronize()
+    fa.timer_start()
+    o, _ = fa.forward_lse(q, k, v, scale=w.scale, lse=lse)
+    kernels = fa.timer_stop()
+    assert kernels["fwd"][1] == 1
+    assert kernels.get("merge", (0.0, 0))[1] == (1 if splits > 1 else 0)
+    try:
+        fa.set_tail_split(False)
+        o_plain = fa.forward(q, k, v, scale=w.scale)
+    finally:
+        fa.set_tail_split(True)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == (0, 0)
+    got = inputs.from_torch(o)
+    for h in range(w.H):
+        ref, ref_lse = oracle.attention(*(inputs.bits_to_f64(bits[n][0, h], w.dtype) for n in "qkv"),
+                                        w.scale, False, with_lse=True)
+        parity.assert_parity(parity.compare(got[0, h], ref, w.dtype), True, f"head {h}")
+        assert np.max(np.abs(lse[0, h].cpu().numpy() - ref_lse)) <= LSE_TOL
+    diff = np.abs(inputs.bits_to_f64(got, w.dtype) - inputs.bits_to_f64(inputs.from_torch(o_plain), w.dtype))
+    if splits == 1:
+        assert diff.max() == 0.0
+    else:
+        assert diff.max() <= 2e-2
 
 
 def test_last_wave_split_workspace_is_reused_across_calls(fa):

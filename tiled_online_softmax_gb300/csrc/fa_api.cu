@@ -425,13 +425,30 @@ fa_status launch_split(const void* Q, const void* K, const void* V, void* O, flo
     return FA_OK;
 }
 
-// Last-wave balancing for fa_fwd / fa_fwd_lse (non-causal): when the units leave a partial
-// last wave of at most half the SMs, its units are split over keys so that the wave runs on
-// (about) all SMs for a fraction of the time. Returns false when nothing is worth splitting.
-bool plan_tail(int64_t units, int64_t Nk, SplitPlan* plan, int64_t* begin, int64_t* count) {
+// Shortest key range worth its own CTA: each range adds the CTA's fixed cost (start-up, first
+// products, epilogue: about five key steps) and a row of partial state to write and merge.
+constexpr int64_t MIN_SPLIT_TILES = 2;
+
+// Work balancing for fa_fwd / fa_fwd_lse (non-causal), by splitting units over keys:
+//  - fewer units than half the SMs: every unit is split into floor(SMs / units) key ranges of at
+//    least MIN_SPLIT_TILES tiles, so that one wave covers (nearly) all SMs;
+//  - a partial last wave of at most half the SMs: its units are split into 2-4 ranges, so that
+//    the wave runs on (about) all SMs for a fraction of the time.
+// Returns false when nothing is worth splitting.
+bool plan_balance(int64_t units, int64_t Nk, SplitPlan* plan, int64_t* begin, int64_t* count) {
+    const int64_t nkt = (Nk + fa::BN - 1) / fa::BN;
+    if (units <= NUM_SMS / 2) {
+        int64_t want = NUM_SMS / units;
+        if (want > nkt / MIN_SPLIT_TILES) want = nkt / MIN_SPLIT_TILES;
+        if (want < 2) return false;
+        *plan = plan_splits(units, Nk, want);
+        if (plan->num_splits < 2) return false;
+        *begin = 0;
+        *count = units;
+        return true;
+    }
     const int64_t tail = units % NUM_SMS;
     if (units <= NUM_SMS || tail == 0 || tail > NUM_SMS / 2) return false;
-    const int64_t nkt = (Nk + fa::BN - 1) / fa::BN;
     int64_t want = NUM_SMS / tail;
     if (want > 4) want = 4;
     if (nkt < 2 * want) return false;
@@ -466,13 +483,13 @@ fa_status library_workspace(size_t bytes, void** out) {
     return FA_OK;
 }
 
-// fa_fwd / fa_fwd_lse: one launch, or the last wave split over keys and merged.
+// fa_fwd / fa_fwd_lse: one launch, or some units split over keys and merged.
 fa_status forward(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
                   int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,
                   int dtype, cudaStream_t strm) {
     SplitPlan plan;
     int64_t begin = 0, count = 0;
-    if (!causal && g_tail_split && plan_tail(units_of(B, H, Nq), Nk, &plan, &begin, &count)) {
+    if (!causal && g_tail_split && plan_balance(units_of(B, H, Nq), Nk, &plan, &begin, &count)) {
         void* ws = nullptr;
         fa_status s = library_workspace(workspace_bytes(count, Nq, D, plan.num_splits), &ws);
         if (s != FA_OK) return s;

@@ -367,7 +367,8 @@ def set_rescale_threshold(log2_threshold: float) -> None:
 
 
 def set_tail_split(enable: bool) -> None:
-    """Turn the last-wave key split of forward() on or off (process-wide)."""
+    """Turn forward()'s work balancing (key splits of some units, then a merge) on or off
+    (process-wide)."""
     _raise_if(lib().fa_set_tail_split(int(bool(enable))))
 
 
