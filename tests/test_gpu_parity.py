@@ -287,3 +287,37 @@ def test_many_slices_with_split_last_wave(fa, orc):
         ref = orc.attention(*(inputs.bits_to_f64(bits[n][b, h], w.dtype) for n in "qkv"),
                             w.scale, False)
         parity.assert_parity(parity.compare(o[b, h], ref, w.dtype), True, f"slice ({b},{h})")
+
+
+@pytest.mark.parametrize("w", [
+    # 16 units split over keys in 4 (attention launch + merge launch), then a causal launch.
+    inputs.Workload("graph_split", 1, 4, 1024, 1024, 128, "bf16", False, seed=15),
+    inputs.Workload("graph_causal", 1, 8, 700, 700, 64, "f16", True, seed=16),
+], ids=lambda w: w.name)
+def test_cuda_graph_replay_matches_eager(fa, w):
+    """Each attention launch is a programmatic dependent of the stream's previous kernel. Two
+    forward calls captured back to back in a CUDA graph (the second reading the first's output as
+    its Q) replay to the same bits as the eager calls, replay after replay."""
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=o1)
+    fa.forward(o1, k, v, causal=w.causal, scale=w.scale, out=o2)  # also sizes the workspace
+    torch.cuda.synchronize()
+    want1, want2 = o1.clone(), o2.clone()
+    g = torch.cuda.CUDAGraph()
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        with torch.cuda.graph(g, stream=s):
+            fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=o1)
+            fa.forward(o1, k, v, causal=w.causal, scale=w.scale, out=o2)
+    torch.cuda.current_stream().wait_stream(s)
+    for _ in range(3):
+        o1.zero_()
+        o2.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        assert fa.last_device_error() == (0, 0)
+        assert torch.equal(o1.view(torch.int16), want1.view(torch.int16))
+        assert torch.equal(o2.view(torch.int16), want2.view(torch.int16))

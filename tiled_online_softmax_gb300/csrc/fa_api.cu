@@ -207,10 +207,22 @@ fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtens
     }
     const unsigned grid = static_cast<unsigned>(p.split_begin) +
                           static_cast<unsigned>(p.split_units) * static_cast<unsigned>(p.num_splits);
+    // Programmatic dependent launch: the CTAs may be scheduled while the stream's previous kernel
+    // finishes; each waits for it (griddepcontrol.wait) before touching global memory.
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(fa::NUM_THREADS);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
     const int ti = timer_begin(stream, FA_KERNEL_FWD);
-    kernel<<<grid, fa::NUM_THREADS, smem, stream>>>(mq, mk, mv, mo, p);
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mo, p);
     timer_end(stream, ti);
-    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return FA_OK;
 }

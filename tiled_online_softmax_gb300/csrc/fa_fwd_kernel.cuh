@@ -533,9 +533,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const Ctl ctl{abort_flag, p.err, p.timeout_ns};
-    // A grid launched after this one as a programmatic dependent (the merge of split key ranges)
-    // may be scheduled once every CTA of this grid has started; it still waits for this grid to
-    // complete before reading anything.
+    // This grid is launched as a programmatic dependent of the stream's previous kernel: the set-up
+    // above (shared memory, TMEM, tensor-map prefetch) may overlap that kernel's last CTAs, and
+    // nothing in global memory is touched before it has completed and its writes are visible.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Likewise a grid launched after this one as a programmatic dependent (the merge of split key
+    // ranges, or the next attention launch) may be scheduled once every CTA of this grid has
+    // started; it waits for this grid to complete before touching global memory.
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (wg == 2) {
