@@ -83,3 +83,22 @@ def test_backward_keys_past_all_queries_get_zero(fa):
     _, dk, dv = fa.backward(q, k, v, o, lse, do, causal=True, scale=w.scale)
     torch.cuda.synchronize()
     assert bool((dk[:, :, 130:] == 0).all()) and bool((dv[:, :, 130:] == 0).all())
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_backward_results_are_ordered_in_the_stream(fa, causal):
+    """The backward's kernels overlap one another (programmatic dependent launches), yet work
+    queued after fa_bwd on the same stream sees every gradient complete: copies taken there, with
+    no synchronisation in between, equal the gradients read after the device is idle."""
+    w = inputs.Workload("bwd_order", 1, 16, 2048, 2048, 128, "bf16", causal, seed=86)
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    do = inputs.to_torch(inputs.draw(w.with_(seed=w.seed + 1000))["q"], w.dtype).cuda()
+    o, lse = fa.forward_lse(q, k, v, causal=causal, scale=w.scale)
+    for _ in range(3):
+        grads = fa.backward(q, k, v, o, lse, do, causal=causal, scale=w.scale)
+        copies = [g.clone() for g in grads]
+        torch.cuda.synchronize()
+        assert fa.last_device_error()[0] == 0
+        for name, g, c in zip(("dq", "dk", "dv"), grads, copies):
+            assert torch.equal(g.view(torch.int16), c.view(torch.int16)), name

@@ -10,6 +10,7 @@
 #include <cstdlib>
 #include <cstring>
 #include <mutex>
+#include <utility>
 
 #include "fa.h"
 #include "fa_fwd_kernel.cuh"
@@ -191,6 +192,26 @@ fa_status device_state(int* dev_out, int** err_out) {
     return FA_OK;
 }
 
+// Launch `kernel` as a programmatic dependent of the stream's previous kernel: its blocks may be
+// scheduled while that kernel finishes, and each executes griddepcontrol.wait before it touches
+// global memory.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), unsigned grid, unsigned block, size_t smem,
+                       cudaStream_t stream, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+    return e == cudaSuccess ? cudaGetLastError() : e;
+}
+
 template <int D, bool BF16, bool CAUSAL>
 fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtensorMap& mk,
                           const CUtensorMap& mv, const CUtensorMap& mo, const fa::Params& p,
@@ -207,22 +228,9 @@ fa_status launch_instance(int dev, int inst, const CUtensorMap& mq, const CUtens
     }
     const unsigned grid = static_cast<unsigned>(p.split_begin) +
                           static_cast<unsigned>(p.split_units) * static_cast<unsigned>(p.num_splits);
-    // Programmatic dependent launch: the CTAs may be scheduled while the stream's previous kernel
-    // finishes; each waits for it (griddepcontrol.wait) before touching global memory.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(fa::NUM_THREADS);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     const int ti = timer_begin(stream, FA_KERNEL_FWD);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mo, p);
+    cudaError_t e = launch_pdl(kernel, grid, fa::NUM_THREADS, smem, stream, mq, mk, mv, mo, p);
     timer_end(stream, ti);
-    if (e == cudaSuccess) e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "kernel launch");
     return FA_OK;
 }
@@ -523,15 +531,15 @@ fa_status launch_rope(const void* X, void* Y, const float* cos_t, const float* s
     const bool bf16 = dtype == FA_BF16;
     const unsigned g = static_cast<unsigned>(blocks);
     const int ti = timer_begin(strm, FA_KERNEL_ROPE);
-    if (form == 0) {
-        if (bf16) fa::fa_rope_kernel<true, 0><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
-        else fa::fa_rope_kernel<false, 0><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
-    } else {
-        if (bf16) fa::fa_rope_kernel<true, 1><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
-        else fa::fa_rope_kernel<false, 1><<<g, 256, 0, strm>>>(x, y, cos_t, sin_t, rows_total, n, int(D));
-    }
+    const int di = int(D);
+    cudaError_t e;
+    if (form == 0)
+        e = bf16 ? launch_pdl(fa::fa_rope_kernel<true, 0>, g, 256, 0, strm, x, y, cos_t, sin_t, rows_total, n, di)
+                 : launch_pdl(fa::fa_rope_kernel<false, 0>, g, 256, 0, strm, x, y, cos_t, sin_t, rows_total, n, di);
+    else
+        e = bf16 ? launch_pdl(fa::fa_rope_kernel<true, 1>, g, 256, 0, strm, x, y, cos_t, sin_t, rows_total, n, di)
+                 : launch_pdl(fa::fa_rope_kernel<false, 1>, g, 256, 0, strm, x, y, cos_t, sin_t, rows_total, n, di);
     timer_end(strm, ti);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "rope kernel launch");
     return FA_OK;
 }
@@ -575,28 +583,17 @@ fa_status launch_bwd_instance(int dev, const CUtensorMap& mq, const CUtensorMap&
     const unsigned nkb = static_cast<unsigned>((p.nk + 127) / 128);
     const unsigned nqb = static_cast<unsigned>((p.nq + 127) / 128);
     int ti = timer_begin(strm, FA_KERNEL_BWD_DKDV);
-    k_kv<<<nkb * static_cast<unsigned>(p.bh), fa::BWD_THREADS, smem, strm>>>(mq, mk, mv, mdo, p);
+    cudaError_t e = launch_pdl(k_kv, nkb * static_cast<unsigned>(p.bh), fa::BWD_THREADS, smem, strm,
+                               mq, mk, mv, mdo, p);
     timer_end(strm, ti);
-    cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return cuda_fail(e, "backward dK/dV launch");
     // dQ depends only on the preprocessing (complete before the dK/dV kernel started), not on
     // dK/dV: a programmatic dependent launch lets its CTAs fill the SMs the dK/dV kernel's last
     // wave leaves idle.
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(nqb * static_cast<unsigned>(p.bh));
-    cfg.blockDim = dim3(fa::BWD_THREADS);
-    cfg.dynamicSmemBytes = smem_q;
-    cfg.stream = strm;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
     ti = timer_begin(strm, FA_KERNEL_BWD_DQ);
-    e = cudaLaunchKernelEx(&cfg, k_q, mq, mk, mv, mdo, p);
+    e = launch_pdl(k_q, nqb * static_cast<unsigned>(p.bh), fa::BWD_THREADS, smem_q, strm, mq, mk, mv, mdo, p);
     timer_end(strm, ti);
     if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
-    if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e, "backward dQ launch");
     return FA_OK;
 }
 
@@ -799,15 +796,15 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
         const int64_t threads = bh * nq_pad * (D / 8);
         const unsigned blocks = static_cast<unsigned>((threads + 255) / 256);
         const int ti = timer_begin(strm, FA_KERNEL_BWD_PREP);
-        if (D == 128) {
-            if (bf16) fa::fa_bwd_prep_kernel<128, true><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
-            else fa::fa_bwd_prep_kernel<128, false><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
-        } else {
-            if (bf16) fa::fa_bwd_prep_kernel<64, true><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
-            else fa::fa_bwd_prep_kernel<64, false><<<blocks, 256, 0, strm>>>(O, dO, LSE, lse2, delta, int(bh), int(Nq), int(nq_pad));
-        }
+        const int ibh = int(bh), inq = int(Nq), ipad = int(nq_pad);
+        cudaError_t e;
+        if (D == 128)
+            e = bf16 ? launch_pdl(fa::fa_bwd_prep_kernel<128, true>, blocks, 256, 0, strm, O, dO, LSE, lse2, delta, ibh, inq, ipad)
+                     : launch_pdl(fa::fa_bwd_prep_kernel<128, false>, blocks, 256, 0, strm, O, dO, LSE, lse2, delta, ibh, inq, ipad);
+        else
+            e = bf16 ? launch_pdl(fa::fa_bwd_prep_kernel<64, true>, blocks, 256, 0, strm, O, dO, LSE, lse2, delta, ibh, inq, ipad)
+                     : launch_pdl(fa::fa_bwd_prep_kernel<64, false>, blocks, 256, 0, strm, O, dO, LSE, lse2, delta, ibh, inq, ipad);
         timer_end(strm, ti);
-        cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess) return cuda_fail(e, "backward prep launch");
     }
     CUtensorMap mq, mk, mv, mdo;

@@ -57,6 +57,11 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const void* __restrict
                                                           float* __restrict__ lse2,
                                                           float* __restrict__ delta, int bh,
                                                           int nq, int nq_pad) {
+    // Launched as a programmatic dependent: O and dO may come from the stream's previous kernel.
+    // The dK/dV kernel, launched after this one the same way, may take SMs as soon as every block
+    // here has started; it waits for this grid to complete before reading anything.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     constexpr int TPR = D / 8;  // threads per row, 8 elements each
     const int64_t w = (static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x) / TPR;
     const int sub = threadIdx.x % TPR;
@@ -245,8 +250,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int n = nqb > i_begin ? nqb - i_begin : 0;
     const uint32_t tmem = bwd_setup<D>(smem, sbase, ptx::smem_u32(tmem_slot), tmem_slot, abort_flag, 1);
     const Ctl ctl{abort_flag, p.err, p.timeout_ns};
+    // Launched as a programmatic dependent of the preprocessing: its outputs (and Q, K, V, dO,
+    // possibly from earlier kernels) are read only after it has completed.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
     // The dQ kernel is launched as a programmatic dependent of this one and reads nothing this
-    // kernel writes, so it may take SMs as soon as every CTA here has started.
+    // kernel writes, so it may take SMs as soon as every CTA here has started (and, being past
+    // the wait above, the preprocessing has completed).
     if (threadIdx.x == 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     if (warp == BWD_LOAD_WARP) {
@@ -659,6 +668,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, TMEM_COLS);
     }
+    // This grid does not wait for the dK/dV kernel it was launched after (it reads nothing that
+    // kernel writes), but it completes only after it, so that work later in the stream that
+    // waits for this grid also sees dK and dV: one CTA, the last one, waits for it before exiting.
+    // Waiting in every CTA would hold SMs that later CTAs of this grid could use.
+    if (blockIdx.x == gridDim.x - 1) asm volatile("griddepcontrol.wait;" ::: "memory");
 }
 
 }  // namespace fa

@@ -44,6 +44,9 @@ __global__ void __launch_bounds__(256) fa_rope_kernel(const uint16_t* x, uint16_
                                                       const float* __restrict__ cos_t,
                                                       const float* __restrict__ sin_t,
                                                       int64_t rows_total, int64_t n, int d) {
+    // Launched as a programmatic dependent: X may come from the stream's previous kernel.
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     const int half = d / 2;
     const int groups = half / 8;  // groups of 8 pairs per row (a power of two: d/16)
     const int shift = __ffs(groups) - 1;
