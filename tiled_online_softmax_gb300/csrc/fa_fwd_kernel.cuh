@@ -278,17 +278,24 @@ __device__ __forceinline__ void epilogue(int t, uint32_t tmem, uint32_t sbase, c
     // written by TMA: whole 128-byte row segments instead of one 16-byte store per row.
     const float inv_l = (l > 0.f) ? 1.f / l : 0.f;
     const uint32_t stage = sbase + L::Q_OFF + t * L::Q_TILE_BYTES;
-#pragma unroll 1
+    // All of the row's O at once (D columns), then one wait.
+    uint32_t o[D / 32][32];
+    if constexpr (D == 128) {
+        ptx::tmem_ld128(o_cols, o);
+    } else {
+#pragma unroll
+        for (int q = 0; q < D / 32; ++q) ptx::tmem_ld32(o_cols + q * 32, o[q]);
+    }
+    ptx::tmem_wait_ld();
+#pragma unroll
+    for (int q = 0; q < D / 32; ++q) ptx::reg_fence(o[q]);
+#pragma unroll
     for (int q = 0; q < D / 32; ++q) {
-        uint32_t o[32];
-        ptx::tmem_ld32(o_cols + q * 32, o);
-        ptx::tmem_wait_ld();
-        ptx::reg_fence(o);
         uint32_t packed[16];
 #pragma unroll
         for (int i = 0; i < 16; ++i)
-            packed[i] = pack2<BF16>(__uint_as_float(o[2 * i]) * inv_l,
-                                    __uint_as_float(o[2 * i + 1]) * inv_l);
+            packed[i] = pack2<BF16>(__uint_as_float(o[q][2 * i]) * inv_l,
+                                    __uint_as_float(o[q][2 * i + 1]) * inv_l);
         // 32 columns = 4 chunks of 16 bytes in column block q / 2, chunks 4 (q % 2) + v of the
         // row; chunk c of row r sits at chunk position c ^ (r % 8).
         const uint32_t row_base = stage + (q / 2) * (BM * 128) + r * 128;
@@ -548,12 +555,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // -------------------------------------------------------------- TMA producer
             if (lane == 0) {
                 const uint32_t sq = sbase + L::Q_OFF, sk = sbase + L::K_OFF, sv = sbase + L::V_OFF;
-                for (int t = 0; t < Q_TILES; ++t) {
+                auto load_q = [&](int t) {
                     ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL + t), L::Q_TILE_BYTES);
                     for (int c = 0; c < L::COL_BLOCKS; ++c)
                         ptx::tma_load_3d(sq + t * L::Q_TILE_BYTES + c * (BM * 128), &tm_q, c * 64,
                                          q0 + t * BM, bh, bar(L::B_Q_FULL + t));
-                }
+                };
+                // Q_0, then K_0, then the other Q tiles: the first product S_0(0) needs only the
+                // first two.
+                load_q(0);
+                int q_loaded = 1;
                 const int n = n_tiles[Q_TILES - 1];
                 int issued = 0;
                 for (int j = 0; j < n; ++j) {
@@ -565,6 +576,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ptx::tma_load_3d(sk + st * L::KV_BYTES + c * (BN * 128), &tm_k, c * 64,
                                          (kv0 + j) * BN, bh, bar(L::B_K_FULL + st));
                     issued = 2 * j + 1;
+                    if (j == 0) {
+                        for (int t = 1; t < Q_TILES; ++t) load_q(t);
+                        q_loaded = Q_TILES;
+                    }
                     if (!wait_bar(bar(L::B_V_EMPTY + st), ph ^ 1, ctl, SITE_LOAD_V_EMPTY)) break;
                     ptx::mbar_arrive_expect_tx(bar(L::B_V_FULL + st), L::KV_BYTES);
                     for (int c = 0; c < L::COL_BLOCKS; ++c)
@@ -575,7 +590,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (*abort_flag) {
                     // Drain: every copy this thread started must land before the CTA's shared
                     // memory is released. The last copy into each stage is its newest phase.
-                    for (int t = 0; t < Q_TILES; ++t)
+                    for (int t = 0; t < q_loaded; ++t)
                         wait_bar(bar(L::B_Q_FULL + t), 0, ctl, SITE_DRAIN, false);
                     for (int x = (issued > 2 * STAGES ? issued - 2 * STAGES : 0); x < issued; ++x) {
                         const int j = x / 2, st = j % STAGES;
