@@ -565,7 +565,7 @@ template <int D, bool BF16, bool CAUSAL>
 fa_status launch_bwd_instance(int dev, const CUtensorMap& mq, const CUtensorMap& mk,
                               const CUtensorMap& mv, const CUtensorMap& mdo, const fa::BwdParams& p,
                               cudaStream_t strm) {
-    constexpr int smem = fa::BwdSmem<D>::ALLOC_BYTES;
+    constexpr int smem = fa::BwdSmem<D, CAUSAL>::ALLOC_BYTES;
     constexpr int smem_q = fa::DqSmem<D>::ALLOC_BYTES;
     auto k_kv = fa::fa_bwd_dkdv_kernel<D, BF16, CAUSAL>;
     auto k_q = fa::fa_bwd_dq_kernel<D, BF16, CAUSAL>;
@@ -1002,6 +1002,8 @@ fa_status fa_last_device_error(void* stream, int* site) {
     if (word == 0) return FA_OK;
     if (site) *site = word;
     if ((e = cudaMemset(g_err_word[dev], 0, 16)) != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
+    if (word == fa::SITE_BWD_SMEM_LAYOUT)
+        return fail(FA_ERR_UNSUPPORTED, "the dK/dV kernel could not align its shared memory (site %d)", word);
     return fail(FA_ERR_TIMEOUT, "a kernel gave up waiting at site %d", word);
 }
 

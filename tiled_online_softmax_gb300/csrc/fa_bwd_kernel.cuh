@@ -45,6 +45,7 @@ enum BwdSite : int {
     SITE_BWD_MMA = 22,
     SITE_BWD_COMPUTE = 23,
     SITE_BWD_DRAIN = 24,
+    SITE_BWD_SMEM_LAYOUT = 25,  // dynamic shared memory too little aligned for the layout: no work done
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -97,24 +98,31 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const void* __restrict
 // ---------------------------------------------------------------------------------------------
 // shared memory of the two main kernels
 // ---------------------------------------------------------------------------------------------
-template <int D>
+template <int D, bool CAUSAL>
 struct BwdSmem {
     static constexpr int COL_BLOCKS = D / 64;
     static constexpr int TILE = 128 * D * 2;          // one 128-row tile of Q, K, V or dO
-    static constexpr int STAGES = 2;
-    // Two resident tiles (R0, R1), then two rings of STAGES tiles (A, B), then per-stage
-    // vectors (lse2, delta: 2 x 128 floats).
-    static constexpr int R0_OFF = 0;
-    static constexpr int R1_OFF = TILE;
-    static constexpr int A_OFF = 2 * TILE;
-    static constexpr int B_OFF = A_OFF + STAGES * TILE;
-    static constexpr int VEC_OFF = B_OFF + STAGES * TILE;
-    static constexpr int BAR_OFF = VEC_OFF + STAGES * 1024;
-    static constexpr int B_RES_FULL = 0;              // resident tiles landed
-    static constexpr int B_A_FULL = 1;                // [STAGES]
-    static constexpr int B_B_FULL = B_A_FULL + STAGES;  // [STAGES]
-    static constexpr int B_EMPTY = B_B_FULL + STAGES;   // [STAGES]
-    static constexpr int B_S_FULL = B_EMPTY + STAGES;
+    // Non-causal (SPLIT): Q_i is read by S^T(i) and dK(i), dO_i by dP^T(i) and dV(i), which
+    // comes first; so Q gets the deeper ring (three stages: Q_{i+3} loads while block i+1 runs)
+    // and dO two. dO's stage also holds the block's per-query vectors (lse2, delta: 2 x 128
+    // floats), freed when dV(i) has run and the compute warps have read them.
+    // Causal: one ring of two stages holds Q_i, dO_i and the vectors together, loaded on Q_FULL
+    // and freed on Q_EMPTY once dK(i) has run (the split rings measured slower there).
+    static constexpr bool SPLIT = !CAUSAL;
+    static constexpr int Q_STAGES = SPLIT ? 3 : 2;
+    static constexpr int DO_STAGES = 2;
+    static constexpr int R0_OFF = 0;                   // K block (resident)
+    static constexpr int R1_OFF = TILE;                // V block (resident)
+    static constexpr int A_OFF = 2 * TILE;             // Q ring
+    static constexpr int B_OFF = A_OFF + Q_STAGES * TILE;   // dO ring
+    static constexpr int VEC_OFF = B_OFF + DO_STAGES * TILE;
+    static constexpr int BAR_OFF = VEC_OFF + DO_STAGES * 1024;
+    static constexpr int B_RES_FULL = 0;                       // resident tiles landed
+    static constexpr int B_Q_FULL = 1;                         // [Q_STAGES]
+    static constexpr int B_Q_EMPTY = B_Q_FULL + Q_STAGES;      // [Q_STAGES] dK(i) done
+    static constexpr int B_DO_FULL = B_Q_EMPTY + Q_STAGES;     // [DO_STAGES] dO_i + vectors (SPLIT)
+    static constexpr int B_DO_EMPTY = B_DO_FULL + DO_STAGES;   // [DO_STAGES] dV(i) + 4 warps (SPLIT)
+    static constexpr int B_S_FULL = B_DO_EMPTY + DO_STAGES;
     static constexpr int B_DP_FULL = B_S_FULL + 1;
     static constexpr int B_P_HALF = B_DP_FULL + 1;      // P^T of queries 0-63 stored
     static constexpr int B_P_FULL = B_P_HALF + 1;
@@ -125,8 +133,14 @@ struct BwdSmem {
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
     static constexpr int BYTES = ABORT_OFF + 4;
-    static constexpr int ALLOC_BYTES = (BYTES + 1024 > 116 * 1024) ? BYTES + 1024 : 116 * 1024;
-    static_assert(ALLOC_BYTES <= 232448, "shared memory budget");
+    // Up to 1024 bytes of slack for aligning the base to 1024 bytes (the 128-byte swizzle atom
+    // repeats every 8 rows), as far as the 227 KB limit allows; the kernel checks at run time
+    // that the slack it needs is there.
+    // At least 116 KB, so that two CTAs never share an SM: each holds all 512 TMEM columns.
+    static constexpr int MAX_BYTES = 232448;
+    static constexpr int FIT_BYTES = BYTES + 1024 <= MAX_BYTES ? BYTES + 1024 : MAX_BYTES;
+    static constexpr int ALLOC_BYTES = FIT_BYTES > 116 * 1024 ? FIT_BYTES : 116 * 1024;
+    static_assert(BYTES + 256 <= MAX_BYTES, "shared memory budget");
 };
 
 // Operand descriptors of a 128-row tile staged by TMA in 64-column blocks (128-byte swizzle).
@@ -181,21 +195,23 @@ __device__ __forceinline__ void zero_row(void* dst_row) {
     for (int i = 0; i < D / 8; ++i) d[i] = make_uint4(0, 0, 0, 0);
 }
 
-// Common prologue: barriers, TMEM. Returns the TMEM base.
-template <int D>
+// Prologue of the dK/dV kernel: barriers, TMEM. Returns the TMEM base.
+template <int D, bool CAUSAL>
 __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t sbase, uint32_t tmem_slot_addr,
-                                              uint32_t* tmem_slot, volatile int* abort_flag,
-                                              int a_full_count) {
-    using L = BwdSmem<D>;
+                                              uint32_t* tmem_slot, volatile int* abort_flag) {
+    using L = BwdSmem<D, CAUSAL>;
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
         *abort_flag = 0;
         ptx::mbar_init(bar(L::B_RES_FULL), 1);
-        for (int s = 0; s < L::STAGES; ++s) {
-            ptx::mbar_init(bar(L::B_A_FULL + s), a_full_count);
-            ptx::mbar_init(bar(L::B_B_FULL + s), 1);
-            ptx::mbar_init(bar(L::B_EMPTY + s), 1);
+        for (int s = 0; s < L::Q_STAGES; ++s) {
+            ptx::mbar_init(bar(L::B_Q_FULL + s), 1);
+            ptx::mbar_init(bar(L::B_Q_EMPTY + s), 1);
+        }
+        for (int s = 0; s < L::DO_STAGES; ++s) {
+            ptx::mbar_init(bar(L::B_DO_FULL + s), 1);
+            ptx::mbar_init(bar(L::B_DO_EMPTY + s), 1 + 4);  // the dV commit and the 4 compute warps
         }
         ptx::mbar_init(bar(L::B_S_FULL), 1);
         ptx::mbar_init(bar(L::B_DP_FULL), 1);
@@ -232,11 +248,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     fa_bwd_dkdv_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                        const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
                        const BwdParams p) {
-    using L = BwdSmem<D>;
-    constexpr int STAGES = L::STAGES;
+    using L = BwdSmem<D, CAUSAL>;
+    constexpr int QS = L::Q_STAGES, DS = L::DO_STAGES;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_u32(smem_raw);
-    uint8_t* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const uint32_t pad = ((raw + 1023u) & ~1023u) - raw;
+    if (pad + L::BYTES > static_cast<uint32_t>(L::ALLOC_BYTES)) {
+        // Not enough slack to align the layout (never seen: the dynamic window starts 1024-byte
+        // aligned). Report it and do nothing; no barrier or TMEM is in use yet.
+        if (threadIdx.x == 0) atomicCAS(p.err, 0, SITE_BWD_SMEM_LAYOUT);
+        return;
+    }
+    uint8_t* smem = smem_raw + pad;
     const uint32_t sbase = ptx::smem_u32(smem);
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + L::ABORT_OFF);
@@ -248,7 +271,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int k0 = kb * 128;
     const int i_begin = CAUSAL ? kb : 0;  // query blocks before the diagonal see none of these keys
     const int n = nqb > i_begin ? nqb - i_begin : 0;
-    const uint32_t tmem = bwd_setup<D>(smem, sbase, ptx::smem_u32(tmem_slot), tmem_slot, abort_flag, 1);
+    const uint32_t tmem = bwd_setup<D, CAUSAL>(smem, sbase, ptx::smem_u32(tmem_slot), tmem_slot, abort_flag);
     const Ctl ctl{abort_flag, p.err, p.timeout_ns};
     // Launched as a programmatic dependent of the preprocessing: its outputs (and Q, K, V, dO,
     // possibly from earlier kernels) are read only after it has completed.
@@ -263,23 +286,34 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::mbar_arrive_expect_tx(bar(L::B_RES_FULL), 2 * L::TILE);
             tma_tile<D>(sbase + L::R0_OFF, &tm_k, k0, bh, bar(L::B_RES_FULL));
             tma_tile<D>(sbase + L::R1_OFF, &tm_v, k0, bh, bar(L::B_RES_FULL));
-            int issued = 0;
+            int issued_q = 0, issued_do = 0;
             for (int it = 0; it < n; ++it) {
-                const int st = it % STAGES;
-                if (!wait_bar(bar(L::B_EMPTY + st), ((it / STAGES) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
                 const int i = i_begin + it;
-                ptx::mbar_arrive_expect_tx(bar(L::B_A_FULL + st), 2 * L::TILE + 1024);
-                tma_tile<D>(sbase + L::A_OFF + st * L::TILE, &tm_q, i * 128, bh, bar(L::B_A_FULL + st));
-                tma_tile<D>(sbase + L::B_OFF + st * L::TILE, &tm_do, i * 128, bh, bar(L::B_A_FULL + st));
+                const int qs = it % QS, ds = it % DS;
+                if (!wait_bar(bar(L::B_Q_EMPTY + qs), ((it / QS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
+                // Without SPLIT the dO tile and the vectors ride on Q_i's barrier (ds == qs).
+                const int do_bar = L::SPLIT ? L::B_DO_FULL + ds : L::B_Q_FULL + qs;
+                ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL + qs), L::SPLIT ? L::TILE : 2 * L::TILE + 1024);
+                tma_tile<D>(sbase + L::A_OFF + qs * L::TILE, &tm_q, i * 128, bh, bar(L::B_Q_FULL + qs));
+                issued_q = it + 1;
+                if constexpr (L::SPLIT) {
+                    if (!wait_bar(bar(L::B_DO_EMPTY + ds), ((it / DS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
+                    ptx::mbar_arrive_expect_tx(bar(do_bar), L::TILE + 1024);
+                }
+                tma_tile<D>(sbase + L::B_OFF + ds * L::TILE, &tm_do, i * 128, bh, bar(do_bar));
                 const size_t vo = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(i) * 128;
-                ptx::bulk_load(sbase + L::VEC_OFF + st * 1024, p.lse2 + vo, 512, bar(L::B_A_FULL + st));
-                ptx::bulk_load(sbase + L::VEC_OFF + st * 1024 + 512, p.delta + vo, 512, bar(L::B_A_FULL + st));
-                issued = it + 1;
+                ptx::bulk_load(sbase + L::VEC_OFF + ds * 1024, p.lse2 + vo, 512, bar(do_bar));
+                ptx::bulk_load(sbase + L::VEC_OFF + ds * 1024 + 512, p.delta + vo, 512, bar(do_bar));
+                issued_do = it + 1;
             }
             if (*abort_flag) {
+                // The newest copy into each buffer is its newest phase.
                 wait_bar(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_DRAIN, false);
-                for (int it = (issued > STAGES ? issued - STAGES : 0); it < issued; ++it)
-                    wait_bar(bar(L::B_A_FULL + it % STAGES), (it / STAGES) & 1, ctl, SITE_BWD_DRAIN, false);
+                for (int it = (issued_q > QS ? issued_q - QS : 0); it < issued_q; ++it)
+                    wait_bar(bar(L::B_Q_FULL + it % QS), (it / QS) & 1, ctl, SITE_BWD_DRAIN, false);
+                if (L::SPLIT)
+                    for (int it = (issued_do > DS ? issued_do - DS : 0); it < issued_do; ++it)
+                        wait_bar(bar(L::B_DO_FULL + it % DS), (it / DS) & 1, ctl, SITE_BWD_DRAIN, false);
             }
         }
         __syncwarp();
@@ -289,8 +323,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         constexpr uint32_t IDESC_OD = ptx::idesc_f16(BF16, 128, D, false, true);
         const uint32_t d_s = tmem + BWD_TMEM_S, d_dp = tmem + BWD_TMEM_DP;
         const uint32_t d_dv = tmem + BWD_TMEM_A, d_dk = tmem + BWD_TMEM_B;
-        auto stage_q = [&](int it) { return sbase + L::A_OFF + (it % STAGES) * L::TILE; };
-        auto stage_do = [&](int it) { return sbase + L::B_OFF + (it % STAGES) * L::TILE; };
+        auto stage_q = [&](int it) { return sbase + L::A_OFF + (it % QS) * L::TILE; };
+        auto stage_do = [&](int it) { return sbase + L::B_OFF + (it % DS) * L::TILE; };
         auto issue_s = [&](int it) {  // S^T = K Q_i^T
 #pragma unroll
             for (int kk = 0; kk < D / 16; ++kk)
@@ -303,11 +337,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         };
         auto commit = [&](int b) { ptx::mma_commit_if(leader, bar(b)); };
         bool ok = n > 0 && wait_bar_warp(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_MMA) &&
-                  wait_bar_warp(bar(L::B_A_FULL + 0), 0, ctl, SITE_BWD_MMA);
+                  wait_bar_warp(bar(L::B_Q_FULL + 0), 0, ctl, SITE_BWD_MMA);
         if (ok) {
             ptx::tc_fence_after();
             issue_s(0);
             commit(L::B_S_FULL);
+            if constexpr (L::SPLIT) ok = wait_bar_warp(bar(L::B_DO_FULL + 0), 0, ctl, SITE_BWD_MMA);
+        }
+        if (ok) {
+            ptx::tc_fence_after();
             issue_dp(0);
             commit(L::B_DP_FULL);
         }
@@ -323,8 +361,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                                     (it > 0 || kk > 0));
             }
             if (!ok) break;
+            if constexpr (L::SPLIT) commit(L::B_DO_EMPTY + it % DS);  // dO_i's last reader
             if (it + 1 < n) {  // S^T of the next block may overwrite P^T now (MMAs run in order)
-                if (!(ok = wait_bar_warp(bar(L::B_A_FULL + (it + 1) % STAGES), ((it + 1) / STAGES) & 1, ctl, SITE_BWD_MMA))) break;
+                if (!(ok = wait_bar_warp(bar(L::B_Q_FULL + (it + 1) % QS), ((it + 1) / QS) & 1, ctl, SITE_BWD_MMA))) break;
                 ptx::tc_fence_after();
                 issue_s(it + 1);
                 commit(L::B_S_FULL);
@@ -335,8 +374,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk)
                 ptx::mma_ts_if(leader, d_dk, d_dp + kk * 8, mnmajor_desc(stage_q(it), kk), IDESC_OD, (it > 0 || kk > 0));
-            commit(L::B_EMPTY + it % STAGES);
+            commit(L::B_Q_EMPTY + it % QS);  // Q_i's last reader
             if (it + 1 < n) {
+                if constexpr (L::SPLIT) {
+                    if (!(ok = wait_bar_warp(bar(L::B_DO_FULL + (it + 1) % DS), ((it + 1) / DS) & 1, ctl, SITE_BWD_MMA))) break;
+                    ptx::tc_fence_after();
+                }
                 issue_dp(it + 1);
                 commit(L::B_DP_FULL);
             }
@@ -357,8 +400,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         bool ok = true;
         for (int it = 0; it < n; ++it) {
             const int i = i_begin + it;
-            const float* vec = reinterpret_cast<const float*>(smem + L::VEC_OFF + (it % STAGES) * 1024);
+            const float* vec = reinterpret_cast<const float*>(smem + L::VEC_OFF + (it % DS) * 1024);
             if (!(ok = wait_bar_warp(bar(L::B_S_FULL), it & 1, ctl, SITE_BWD_COMPUTE))) break;
+            // The vectors travel with dO_i (usually landed long before S^T(i) is ready); without
+            // SPLIT they landed with Q_i, before S^T(i) was computed.
+            if constexpr (L::SPLIT)
+                if (!(ok = wait_bar_warp(bar(L::B_DO_FULL + it % DS), (it / DS) & 1, ctl, SITE_BWD_COMPUTE))) break;
             ptx::tc_fence_after();
             uint32_t sr[4][32];
 #pragma unroll
@@ -411,6 +458,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(L::B_DS_FULL));
+            if constexpr (L::SPLIT) {
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(bar(L::B_DO_EMPTY + it % DS));  // done with the vectors
+            }
         }
         // Epilogue: dV and scale * dK for this thread's key row.
         const size_t row_off = (static_cast<size_t>(bh) * p.nk + kr) * D * 2;
