@@ -267,6 +267,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int nkb = (p.nk + 127) / 128, nqb = (p.nq + 127) / 128;
+    // The CTAs of one slice are adjacent (they share Q and dO in L2). Under causal masking the
+    // longest ones (kb = 0) come first within each slice; ordering them longest-first across all
+    // slices instead measured 5 % slower on a 16 x 16384 launch (Q and dO of every slice in flight).
     const int bh = blockIdx.x / nkb, kb = blockIdx.x % nkb;
     const int k0 = kb * 128;
     const int i_begin = CAUSAL ? kb : 0;  // query blocks before the diagonal see none of these keys
@@ -537,7 +540,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
 
     const int nkb = (p.nk + 127) / 128, nqb = (p.nq + 127) / 128;
-    const int bh = blockIdx.x / nqb, qb = blockIdx.x % nqb;
+    // Causal: the query blocks with the most key blocks (the last ones) first, across all slices,
+    // so the last CTAs dispatched are the shortest (slice by slice, each slice's longest CTA came
+    // last: 4-9 % slower); otherwise the CTAs of one slice are adjacent.
+    const int bh = CAUSAL ? static_cast<int>(blockIdx.x % p.bh) : static_cast<int>(blockIdx.x / nqb);
+    const int qb = CAUSAL ? nqb - 1 - static_cast<int>(blockIdx.x / p.bh) : static_cast<int>(blockIdx.x % nqb);
     const int q0 = qb * 128;
     const int n = CAUSAL ? min(nkb, qb + 1) : nkb;  // key blocks up to the diagonal
 
