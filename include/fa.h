@@ -30,6 +30,12 @@
  * Errors: every entry point returns a fa_status. Argument checks happen before any CUDA call;
  * a rejected call has no side effect. fa_last_error_message() gives a one-line reason for the
  * last non-FA_OK status returned on the calling host thread.
+ *
+ * Stream order: libfa's kernels are launched as programmatic dependents of the kernel before
+ * them in the stream (their start-up overlaps its last blocks), but each waits for that kernel
+ * to complete before touching global memory, and each call's results are complete for any work
+ * queued after it on the stream. Stream semantics are therefore those of ordinary launches,
+ * also under CUDA graph capture.
  */
 #ifndef TILED_ONLINE_SOFTMAX_FA_H
 #define TILED_ONLINE_SOFTMAX_FA_H

@@ -321,3 +321,27 @@ def test_cuda_graph_replay_matches_eager(fa, w):
         assert fa.last_device_error() == (0, 0)
         assert torch.equal(o1.view(torch.int16), want1.view(torch.int16))
         assert torch.equal(o2.view(torch.int16), want2.view(torch.int16))
+
+
+@pytest.mark.parametrize("w", [
+    inputs.Workload("order_split", 1, 4, 1024, 1024, 128, "bf16", False, seed=17),  # fwd + merge
+    inputs.Workload("order_causal", 1, 16, 2048, 2048, 128, "bf16", True, seed=18),
+], ids=lambda w: w.name)
+def test_results_are_ordered_in_the_stream(fa, w):
+    """Work queued right after a forward call on the same stream (here a copy of O, and a second
+    call that reads O as its Q) sees the call's complete result, with no synchronisation between
+    them: the copies equal O read once the device is idle, and the chained call equals the same
+    call run on its own."""
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    for _ in range(3):
+        fa.forward(q, k, v, causal=w.causal, scale=w.scale, out=o1)
+        copy = o1.clone()
+        fa.forward(o1, k, v, causal=w.causal, scale=w.scale, out=o2)
+        torch.cuda.synchronize()
+        assert fa.last_device_error() == (0, 0)
+        assert torch.equal(copy.view(torch.int16), o1.view(torch.int16))
+        alone = fa.forward(copy, k, v, causal=w.causal, scale=w.scale)
+        torch.cuda.synchronize()
+        assert torch.equal(alone.view(torch.int16), o2.view(torch.int16))
