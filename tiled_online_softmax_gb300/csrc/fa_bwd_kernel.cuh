@@ -104,23 +104,27 @@ struct BwdSmem {
     static constexpr int TILE = 128 * D * 2;          // one 128-row tile of Q, K, V or dO
     // Non-causal (SPLIT): Q_i is read by S^T(i) and dK(i), dO_i by dP^T(i) and dV(i), which
     // comes first; so Q gets the deeper ring (three stages: Q_{i+3} loads while block i+1 runs)
-    // and dO two. dO's stage also holds the block's per-query vectors (lse2, delta: 2 x 128
-    // floats), freed when dV(i) has run and the compute warps have read them.
-    // Causal: one ring of two stages holds Q_i, dO_i and the vectors together, loaded on Q_FULL
-    // and freed on Q_EMPTY once dK(i) has run (the split rings measured slower there).
+    // and dO two. Each Q stage also holds the block's lse2 (128 floats, read for P^T), each dO
+    // stage its delta (read for dS^T, after dP^T(i) has read dO_i): the compute warps never wait
+    // on a load themselves. A dO stage is freed when dV(i) has run and the compute warps have
+    // read its delta.
+    // Causal: one ring of two stages; Q_i, dO_i, lse2 and delta all land on Q_FULL and are freed
+    // on Q_EMPTY once dK(i) has run (the split rings measured 6-11 % slower there).
     static constexpr bool SPLIT = !CAUSAL;
     static constexpr int Q_STAGES = SPLIT ? 3 : 2;
     static constexpr int DO_STAGES = 2;
+    static constexpr int VEC_BYTES = 128 * 4;
     static constexpr int R0_OFF = 0;                   // K block (resident)
     static constexpr int R1_OFF = TILE;                // V block (resident)
     static constexpr int A_OFF = 2 * TILE;             // Q ring
     static constexpr int B_OFF = A_OFF + Q_STAGES * TILE;   // dO ring
-    static constexpr int VEC_OFF = B_OFF + DO_STAGES * TILE;
-    static constexpr int BAR_OFF = VEC_OFF + DO_STAGES * 1024;
+    static constexpr int LSE_OFF = B_OFF + DO_STAGES * TILE;           // lse2 per Q stage
+    static constexpr int DELTA_OFF = LSE_OFF + Q_STAGES * VEC_BYTES;  // delta per dO stage
+    static constexpr int BAR_OFF = DELTA_OFF + DO_STAGES * VEC_BYTES;
     static constexpr int B_RES_FULL = 0;                       // resident tiles landed
     static constexpr int B_Q_FULL = 1;                         // [Q_STAGES]
     static constexpr int B_Q_EMPTY = B_Q_FULL + Q_STAGES;      // [Q_STAGES] dK(i) done
-    static constexpr int B_DO_FULL = B_Q_EMPTY + Q_STAGES;     // [DO_STAGES] dO_i + vectors (SPLIT)
+    static constexpr int B_DO_FULL = B_Q_EMPTY + Q_STAGES;     // [DO_STAGES] dO_i + delta (SPLIT)
     static constexpr int B_DO_EMPTY = B_DO_FULL + DO_STAGES;   // [DO_STAGES] dV(i) + 4 warps (SPLIT)
     static constexpr int B_S_FULL = B_DO_EMPTY + DO_STAGES;
     static constexpr int B_DP_FULL = B_S_FULL + 1;
@@ -293,20 +297,23 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             for (int it = 0; it < n; ++it) {
                 const int i = i_begin + it;
                 const int qs = it % QS, ds = it % DS;
-                if (!wait_bar(bar(L::B_Q_EMPTY + qs), ((it / QS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
-                // Without SPLIT the dO tile and the vectors ride on Q_i's barrier (ds == qs).
+                const size_t vo = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(i) * 128;
+                // Without SPLIT, dO_i and delta land on Q_i's barrier too (ds == qs).
                 const int do_bar = L::SPLIT ? L::B_DO_FULL + ds : L::B_Q_FULL + qs;
-                ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL + qs), L::SPLIT ? L::TILE : 2 * L::TILE + 1024);
+                if (!wait_bar(bar(L::B_Q_EMPTY + qs), ((it / QS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
+                ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL + qs),
+                                           L::SPLIT ? L::TILE + L::VEC_BYTES : 2 * (L::TILE + L::VEC_BYTES));
                 tma_tile<D>(sbase + L::A_OFF + qs * L::TILE, &tm_q, i * 128, bh, bar(L::B_Q_FULL + qs));
+                ptx::bulk_load(sbase + L::LSE_OFF + qs * L::VEC_BYTES, p.lse2 + vo, L::VEC_BYTES,
+                               bar(L::B_Q_FULL + qs));
                 issued_q = it + 1;
                 if constexpr (L::SPLIT) {
                     if (!wait_bar(bar(L::B_DO_EMPTY + ds), ((it / DS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
-                    ptx::mbar_arrive_expect_tx(bar(do_bar), L::TILE + 1024);
+                    ptx::mbar_arrive_expect_tx(bar(do_bar), L::TILE + L::VEC_BYTES);
                 }
                 tma_tile<D>(sbase + L::B_OFF + ds * L::TILE, &tm_do, i * 128, bh, bar(do_bar));
-                const size_t vo = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(i) * 128;
-                ptx::bulk_load(sbase + L::VEC_OFF + ds * 1024, p.lse2 + vo, 512, bar(do_bar));
-                ptx::bulk_load(sbase + L::VEC_OFF + ds * 1024 + 512, p.delta + vo, 512, bar(do_bar));
+                ptx::bulk_load(sbase + L::DELTA_OFF + ds * L::VEC_BYTES, p.delta + vo, L::VEC_BYTES,
+                               bar(do_bar));
                 issued_do = it + 1;
             }
             if (*abort_flag) {
@@ -403,12 +410,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         bool ok = true;
         for (int it = 0; it < n; ++it) {
             const int i = i_begin + it;
-            const float* vec = reinterpret_cast<const float*>(smem + L::VEC_OFF + (it % DS) * 1024);
+            // lse2 landed with Q_i (before S^T(i) was computed), delta with dO_i (before dP^T(i)).
+            const float* lse2 = reinterpret_cast<const float*>(smem + L::LSE_OFF + (it % QS) * L::VEC_BYTES);
+            const float* dlt = reinterpret_cast<const float*>(smem + L::DELTA_OFF + (it % DS) * L::VEC_BYTES);
             if (!(ok = wait_bar_warp(bar(L::B_S_FULL), it & 1, ctl, SITE_BWD_COMPUTE))) break;
-            // The vectors travel with dO_i (usually landed long before S^T(i) is ready); without
-            // SPLIT they landed with Q_i, before S^T(i) was computed.
-            if constexpr (L::SPLIT)
-                if (!(ok = wait_bar_warp(bar(L::B_DO_FULL + it % DS), (it / DS) & 1, ctl, SITE_BWD_COMPUTE))) break;
             ptx::tc_fence_after();
             uint32_t sr[4][32];
 #pragma unroll
@@ -428,7 +433,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int q = 2 * h + qq, col = q * 32 + e;
-                        float pv = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -vec[col]));
+                        float pv = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -lse2[col]));
                         if (diag && i * 128 + col < kr) pv = 0.f;
                         pf[col] = pv;
                     }
@@ -453,7 +458,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 float ds[32];
 #pragma unroll
                 for (int e = 0; e < 32; ++e)
-                    ds[e] = pf[q * 32 + e] * (__uint_as_float(dr[e]) - vec[128 + q * 32 + e]);
+                    ds[e] = pf[q * 32 + e] * (__uint_as_float(dr[e]) - dlt[q * 32 + e]);
                 uint32_t w[16];
                 pack16<BF16>(ds, w);
                 ptx::tmem_st16(dp_cols + q * 16, w);
@@ -463,7 +468,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::mbar_arrive(bar(L::B_DS_FULL));
             if constexpr (L::SPLIT) {
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(L::B_DO_EMPTY + it % DS));  // done with the vectors
+                if (lane == 0) ptx::mbar_arrive(bar(L::B_DO_EMPTY + it % DS));  // done with delta
             }
         }
         // Epilogue: dV and scale * dK for this thread's key row.
