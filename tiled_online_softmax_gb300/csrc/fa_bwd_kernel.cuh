@@ -699,19 +699,27 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 }
             if (!(ok = wait_bar_warp(bar(L::B_DP_FULL), j & 1, ctl, SITE_BWD_COMPUTE))) break;
             ptx::tc_fence_after();
-            // dS = P (dP - D), written over this block's S buffer (all of S is in registers).
+            // dS = P (dP - D), written over this block's S buffer (all of S is in registers). dP
+            // comes in two loads of 64 columns, each waited for once.
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                uint32_t dr[32];
-                ptx::tmem_ld32(dp_cols + q * 32, dr);
+            for (int h = 0; h < 2; ++h) {
+                uint32_t dr[2][32];
+                ptx::tmem_ld32(dp_cols + (2 * h) * 32, dr[0]);
+                ptx::tmem_ld32(dp_cols + (2 * h + 1) * 32, dr[1]);
                 ptx::tmem_wait_ld();
-                ptx::reg_fence(dr);
-                float ds[32];
+                ptx::reg_fence(dr[0]);
+                ptx::reg_fence(dr[1]);
 #pragma unroll
-                for (int e = 0; e < 32; ++e) ds[e] = pf[q * 32 + e] * (__uint_as_float(dr[e]) - dlt);
-                uint32_t w[16];
-                pack16<BF16>(ds, w);
-                ptx::tmem_st16(s_cols + q * 16, w);
+                for (int qq = 0; qq < 2; ++qq) {
+                    const int q = 2 * h + qq;
+                    float ds[32];
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        ds[e] = pf[q * 32 + e] * (__uint_as_float(dr[qq][e]) - dlt);
+                    uint32_t w[16];
+                    pack16<BF16>(ds, w);
+                    ptx::tmem_st16(s_cols + q * 16, w);
+                }
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
