@@ -114,6 +114,12 @@ def test_headline_full_size(fa, orc):
     sampled_check(fa, orc, w, [(0, 0), (0, 31)], 128)
 
 
+def test_headline_d64_full_size(fa, orc):
+    """The headline shape at D = 64 in fp16 (4-stage K/V ring, split last wave)."""
+    w = inputs.WORKLOADS["headline_d64"]
+    sampled_check(fa, orc, w, [(0, 0), (0, 17), (0, 31)], 96)
+
+
 # --- edge cases ------------------------------------------------------------------------------
 
 EDGE_SIZES = [1, 2, 63, 64, 65, 127, 128, 129, 255, 257]
