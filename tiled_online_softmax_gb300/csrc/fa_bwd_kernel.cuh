@@ -14,8 +14,12 @@
 //   fa_bwd_dq_kernel    one CTA per 128 queries: S = Q K_j^T (two TMEM buffers, computed ahead)
 //                       and dP = dO V_j^T, dS over S, dQ += dS K_j, over every key block j.
 // Warp roles (192 threads): warps 0-3 compute (thread r owns TMEM lane r: a key row in the
-// first kernel, a query row in the second), warp 4 issues MMAs (an elected lane) and owns TMEM,
-// warp 5 issues TMA copies. Every wait is bounded as in the forward kernel.
+// first kernel, a query row in the second), warp 4 issues MMAs (an elected lane, predicated
+// issue) and owns TMEM, warp 5 issues TMA copies. Every wait is bounded as in the forward kernel.
+// The three kernels are launched back to back as programmatic dependents: the dK/dV kernel
+// waits for the preprocessing before reading anything; the dQ kernel reads nothing the dK/dV
+// kernel writes and does not wait for it, except in its last CTA, so that the dQ grid
+// completes after the dK/dV grid.
 #pragma once
 
 #include "fa_fwd_kernel.cuh"

@@ -25,11 +25,16 @@
 //                            max and sum need no shuffles. When a row of the warp moves its
 //                            reference max, the warp also rescales its rows of O_0 in TMEM.
 //   warpgroup 1 (warps 4-7)  softmax of query tile 1.
-//                            After its key loop each of them writes its tile: O_t / l, rounded.
-//   warp 8                   MMA issuer (an elected lane issues) and TMEM owner.
-//   warp 9                   TMA producer (one lane): Q_0 and Q_1 once, then K and V tiles
+//                            After its key loop each of them writes its tile: O_t / l, rounded,
+//                            staged in shared memory and stored by TMA.
+//   warp 8                   MMA issuer (one elected lane issues, as predicated instructions
+//                            the whole warp runs) and TMEM owner.
+//   warp 9                   TMA producer (one lane): Q_0, K_0, Q_1, V_0, then K and V tiles
 //                            through rings of stages.
 //   warps 10-11              idle.
+// The grid is launched as a programmatic dependent of the stream's previous kernel; its set-up
+// may overlap that kernel's end, and nothing in global memory is touched before
+// griddepcontrol.wait.
 // The MMA warp issues, per key tile j: PV_0(j) in two halves (keys 0-63 as soon as the softmax
 // releases them, then 64-127), S_0(j+1), PV_1(j) likewise, S_1(j+1). While one tile's softmax
 // runs, the tensor cores work on the other tile's products.
