@@ -269,7 +269,9 @@ fa_status fa_wait_selftest(unsigned long long timeout_ns, void* stream);
  * maximum exceeds the reference by at most this much (the conditional rescaling paragraph of
  * ithelp article 10405336, "FlashAttention 保留三個狀態"). O / l is unchanged by the choice;
  * the 16-bit weights P stay <= 2^threshold. 0 rescales on every rise of the maximum. Range
- * [0, 15] (fp16 P must stay finite); default 8. Affects launches made after the call.
+ * [0, 64]; default 32. fp16 launches use min(threshold, 15), so that their weights stay below
+ * the fp16 maximum; bf16 weights have fp32's exponent range and keep their relative precision
+ * at any size, and O and l accumulate in fp32. Affects launches made after the call.
  */
 fa_status fa_set_rescale_threshold(float log2_threshold);
 float fa_get_rescale_threshold(void);

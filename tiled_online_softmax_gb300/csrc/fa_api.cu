@@ -79,7 +79,15 @@ std::mutex g_mutex;
 int* g_err_word[MAX_DEVICES] = {};         // device error word per device (16 bytes)
 int g_arch_ok[MAX_DEVICES] = {};           // 0 unknown, 1 sm_103, -1 other
 unsigned g_attr_set[MAX_DEVICES] = {};     // bit per kernel instance: smem attribute applied
-float g_rescale_threshold = 8.0f;          // lazy-rescale threshold (log2 units)
+float g_rescale_threshold = 32.0f;         // lazy-rescale threshold (log2 units)
+// fp16 weights P <= 2^threshold must stay below the fp16 maximum (65504 < 2^16); bf16 has
+// fp32's exponent range, and the fp32 accumulators O and l hold far larger values.
+constexpr float FP16_RESCALE_THRESHOLD_MAX = 15.0f;
+float rescale_threshold_for(int dtype) {
+    return dtype == FA_F16 && g_rescale_threshold > FP16_RESCALE_THRESHOLD_MAX
+               ? FP16_RESCALE_THRESHOLD_MAX
+               : g_rescale_threshold;
+}
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -268,7 +276,7 @@ fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LS
     p.nk = static_cast<int>(Nk);
     p.num_units = static_cast<int>((Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS);
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    p.rescale_threshold = g_rescale_threshold;
+    p.rescale_threshold = rescale_threshold_for(int(dtype));
     p.timeout_ns = wait_timeout_ns();
     const int total_units = p.num_units * p.bh;
     const bool splitting = split.split_begin >= 0 && split.split_units > 0 && split.num_splits > 1;
@@ -634,7 +642,7 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, i
     p.split_begin = p.num_units * p.bh;
     p.split_units = 0;
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
-    p.rescale_threshold = g_rescale_threshold;
+    p.rescale_threshold = rescale_threshold_for(int(dtype));
     p.timeout_ns = wait_timeout_ns();
     const int inst = (D == 128 ? 4 : 0) + (dtype == FA_BF16 ? 2 : 0) + (causal ? 1 : 0);
     switch (inst) {
@@ -1022,8 +1030,8 @@ const char* fa_status_string(fa_status status) {
 const char* fa_last_error_message(void) { return g_msg; }
 
 fa_status fa_set_rescale_threshold(float log2_threshold) {
-    if (!std::isfinite(log2_threshold) || log2_threshold < 0.f || log2_threshold > 15.f)
-        return fail(FA_ERR_INVALID_ARGUMENT, "rescale threshold must be in [0, 15], got %g",
+    if (!std::isfinite(log2_threshold) || log2_threshold < 0.f || log2_threshold > 64.f)
+        return fail(FA_ERR_INVALID_ARGUMENT, "rescale threshold must be in [0, 64], got %g",
                     double(log2_threshold));
     g_rescale_threshold = log2_threshold;
     return FA_OK;

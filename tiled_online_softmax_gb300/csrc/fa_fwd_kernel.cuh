@@ -16,9 +16,9 @@
 // to HBM"). The recurrence is section 11.6 "Online softmax" one key block at a time ("Flash
 // Attention 2", "Overview of the algorithm"; phobos "Attention", `online_softmax`). The maximum
 // is updated lazily: while a row's new maximum exceeds its reference maximum by at most a
-// threshold (8 in log2 units), the reference is kept and nothing is rescaled (the conditional
-// rescaling of ithelp article 10405336, FlashAttention 保留三個狀態); l and O share the
-// reference, so O / l is unchanged and P stays <= 2^threshold.
+// threshold (log2 units: 32 for bf16, at most 15 for fp16), the reference is kept and nothing is
+// rescaled (the conditional rescaling of ithelp article 10405336, FlashAttention 保留三個狀態);
+// l and O share the reference, so O / l is unchanged and P stays <= 2^threshold.
 //
 // Warp roles (384 threads, registers rebalanced with setmaxnreg):
 //   warpgroup 0 (warps 0-3)  softmax of query tile 0: thread r owns row r (TMEM lane r), so row

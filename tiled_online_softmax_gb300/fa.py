@@ -362,7 +362,8 @@ def wait_selftest(timeout_ns: int, stream=None) -> None:
 
 
 def set_rescale_threshold(log2_threshold: float) -> None:
-    """Process-wide lazy-rescale threshold (log2 units; 0 = rescale on every rise)."""
+    """Process-wide lazy-rescale threshold (log2 units, [0, 64]; 0 = rescale on every rise;
+    fp16 launches use at most 15)."""
     _raise_if(lib().fa_set_rescale_threshold(float(log2_threshold)))
 
 
