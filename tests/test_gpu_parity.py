@@ -156,6 +156,17 @@ def test_late_maximum(fa, orc):
     parity.assert_parity(parity.compare(inputs.from_torch(o), ref, "f16"), True, "late max")
 
 
+@pytest.mark.parametrize("w", [
+    inputs.Workload("neg_scale", 1, 3, 300, 333, 128, "bf16", False, scale=-0.0883883, seed=19),
+    inputs.Workload("neg_scale_causal", 2, 2, 257, 257, 64, "f16", True, scale=-0.125, seed=20),
+    inputs.Workload("neg_scale_split", 1, 2, 200, 2000, 64, "bf16", False, scale=-0.5, seed=21),
+], ids=lambda w: w.name)
+def test_negative_scale(fa, orc, w):
+    """A negative scale (the largest weights go to the most negative scores) matches the oracle,
+    through the single launch, the causal mask and the key split with its merge."""
+    full_check(fa, orc, w, literal=False)
+
+
 def test_all_equal_scores_give_mean(fa):
     """Q = 0: every visible key weighs the same, O is the (prefix) mean of V."""
     for causal in (False, True):

@@ -343,8 +343,11 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
     const uint32_t o_cols = tmem + lane_base + tmem_o(t);
     // A zero scale would turn the -inf of a hidden score into 0 * inf = NaN; a tiny positive
     // scale gives the same weights (every visible score maps to 2^0 = 1) and keeps -inf -> 0.
-    const float c = (p.scale_log2 == 0.f) ? 1e-30f : p.scale_log2;
-    const bool neg = c < 0.f;
+    const float c_signed = (p.scale_log2 == 0.f) ? 1e-30f : p.scale_log2;
+    // A negative scale is applied as |c| to negated scores (s * c == (-s) * |c|), so the maximum,
+    // the masks and the exponentials below have one form: the MMA warp then computes S with
+    // A = -Q (the instruction descriptor's negate-A bit).
+    const float c = fabsf(c_signed);
     const float tau = p.rescale_threshold;
     float m_ref = -INFINITY;  // reference max of the scaled scores (log2 units)
     float l = 0.f;            // running denominator relative to m_ref
@@ -364,7 +367,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
         int lim = p.nk - k0;
         if constexpr (CAUSAL) lim = min(lim, row + 1 - k0);
         if (need_mask) {
-            const uint32_t hidden = neg ? 0x7f800000u : 0xff800000u;  // +inf / -inf
+            const uint32_t hidden = 0xff800000u;  // -inf
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
@@ -372,9 +375,9 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
                     if (q * 32 + i >= lim) sr[q][i] = hidden;
         }
 
-        // Tile maximum on the raw scores (scaling by c >= 0 is monotone; c < 0 uses the min),
-        // as four independent chains per block of 32 columns: chain c of block q covers columns
-        // c, c + 4, c + 8, ... so the 3-input steps of different chains overlap.
+        // Tile maximum on the raw scores (scaling by c > 0 is monotone), as four independent
+        // chains per block of 32 columns: chain c of block q covers columns c, c + 4, c + 8, ...
+        // so the 3-input steps of different chains overlap.
         float mx[4];
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
@@ -385,19 +388,14 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
             for (int i = 4; i < 28; i += 8)
 #pragma unroll
                 for (int c = 0; c < 4; ++c)
-                    ch[c] = neg ? ptx::fmin3(ch[c], __uint_as_float(sr[q][i + c]),
-                                             __uint_as_float(sr[q][i + 4 + c]))
-                                : ptx::fmax3(ch[c], __uint_as_float(sr[q][i + c]),
-                                             __uint_as_float(sr[q][i + 4 + c]));
+                    ch[c] = ptx::fmax3(ch[c], __uint_as_float(sr[q][i + c]),
+                                       __uint_as_float(sr[q][i + 4 + c]));
 #pragma unroll
             for (int c = 0; c < 4; ++c)
-                ch[c] = neg ? fminf(ch[c], __uint_as_float(sr[q][28 + c]))
-                            : fmaxf(ch[c], __uint_as_float(sr[q][28 + c]));
-            mx[q] = neg ? fminf(fminf(ch[0], ch[1]), fminf(ch[2], ch[3]))
-                        : fmaxf(fmaxf(ch[0], ch[1]), fmaxf(ch[2], ch[3]));
+                ch[c] = fmaxf(ch[c], __uint_as_float(sr[q][28 + c]));
+            mx[q] = fmaxf(fmaxf(ch[0], ch[1]), fmaxf(ch[2], ch[3]));
         }
-        const float mraw = neg ? fminf(fminf(mx[0], mx[1]), fminf(mx[2], mx[3]))
-                               : fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
+        const float mraw = fmaxf(fmaxf(mx[0], mx[1]), fmaxf(mx[2], mx[3]));
         const float m_tile = (mraw == INFINITY || mraw == -INFINITY) ? -INFINITY : mraw * c;
 
         // Lazy reference update: move m_ref only when the row max rose by more than tau.
@@ -427,7 +425,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
                     float x0, x1;
                     ptx::ffma2(x0, x1, __uint_as_float(sr[q][i]), __uint_as_float(sr[q][i + 1]),
                                c, neg_m);
-                    // A hidden score holds -inf (+inf when c < 0), so its weight is 2^-inf = 0.
+                    // A hidden score holds -inf, so its weight is 2^-inf = 0.
                     const float p0 = ptx::ex2(x0), p1 = ptx::ex2(x1);
                     const uint32_t u = pack2<BF16>(p0, p1);
                     ptx::add_halves<BF16>(acc[(i >> 1) & 3], acc[4 + ((i >> 1) & 3)], u);
@@ -613,7 +611,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             uint32_t leader;
             asm volatile("{\n\t.reg .pred P;\n\telect.sync _|P, 0xffffffff;\n\tselp.u32 %0, 1, 0, P;\n\t}"
                          : "=r"(leader));
-            constexpr uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false);
+            // S = Q K^T, or -(Q K^T) under a negative scale (negate-A bit of the descriptor).
+            const uint32_t IDESC_S = ptx::idesc_f16(BF16, BM, BN, false, false) |
+                                     (p.scale_log2 < 0.f ? ptx::IDESC_NEGATE_A : 0u);
             constexpr uint32_t IDESC_O = ptx::idesc_f16(BF16, BM, D, false, true);
             const uint32_t sq = sbase + L::Q_OFF, sk = sbase + L::K_OFF, sv = sbase + L::V_OFF;
             // S_t = Q_t K_j^T: K-dimension D in steps of 16 elements (32 bytes inside a 128-byte

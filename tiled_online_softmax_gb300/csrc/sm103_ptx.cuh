@@ -287,6 +287,10 @@ __device__ __forceinline__ uint64_t sdesc_sw128(uint32_t smem_addr, uint32_t lbo
     return d;
 }
 
+// Instruction-descriptor bit that negates the A operand of a kind::f16 MMA (bit 13; bit 14
+// negates B).
+constexpr uint32_t IDESC_NEGATE_A = 1u << 13;
+
 // Instruction descriptor for kind::f16 with an fp32 accumulator:
 //   [4,6) D format (1 = f32), [7,10) A format, [10,13) B format (0 = f16, 1 = bf16),
 //   [15] A major (0 = K-major), [16] B major (1 = MN-major), [17,23) N >> 3, [24,29) M >> 4.
@@ -364,11 +368,6 @@ __device__ __forceinline__ void ffma2(float& d0, float& d1, float a0, float a1, 
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
     float d;
     asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
-    return d;
-}
-__device__ __forceinline__ float fmin3(float a, float b, float c) {
-    float d;
-    asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
     return d;
 }
 
