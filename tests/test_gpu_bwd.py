@@ -33,6 +33,11 @@ CASES = [
     inputs.Workload("bwd_causal_bf16", 2, 2, 384, 384, 128, "bf16", True, seed=83),
     inputs.Workload("bwd_causal_ragged_f16", 1, 2, 200, 333, 64, "f16", True, seed=84),
     inputs.Workload("bwd_long_bf16", 1, 2, 1024, 1024, 128, "bf16", True, seed=85),
+    # A negative scale: hidden scores then hold +inf, so that 2^(s*c - L) is still 0.
+    inputs.Workload("bwd_neg_scale_causal_f16", 1, 2, 300, 300, 64, "f16", True, scale=-0.125,
+                    seed=88),
+    inputs.Workload("bwd_neg_scale_ragged_bf16", 1, 2, 200, 333, 128, "bf16", False,
+                    scale=-0.0883883, seed=89),
 ]
 
 

@@ -410,7 +410,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const int kr = k0 + r;
         const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
         const uint32_t s_cols = tmem + lanes + BWD_TMEM_S, dp_cols = tmem + lanes + BWD_TMEM_DP;
-        const float c = p.scale_log2;
+        // A zero scale would turn a hidden score's -inf into 0 * inf = NaN; a tiny one gives the
+        // same weights. Hidden scores hold -inf (+inf under a negative scale), so 2^(s*c - L)
+        // is 0 for them with no per-element test in the exponential loop.
+        const float c = (p.scale_log2 == 0.f) ? 1e-30f : p.scale_log2;
+        const uint32_t hidden = c < 0.f ? 0x7f800000u : 0xff800000u;
         bool ok = true;
         for (int it = 0; it < n; ++it) {
             const int i = i_begin + it;
@@ -428,6 +432,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             // P^T[r][col] = 2^(s*c - LSE2[col]); padded queries have LSE2 = +inf, so P = 0.
             // On the diagonal block a query before this key (q < k) does not see it.
             const bool diag = CAUSAL && (i == kb);
+            if (diag) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (i * 128 + q * 32 + e < kr) sr[q][e] = hidden;
+            }
             float pf[128];
             // P^T in two halves of 64 queries, each released to the dV product once stored.
 #pragma unroll
@@ -437,9 +448,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
                     for (int e = 0; e < 32; ++e) {
                         const int q = 2 * h + qq, col = q * 32 + e;
-                        float pv = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -lse2[col]));
-                        if (diag && i * 128 + col < kr) pv = 0.f;
-                        pf[col] = pv;
+                        pf[col] = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -lse2[col]));
                     }
                 uint32_t pk[32];
 #pragma unroll
@@ -673,7 +682,11 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         const int row = q0 + r;
         const uint32_t lanes = static_cast<uint32_t>(warp * 32) << 16;
         const uint32_t dp_cols = tmem + lanes + DQ_TMEM_DP;
-        const float c = p.scale_log2;
+        // A zero scale would turn a hidden score's -inf into 0 * inf = NaN; a tiny one gives the
+        // same weights. Hidden scores hold -inf (+inf under a negative scale), so 2^(s*c - L)
+        // is 0 for them with no per-element test in the exponential loop.
+        const float c = (p.scale_log2 == 0.f) ? 1e-30f : p.scale_log2;
+        const uint32_t hidden = c < 0.f ? 0x7f800000u : 0xff800000u;
         const size_t vo = static_cast<size_t>(bh) * p.nq_pad + row;  // row < nq_pad always
         const float lse2 = p.lse2[vo], dlt = p.delta[vo];
         bool ok = true;
@@ -691,16 +704,19 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             const int k0 = j * 128;
             int lim = p.nk - k0;
             if constexpr (CAUSAL) lim = min(lim, row + 1 - k0);
-            const bool need_mask = lim < 128;
+            if (lim < 128) {
+#pragma unroll
+                for (int q = 0; q < 4; ++q)
+#pragma unroll
+                    for (int e = 0; e < 32; ++e)
+                        if (q * 32 + e >= lim) sr[q][e] = hidden;
+            }
             float pf[128];
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int e = 0; e < 32; ++e) {
-                    float pv = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -lse2));
-                    if (need_mask && q * 32 + e >= lim) pv = 0.f;
-                    pf[q * 32 + e] = pv;
-                }
+                for (int e = 0; e < 32; ++e)
+                    pf[q * 32 + e] = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -lse2));
             if (!(ok = wait_bar_warp(bar(L::B_DP_FULL), j & 1, ctl, SITE_BWD_COMPUTE))) break;
             ptx::tc_fence_after();
             // dS = P (dP - D), written over this block's S buffer (all of S is in registers). dP
