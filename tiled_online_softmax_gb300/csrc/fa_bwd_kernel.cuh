@@ -99,6 +99,33 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const void* __restrict
     }
 }
 
+// Packed fp32 arithmetic of the compute warps (pairs of columns in one instruction).
+// {d0, d1} = {a0, a1} * {b0, b1} + {c0, c1}, one packed fused multiply-add.
+__device__ __forceinline__ void ffma2v(float& d0, float& d1, float a0, float a1, float b0, float b1,
+                                       float c0, float c1) {
+    asm("{\n\t.reg .b64 a, b, c, d;\n\t"
+        "mov.b64 a, {%2, %3};\n\t"
+        "mov.b64 b, {%4, %5};\n\t"
+        "mov.b64 c, {%6, %7};\n\t"
+        "fma.rn.f32x2 d, a, b, c;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(a0), "f"(a1), "f"(b0), "f"(b1), "f"(c0), "f"(c1));
+}
+// {d0, d1} = {p0, p1} * ({x0, x1} - {y0, y1}): a packed subtract, then a packed multiply.
+__device__ __forceinline__ void fmulsub2(float& d0, float& d1, float p0, float p1, float x0, float x1,
+                                         float y0, float y1) {
+    asm("{\n\t.reg .b64 p, x, y, d;\n\t"
+        "mov.b64 p, {%2, %3};\n\t"
+        "mov.b64 x, {%4, %5};\n\t"
+        "mov.b64 y, {%6, %7};\n\t"
+        "sub.rn.f32x2 d, x, y;\n\t"
+        "mul.rn.f32x2 d, p, d;\n\t"
+        "mov.b64 {%0, %1}, d;\n\t}"
+        : "=f"(d0), "=f"(d1)
+        : "f"(p0), "f"(p1), "f"(x0), "f"(x1), "f"(y0), "f"(y1));
+}
+
 // ---------------------------------------------------------------------------------------------
 // shared memory of the two main kernels
 // ---------------------------------------------------------------------------------------------
@@ -446,9 +473,13 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
                 for (int qq = 0; qq < 2; ++qq)
 #pragma unroll
-                    for (int e = 0; e < 32; ++e) {
+                    for (int e = 0; e < 32; e += 2) {
                         const int q = 2 * h + qq, col = q * 32 + e;
-                        pf[col] = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -lse2[col]));
+                        float x0, x1;
+                        ffma2v(x0, x1, __uint_as_float(sr[q][e]), __uint_as_float(sr[q][e + 1]), c, c,
+                                    -lse2[col], -lse2[col + 1]);
+                        pf[col] = ptx::ex2(x0);
+                        pf[col + 1] = ptx::ex2(x1);
                     }
                 uint32_t pk[32];
 #pragma unroll
@@ -470,8 +501,10 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 ptx::reg_fence(dr);
                 float ds[32];
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    ds[e] = pf[q * 32 + e] * (__uint_as_float(dr[e]) - dlt[q * 32 + e]);
+                for (int e = 0; e < 32; e += 2)
+                    fmulsub2(ds[e], ds[e + 1], pf[q * 32 + e], pf[q * 32 + e + 1],
+                                  __uint_as_float(dr[e]), __uint_as_float(dr[e + 1]),
+                                  dlt[q * 32 + e], dlt[q * 32 + e + 1]);
                 uint32_t w[16];
                 pack16<BF16>(ds, w);
                 ptx::tmem_st16(dp_cols + q * 16, w);
@@ -715,8 +748,12 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 #pragma unroll
             for (int q = 0; q < 4; ++q)
 #pragma unroll
-                for (int e = 0; e < 32; ++e)
-                    pf[q * 32 + e] = ptx::ex2(fmaf(__uint_as_float(sr[q][e]), c, -lse2));
+                for (int e = 0; e < 32; e += 2) {
+                    float x0, x1;
+                    ptx::ffma2(x0, x1, __uint_as_float(sr[q][e]), __uint_as_float(sr[q][e + 1]), c, -lse2);
+                    pf[q * 32 + e] = ptx::ex2(x0);
+                    pf[q * 32 + e + 1] = ptx::ex2(x1);
+                }
             if (!(ok = wait_bar_warp(bar(L::B_DP_FULL), j & 1, ctl, SITE_BWD_COMPUTE))) break;
             ptx::tc_fence_after();
             // dS = P (dP - D), written over this block's S buffer (all of S is in registers). dP
@@ -734,8 +771,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                     const int q = 2 * h + qq;
                     float ds[32];
 #pragma unroll
-                    for (int e = 0; e < 32; ++e)
-                        ds[e] = pf[q * 32 + e] * (__uint_as_float(dr[qq][e]) - dlt);
+                    for (int e = 0; e < 32; e += 2)
+                        fmulsub2(ds[e], ds[e + 1], pf[q * 32 + e], pf[q * 32 + e + 1],
+                                      __uint_as_float(dr[qq][e]), __uint_as_float(dr[qq][e + 1]), dlt, dlt);
                     uint32_t w[16];
                     pack16<BF16>(ds, w);
                     ptx::tmem_st16(s_cols + q * 16, w);
