@@ -133,16 +133,12 @@ template <int D, bool CAUSAL>
 struct BwdSmem {
     static constexpr int COL_BLOCKS = D / 64;
     static constexpr int TILE = 128 * D * 2;          // one 128-row tile of Q, K, V or dO
-    // Non-causal (SPLIT): Q_i is read by S^T(i) and dK(i), dO_i by dP^T(i) and dV(i), which
-    // comes first; so Q gets the deeper ring (three stages: Q_{i+3} loads while block i+1 runs)
-    // and dO two. Each Q stage also holds the block's lse2 (128 floats, read for P^T), each dO
-    // stage its delta (read for dS^T, after dP^T(i) has read dO_i): the compute warps never wait
-    // on a load themselves. A dO stage is freed when dV(i) has run and the compute warps have
-    // read its delta.
-    // Causal: one ring of two stages; Q_i, dO_i, lse2 and delta all land on Q_FULL and are freed
-    // on Q_EMPTY once dK(i) has run (the split rings measured 6-11 % slower there).
-    static constexpr bool SPLIT = !CAUSAL;
-    static constexpr int Q_STAGES = SPLIT ? 3 : 2;
+    // Q_i is read by S^T(i) and dK(i), dO_i by dP^T(i) and dV(i), which comes first; so Q gets
+    // the deeper ring (three stages: Q_{i+3} loads while block i+1 runs) and dO two. Each Q stage
+    // also holds the block's lse2 (128 floats, read for P^T), each dO stage its delta (read for
+    // dS^T, after dP^T(i) has read dO_i): the compute warps never wait on a load themselves.
+    // A dO stage is freed when dV(i) has run and the compute warps have read its delta.
+    static constexpr int Q_STAGES = 3;
     static constexpr int DO_STAGES = 2;
     static constexpr int VEC_BYTES = 128 * 4;
     static constexpr int R0_OFF = 0;                   // K block (resident)
@@ -155,8 +151,8 @@ struct BwdSmem {
     static constexpr int B_RES_FULL = 0;                       // resident tiles landed
     static constexpr int B_Q_FULL = 1;                         // [Q_STAGES]
     static constexpr int B_Q_EMPTY = B_Q_FULL + Q_STAGES;      // [Q_STAGES] dK(i) done
-    static constexpr int B_DO_FULL = B_Q_EMPTY + Q_STAGES;     // [DO_STAGES] dO_i + delta (SPLIT)
-    static constexpr int B_DO_EMPTY = B_DO_FULL + DO_STAGES;   // [DO_STAGES] dV(i) + 4 warps (SPLIT)
+    static constexpr int B_DO_FULL = B_Q_EMPTY + Q_STAGES;     // [DO_STAGES] dO_i + delta
+    static constexpr int B_DO_EMPTY = B_DO_FULL + DO_STAGES;   // [DO_STAGES] dV(i) + 4 warps
     static constexpr int B_S_FULL = B_DO_EMPTY + DO_STAGES;
     static constexpr int B_DP_FULL = B_S_FULL + 1;
     static constexpr int B_P_HALF = B_DP_FULL + 1;      // P^T of queries 0-63 stored
@@ -329,19 +325,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 const int i = i_begin + it;
                 const int qs = it % QS, ds = it % DS;
                 const size_t vo = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(i) * 128;
-                // Without SPLIT, dO_i and delta land on Q_i's barrier too (ds == qs).
-                const int do_bar = L::SPLIT ? L::B_DO_FULL + ds : L::B_Q_FULL + qs;
+                const int do_bar = L::B_DO_FULL + ds;
                 if (!wait_bar(bar(L::B_Q_EMPTY + qs), ((it / QS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
-                ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL + qs),
-                                           L::SPLIT ? L::TILE + L::VEC_BYTES : 2 * (L::TILE + L::VEC_BYTES));
+                ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL + qs), L::TILE + L::VEC_BYTES);
                 tma_tile<D>(sbase + L::A_OFF + qs * L::TILE, &tm_q, i * 128, bh, bar(L::B_Q_FULL + qs));
                 ptx::bulk_load(sbase + L::LSE_OFF + qs * L::VEC_BYTES, p.lse2 + vo, L::VEC_BYTES,
                                bar(L::B_Q_FULL + qs));
                 issued_q = it + 1;
-                if constexpr (L::SPLIT) {
-                    if (!wait_bar(bar(L::B_DO_EMPTY + ds), ((it / DS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
-                    ptx::mbar_arrive_expect_tx(bar(do_bar), L::TILE + L::VEC_BYTES);
-                }
+                if (!wait_bar(bar(L::B_DO_EMPTY + ds), ((it / DS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
+                ptx::mbar_arrive_expect_tx(bar(do_bar), L::TILE + L::VEC_BYTES);
                 tma_tile<D>(sbase + L::B_OFF + ds * L::TILE, &tm_do, i * 128, bh, bar(do_bar));
                 ptx::bulk_load(sbase + L::DELTA_OFF + ds * L::VEC_BYTES, p.delta + vo, L::VEC_BYTES,
                                bar(do_bar));
@@ -352,9 +344,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 wait_bar(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_DRAIN, false);
                 for (int it = (issued_q > QS ? issued_q - QS : 0); it < issued_q; ++it)
                     wait_bar(bar(L::B_Q_FULL + it % QS), (it / QS) & 1, ctl, SITE_BWD_DRAIN, false);
-                if (L::SPLIT)
-                    for (int it = (issued_do > DS ? issued_do - DS : 0); it < issued_do; ++it)
-                        wait_bar(bar(L::B_DO_FULL + it % DS), (it / DS) & 1, ctl, SITE_BWD_DRAIN, false);
+                for (int it = (issued_do > DS ? issued_do - DS : 0); it < issued_do; ++it)
+                    wait_bar(bar(L::B_DO_FULL + it % DS), (it / DS) & 1, ctl, SITE_BWD_DRAIN, false);
             }
         }
         __syncwarp();
@@ -383,7 +374,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::tc_fence_after();
             issue_s(0);
             commit(L::B_S_FULL);
-            if constexpr (L::SPLIT) ok = wait_bar_warp(bar(L::B_DO_FULL + 0), 0, ctl, SITE_BWD_MMA);
+            ok = wait_bar_warp(bar(L::B_DO_FULL + 0), 0, ctl, SITE_BWD_MMA);
         }
         if (ok) {
             ptx::tc_fence_after();
@@ -402,7 +393,7 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                                     (it > 0 || kk > 0));
             }
             if (!ok) break;
-            if constexpr (L::SPLIT) commit(L::B_DO_EMPTY + it % DS);  // dO_i's last reader
+            commit(L::B_DO_EMPTY + it % DS);  // dO_i's last reader
             if (it + 1 < n) {  // S^T of the next block may overwrite P^T now (MMAs run in order)
                 if (!(ok = wait_bar_warp(bar(L::B_Q_FULL + (it + 1) % QS), ((it + 1) / QS) & 1, ctl, SITE_BWD_MMA))) break;
                 ptx::tc_fence_after();
@@ -417,10 +408,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 ptx::mma_ts_if(leader, d_dk, d_dp + kk * 8, mnmajor_desc(stage_q(it), kk), IDESC_OD, (it > 0 || kk > 0));
             commit(L::B_Q_EMPTY + it % QS);  // Q_i's last reader
             if (it + 1 < n) {
-                if constexpr (L::SPLIT) {
-                    if (!(ok = wait_bar_warp(bar(L::B_DO_FULL + (it + 1) % DS), ((it + 1) / DS) & 1, ctl, SITE_BWD_MMA))) break;
-                    ptx::tc_fence_after();
-                }
+                if (!(ok = wait_bar_warp(bar(L::B_DO_FULL + (it + 1) % DS), ((it + 1) / DS) & 1, ctl, SITE_BWD_MMA))) break;
+                ptx::tc_fence_after();
                 issue_dp(it + 1);
                 commit(L::B_DP_FULL);
             }
@@ -512,10 +501,8 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
             ptx::mbar_arrive(bar(L::B_DS_FULL));
-            if constexpr (L::SPLIT) {
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(bar(L::B_DO_EMPTY + it % DS));  // done with delta
-            }
+            __syncwarp();
+            if (lane == 0) ptx::mbar_arrive(bar(L::B_DO_EMPTY + it % DS));  // done with delta
         }
         // Epilogue: dV and scale * dK for this thread's key row.
         const size_t row_off = (static_cast<size_t>(bh) * p.nk + kr) * D * 2;
