@@ -196,6 +196,27 @@ def pin_row_shift_invariance(orc):
                f"online shift {mag}")
 
 
+def pin_negative_scale_is_negated_keys(orc):
+    """A negative scale weights the most negative scores most: attention with -scale equals
+    attention with K negated and +scale, exactly (the scores are the same numbers), causal or
+    not, with the LSE too; and the weights still form a distribution."""
+    rng = _rng(29)
+    nq, nk, d = 7, 13, 5
+    q, k, v = rng.standard_normal((nq, d)) * 2, rng.standard_normal((nk, d)) * 2, rng.standard_normal((nk, d))
+    for causal in (False, True):
+        o_neg, l_neg = orc.attention(q, k, v, -0.7, causal, with_lse=True)
+        o_ref, l_ref = orc.attention(q, -k, v, 0.7, causal, with_lse=True)
+        _close(o_neg, o_ref, 1e-14, 1e-15, f"negative scale causal={causal}")
+        _close(l_neg, l_ref, 1e-14, 1e-15, f"negative scale LSE causal={causal}")
+        p = orc.softmax(q, k, -0.7, causal)
+        _close(p.sum(1), np.ones(nq), 1e-14, 0, f"negative scale rows causal={causal}")
+        # The weight goes to the key with the most negative score q . k (row 0, non-causal).
+        if not causal:
+            s0 = q[0] @ k.T
+            if int(np.argmax(p[0])) != int(np.argmin(s0)):
+                raise AssertionError("largest weight is not on the most negative score")
+
+
 def pin_softmax_rows_are_distributions(orc):
     rng = _rng(16)
     q, k = rng.standard_normal((10, 5)) * 2, rng.standard_normal((12, 5)) * 2
