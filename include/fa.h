@@ -198,7 +198,7 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
  * Q, K, V, O are host pointers with the layout above (pinned memory gives full copy speed and
  * lets copies overlap the computation). The call copies Q, K, V to device memory owned by
  * libfa, computes, copies O back and returns when O is complete. The (batch, head) slices are
- * processed in up to 8 chunks on three libfa-owned streams, ordered after the work already on
+ * processed in up to 6 chunks on three libfa-owned streams, ordered after the work already on
  * `stream`: while one chunk computes, the next is copied in and the previous copied out. Each
  * chunk is one attention launch (no key split). The device staging buffers grow to the
  * largest request seen and are kept until process exit (or fa_release_host_buffers); the

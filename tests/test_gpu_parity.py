@@ -260,7 +260,7 @@ def test_rescale_threshold_setter_validates(fa):
 
 def test_host_buffer_pipeline_uneven_chunks(fa):
     """The host entry copies and computes in chunks of slices on several streams: 37 slices make
-    chunks of 5 and a last one of 2. The result equals the device entry's bit for bit."""
+    chunks of 7 and a last one of 2. The result equals the device entry's bit for bit."""
     w = inputs.Workload("host_chunks", 1, 37, 300, 500, 64, "f16", True, seed=13)
     bits = inputs.draw(w)
     dev = inputs.from_torch(run_gpu(fa, bits, w))

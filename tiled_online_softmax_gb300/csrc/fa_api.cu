@@ -891,7 +891,8 @@ fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int6
     // engines of the two directions and the SMs work in parallel). Chunks go round-robin over
     // three streams; each stream copies in, computes and copies out its chunks in order.
     const int64_t bh = B * H;
-    const int64_t chunks = bh < 8 ? bh : 8;
+    // Six chunks measured best on the headline shape (8: 5 % slower, 16: 10 % slower, 4: 2 %).
+    const int64_t chunks = bh < 6 ? bh : 6;
     const int64_t per = (bh + chunks - 1) / chunks;
     const size_t q_slice = size_t(Nq) * size_t(D) * 2, kv_slice = size_t(Nk) * size_t(D) * 2;
     auto* hq = static_cast<const uint8_t*>(Q);
