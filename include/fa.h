@@ -82,19 +82,23 @@ typedef enum fa_status {
  * (kept until process exit); make that first call outside any stream capture.
  *
  * Work balancing (non-causal), by splitting 256-row work units over keys and merging them as in
- * fa_fwd_splitkv (two launches):
- *   - at most 76 units (half of the 152 SMs): each unit is split into floor(152 / units) key
- *     ranges of at least 2 key tiles (256 keys), so that one wave covers nearly all SMs;
- *   - more than 152 units whose last wave fills at most half of the SMs: the units of that
- *     wave are split into 2-4 ranges.
+ * fa_fwd_splitkv (two launches), on a device with S streaming multiprocessors (read from the
+ * device: 152 on a GB300):
+ *   - at most S/2 units: each unit is split into floor(S / units) key ranges of at least 2 key
+ *     tiles (256 keys), so that one wave covers nearly all SMs;
+ *   - more than S units whose last wave fills at most half of the SMs: the units of that wave
+ *     are split into 2-4 ranges.
  * Shapes with fewer than 4 key tiles (Nk <= 384), and causal launches, always run as one
- * launch.
- * The partial states live in a device workspace owned by libfa:
- * allocated the first time a shape needs it, grown when a later shape needs more, kept until
- * process exit. Calls that might grow it must not run under stream capture; all calls on one
- * device share it, so fa_fwd calls on different streams must be ordered. fa_set_tail_split(0)
- * turns the balancing off (one launch, no workspace). Split units' rows differ from the single
- * launch's only by rounding.
+ * launch; fa_fwd_plan reports what a shape gets. The split units times their ranges never exceed
+ * S CTAs, so their partial states fit a fixed-size workspace. libfa keeps a pool of 4 such
+ * workspaces per device (about 20 MB each on 152 SMs), allocated together by the first call that
+ * splits and kept until process exit; no call allocates, grows or frees it afterwards. A call
+ * uses the workspace its stream used last, else one whose previous user has finished on the GPU,
+ * and records an event on `stream` after its merge: calls on different streams never share
+ * partial states, with no ordering required between them. A call runs as one unsplit launch
+ * instead (no workspace; rows differ only by rounding) when its stream is being captured into a
+ * CUDA graph, or when all 4 workspaces are still in use by other streams' unfinished calls.
+ * fa_set_tail_split(0) turns the balancing off (always one launch).
  */
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H,
                  int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, fa_dtype dtype,
@@ -112,6 +116,27 @@ fa_status fa_fwd_lse(const void* Q, const void* K, const void* V, void* O, float
                      fa_dtype dtype, void* stream);
 
 /*
+ * fa_fwd_plan -- how fa_fwd and fa_fwd_lse divide a shape into launches (host only, no GPU work).
+ *   num_sms  the SM count to plan for; 0 = the current device's (FA_ERR_UNSUPPORTED without an
+ *            sm_103 device).
+ * Sizes, D and causal are checked as in fa_fwd (no pointers). The plan follows the balancing rules
+ * above and the fa_set_tail_split setting; it does not model the run-time fall-backs to one launch
+ * (stream capture, every workspace busy).
+ */
+typedef struct fa_plan {
+    int64_t units;           /* 256-row work units: B * H * ceil(Nq / 256) */
+    int64_t split_begin;     /* first unit split over keys (== units when none is) */
+    int64_t split_units;     /* units split over keys (0: one launch) */
+    int num_splits;          /* key ranges of each split unit (1 when none) */
+    int tiles_per_split;     /* 128-key tiles per range (all key tiles when none) */
+    int64_t ctas;            /* thread blocks of the attention launch */
+    int launches;            /* 1: attention only; 2: attention, then the merge */
+    size_t workspace_bytes;  /* partial state the split writes (0 when none) */
+} fa_plan;
+fa_status fa_fwd_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal,
+                      int num_sms, fa_plan* out);
+
+/*
  * Split over keys (flash-decoding), non-causal only.
  *
  * With few query rows (decoding, short chunks against a long context) one CTA per 256 query
@@ -122,7 +147,8 @@ fa_status fa_fwd_lse(const void* Q, const void* K, const void* V, void* O, float
  * "11. Fusion, recompute, and flash attention", section 11.6, last paragraph, and exercise
  * "Flash-decoding") and writes O = o / l (and LSE when non-null).
  *
- *   num_splits  requested number of key ranges per slice; 0 picks one that covers the SMs.
+ *   num_splits  requested number of key ranges per slice; 0 picks one that covers the current
+ *               device's SMs (152 when there is no sm_103 device, for a size query).
  *               The effective count is at most ceil(Nk / 128), every range holds whole tiles
  *               of 128 keys, and 1 runs fa_fwd itself (no workspace needed).
  *   workspace   caller-owned device memory, 256-byte aligned, at least
@@ -151,12 +177,16 @@ fa_status fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, f
  * one rounding to `dtype`. Y may equal X (in place); otherwise they must not overlap. All
  * pointers are device pointers, 16-byte aligned; D a multiple of 16 (at most 512).
  *
- * fa_fwd_rope runs attention on the rotated Q and K: it rotates Q (tables cos_q/sin_q [Nq][D/2])
- * and K (cos_k/sin_k [Nk][D/2]) into `workspace` (caller-owned device memory, 256-byte aligned,
- * at least fa_rope_workspace_bytes(B, H, Nq, Nk, D) bytes) and then computes fa_fwd_lse on
- * them (LSE may be NULL). Q and K themselves are left unchanged. The rotation is a separate
- * memory-bound pass in front of the attention kernel: K is read by every query block of its
- * slice, so rotating it once is cheaper than rotating it inside each thread block.
+ * fa_fwd_rope runs attention on the rotated Q and K (tables cos_q/sin_q [Nq][D/2] for Q and
+ * cos_k/sin_k [Nk][D/2] for K, 16-byte aligned) and writes O (and LSE when non-null, as in
+ * fa_fwd_lse); Q and K themselves are left unchanged. K is rotated first, by the fa_rope pass,
+ * into `workspace` (caller-owned device memory, 256-byte aligned, at least
+ * fa_rope_workspace_bytes(B, H, Nq, Nk, D) bytes = the size of K): every query block of a slice
+ * reads all of K, so rotating it once is cheaper than rotating it in each thread block. Q is
+ * rotated inside the attention kernel: each 128-row tile right after its load into shared
+ * memory, before its first product, by the same fp32 arithmetic as fa_rope (so the result equals
+ * fa_rope on Q and K followed by fa_fwd_lse, bit for bit, whenever both run the same launches).
+ * Two launches (three when the attention's work balancing splits the shape over keys).
  */
 fa_status fa_rope(const void* X, void* Y, const float* cos_t, const float* sin_t, int64_t B,
                   int64_t H, int64_t N, int64_t D, int form, fa_dtype dtype, void* stream);
@@ -230,10 +260,13 @@ fa_status fa_release_host_buffers(void);
  * D, so no valid problem reaches that limit today).
  *
  * Arguments, layouts, ownership and validation are those of fa_fwd (device pointers, async
- * on `stream`). Each call clears the record with cudaMemsetAsync on `stream` before its launch.
- * All calls share the one array and it keeps the last call's contents, so calls that overlap on
- * the GPU (different streams with no ordering between them) race on it. The record is not read
- * back by any entry point; a timeout there means the output of that call is incomplete.
+ * on `stream`), except that the whole computation is always one launch (no key split, which
+ * would need a workspace). Each call clears the record with cudaMemsetAsync on `stream` before
+ * its launch. All calls share the one array and it keeps the last call's contents, so calls that
+ * overlap on the GPU (different streams with no ordering between them) race on it.
+ * fa_last_device_error also reads and clears this record: after a call, it returns
+ * FA_ERR_TIMEOUT if one of that call's bounded waits ran out (the output is then incomplete).
+ * fa_wait_selftest_noalloc makes a wait run out on purpose with this record as its target.
  *
  * The first call on each device, with that device current, looks up the array's device address
  * (cudaGetSymbolAddress) and sets the kernel's shared-memory limit; make that first call before
@@ -243,12 +276,16 @@ fa_status fa_release_host_buffers(void);
 fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, int64_t B,
                          int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,
                          fa_dtype dtype, void* stream);
+/* fa_wait_selftest (below) aimed at fa_fwd_noalloc's static record; allocates nothing. */
+fa_status fa_wait_selftest_noalloc(unsigned long long timeout_ns, void* stream);
 
 /*
  * fa_last_device_error -- synchronise `stream`, then read and clear the current device's
- * kernel error word. Returns FA_ERR_TIMEOUT if a kernel launched by libfa on this device gave
- * up a bounded wait since the last check (its output is then incomplete), FA_ERR_CUDA if the
- * synchronisation failed, FA_OK otherwise. `site` (may be NULL) receives the wait site code.
+ * kernel error words: the one every entry point but fa_fwd_noalloc reports into, and
+ * fa_fwd_noalloc's static record. Returns FA_ERR_TIMEOUT if a kernel launched by libfa on this
+ * device gave up a bounded wait since the last check (its output is then incomplete), FA_ERR_CUDA
+ * if the synchronisation failed, FA_OK otherwise. `site` (may be NULL) receives the wait site
+ * code. Allocates nothing.
  */
 fa_status fa_last_device_error(void* stream, int* site);
 
@@ -302,6 +339,27 @@ typedef enum {
 fa_status fa_timer_start(void);
 fa_status fa_timer_stop(void);
 fa_status fa_timer_read(fa_kernel_kind kind, double* total_ms, int* launches);
+
+/*
+ * Checked build. libfa_debug.so is libfa built with FA_DEBUG_BOUNDS: every kernel checks the
+ * index of each global store against the extent of the tensor it writes, and a store that would
+ * leave it is skipped and recorded (site code 40-47 by kernel, and the offending element or row
+ * index) instead of being made. It exports the same functions and gives the same results; the
+ * release build compiles the checks away.
+ *
+ * fa_debug_bounds_enabled   1 in the checked build, 0 in the release build.
+ * fa_debug_bounds_report    read and clear the first violation recorded since the last report
+ *                           (*site 0: none). Call once the work has finished (after synchronising
+ *                           the streams that ran it). The release build always reports none.
+ * fa_debug_bounds_selftest  checked build only (else FA_ERR_UNSUPPORTED): two stores into `buf`
+ *                           (device memory of at least 64 ints, 4-byte aligned), at indices 8 and
+ *                           40, both checked against a stated bound of 32. The first is made; the
+ *                           second is recorded (site 49, index 40) and skipped. Asynchronous on
+ *                           `stream`. The pages have no counterpart: this tests the checks.
+ */
+int fa_debug_bounds_enabled(void);
+fa_status fa_debug_bounds_report(int* site, long long* index);
+fa_status fa_debug_bounds_selftest(int* buf, void* stream);
 
 /* A static, human-readable name for a status code. */
 const char* fa_status_string(fa_status status);

@@ -1,23 +1,38 @@
 """Comparison of kernel output with the fp64 oracle, element by element.
 
 Tolerance (the attention forward's stated bar): max |err| <= 1e-2 and mean |err| <= 1e-3 against
-the exact result, for fp32 accumulation with fp16/bf16 inputs and output. Rounding the exact
-result to the 16-bit output type already costs up to half an ulp of |O|; on inputs where |O|
-exceeds 2 (the large-magnitude workload, Q and K ~ N(0, 9)), half a bf16 ulp is 0.0156 > 1e-2,
-so no 16-bit output can meet the literal bound there. Likewise, on tiny problems (a row or two,
-few keys) |O| is about 1 and bf16 output rounding alone averages about 1e-3. The relaxed
-reading therefore charges the kernel only for error beyond the unavoidable output rounding:
-elementwise |err| <= 1e-2 + ulp(O_ref)/2 and mean |err| <= 1e-3 + mean |round(O_ref) - O_ref|.
-The literal bound is asserted on every named N(0,1) workload; the relaxed one on the
-large-magnitude workload and on the small edge-shape cases. The report always gives the literal
-max and mean and the rounding floor.
+the exact result, for fp32 accumulation with fp16/bf16 inputs and output.
+
+Two readings of that bar, both against the exact (unrounded) oracle result O_ref:
+
+* max |err|.  "literal": every element within 1e-2. "rounding": every element within
+  1e-2 + ulp(O_ref)/2. Rounding the exact result to the 16-bit output type already costs up to
+  half an ulp; on the large-magnitude workload (Q and K ~ N(0, 9)) |O| reaches 4 and more, where
+  half a bf16 ulp is 0.0156 > 1e-2, so no 16-bit output meets the literal max there.
+* mean |err|.  "literal": at most 1e-3. "floor": at most 1e-3 + mean |round(O_ref) - O_ref|, the
+  mean cost of rounding the exact result itself. The floor reading is allowed only where that
+  mean rounding floor exceeds MEAN_FLOOR_RELAX = 5e-4: tiny problems (a handful of keys), whose
+  |O| is near 1 and whose bf16 rounding alone averages 1e-3 to 2e-3. Below that threshold the
+  kernel's own rounding (16-bit P, fp32 sums) adds too little to carry a correct result past
+  1e-3, so the literal mean is asserted. "auto" picks "floor" exactly when the threshold is
+  exceeded.
+
+Every named N(0, 1) workload is held to the literal max and mean; the large-magnitude workload to
+the rounding max and the literal mean; edge shapes to the rounding max and the auto mean.
+
+Set FA_PARITY_REPORT to a file path to append one JSON line per comparison (name, shape, rows,
+literal max and mean, rounding floor, the readings asserted).
 """
+import json
+import os
+
 import numpy as np
 
 from tiled_online_softmax_gb300 import inputs
 
 MAX_ERR = 1e-2
 MEAN_ERR = 1e-3
+MEAN_FLOOR_RELAX = 5e-4
 MANTISSA_BITS = {"f16": 10, "bf16": 7}
 
 
@@ -39,13 +54,67 @@ def compare(out_bits: np.ndarray, ref: np.ndarray, dtype: str) -> dict:
     )
 
 
-def assert_parity(stats: dict, literal: bool = True, what: str = "") -> None:
+def merge(parts: list) -> dict:
+    """Statistics of the union of disjoint comparisons (element-weighted means)."""
+    n = sum(p["n"] for p in parts)
+    return dict(
+        max_err=max(p["max_err"] for p in parts),
+        mean_err=sum(p["mean_err"] * p["n"] for p in parts) / n,
+        rounding_floor=max(p["rounding_floor"] for p in parts),
+        mean_floor=sum(p["mean_floor"] * p["n"] for p in parts) / n,
+        n=n, finite=all(p["finite"] for p in parts),
+        worst_excess=max(p["worst_excess"] for p in parts),
+    )
+
+
+def mean_bound(stats: dict, mean: str) -> float:
+    if mean == "literal":
+        return MEAN_ERR
+    if mean == "auto":
+        mean = "floor" if stats["mean_floor"] > MEAN_FLOOR_RELAX else "literal"
+        return mean_bound(stats, mean)
+    if mean == "floor":
+        assert stats["mean_floor"] > MEAN_FLOOR_RELAX, (
+            f"the floor reading of the mean is only for rounding floors above {MEAN_FLOOR_RELAX}")
+        return MEAN_ERR + stats["mean_floor"]
+    raise ValueError(mean)
+
+
+def assert_parity(stats: dict, literal: bool = True, what: str = "", mean: str | None = None) -> None:
+    """literal: the max reading ("literal" if True, "rounding" if False). mean: "literal",
+    "floor" or "auto"; default "literal" with the literal max, "auto" with the rounding max."""
+    if mean is None:
+        mean = "literal" if literal else "auto"
+    mb = mean_bound(stats, mean)
+    _report(what, stats, literal, mean, mb)
     assert stats["finite"], f"{what}: non-finite output"
-    mean_bound = MEAN_ERR if literal else MEAN_ERR + stats["mean_floor"]
-    assert stats["mean_err"] <= mean_bound, f"{what}: mean |err| {stats['mean_err']:.3g} > {mean_bound:.3g}"
+    assert stats["mean_err"] <= mb, f"{what}: mean |err| {stats['mean_err']:.3g} > {mb:.3g}"
     if literal:
         assert stats["max_err"] <= MAX_ERR, f"{what}: max |err| {stats['max_err']:.3g} > {MAX_ERR}"
     else:
         assert stats["worst_excess"] <= 0, (
             f"{what}: max |err| {stats['max_err']:.3g} exceeds 1e-2 + ulp/2 "
             f"(rounding floor {stats['rounding_floor']:.3g})")
+
+
+_context: dict = {}
+
+
+def describe(w) -> None:
+    """Shape of the workload the next reported comparisons belong to."""
+    _context.clear()
+    _context.update(shape=f"B={w.B} H={w.H} Nq={w.Nq} Nk={w.Nk} D={w.D} {w.dtype}"
+                          f"{' causal' if w.causal else ''}", D=w.D)
+
+
+def _report(what, stats, literal, mean, mb) -> None:
+    path = os.environ.get("FA_PARITY_REPORT")
+    if not path:
+        return
+    rec = dict(what=what, **_context, rows=stats["n"] // _context.get("D", 1) if _context else None,
+               elements=stats["n"], max_err=stats["max_err"], mean_err=stats["mean_err"],
+               rounding_floor=stats["rounding_floor"], mean_floor=stats["mean_floor"],
+               max_reading="literal" if literal else "rounding", mean_reading=mean,
+               mean_bound=mb, worst_excess=stats["worst_excess"])
+    with open(path, "a") as f:
+        f.write(json.dumps(rec) + "\n")

@@ -52,7 +52,11 @@ def test_lse_matches_oracle(fa, w):
     # The LSE path writes the same O as fa_fwd.
     assert torch.equal(o.view(torch.int16), o_plain.view(torch.int16))
     stats = parity.compare(inputs.from_torch(o), ref_o, w.dtype)
-    parity.assert_parity(stats, w.name in ("single_head", "ragged", "causal_prefill"), w.name)
+    parity.describe(w)
+    if w.sigma_q == 1.0:
+        parity.assert_parity(stats, True, w.name)
+    else:  # the large-magnitude distribution: max beyond output rounding, literal mean
+        parity.assert_parity(stats, False, w.name, mean="literal")
 
 
 def test_lse_rejects_bad_pointer(fa):

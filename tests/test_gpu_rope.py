@@ -71,3 +71,40 @@ def test_attention_on_rotated_inputs(fa, form):
                                     w.scale, True, with_lse=True)
     parity.assert_parity(parity.compare(inputs.from_torch(o), ref, "bf16"), False, "rope attention")
     assert np.max(np.abs(lse.cpu().numpy() - ref_lse)) <= 4e-3
+
+
+@pytest.mark.parametrize("w,form", [
+    (inputs.Workload("rope_fused_causal", 1, 4, 300, 300, 128, "bf16", True, seed=81), 0),
+    (inputs.Workload("rope_fused_split", 1, 2, 200, 3000, 128, "bf16", False, seed=82), 1),
+    (inputs.Workload("rope_fused_d64_f16", 2, 3, 257, 1000, 64, "f16", False, seed=83), 0),
+    (inputs.Workload("rope_fused_d64_pairs", 1, 5, 513, 513, 64, "bf16", True, seed=84), 1),
+], ids=lambda x: getattr(x, "name", str(x)))
+def test_fused_q_rotation_equals_the_two_pass_form(fa, w, form):
+    """fa_fwd_rope rotates Q inside the attention kernel (in shared memory, after each tile's
+    load) and K in a pass of its own. The result equals rotating both with fa_rope and then
+    running the attention, bit for bit (same fp32 rotation, same launches), for both pair forms,
+    both head dims and dtypes, causal or split over keys, with ragged query tiles; and it matches
+    the oracle on the rotated inputs."""
+    bits = inputs.draw(w)
+    c, s = tables(max(w.Nq, w.Nk), w.D, offset=3)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    cq, sq = torch.from_numpy(c[:w.Nq]).cuda(), torch.from_numpy(s[:w.Nq]).cuda()
+    ck, sk = torch.from_numpy(c[:w.Nk]).cuda(), torch.from_numpy(s[:w.Nk]).cuda()
+    lse = torch.empty(w.B, w.H, w.Nq, dtype=torch.float32, device="cuda")
+    fused = fa.forward_rope(q, k, v, cq, sq, ck, sk, form=form, causal=w.causal, scale=w.scale,
+                            lse=lse)
+    qr, kr = fa.rope(q, cq, sq, form=form), fa.rope(k, ck, sk, form=form)
+    lse2 = torch.empty_like(lse)
+    two_pass, _ = fa.forward_lse(qr, kr, v, causal=w.causal, scale=w.scale, lse=lse2)
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == (0, 0)
+    assert torch.equal(fused.view(torch.int16), two_pass.view(torch.int16))
+    assert torch.equal(lse, lse2)
+    rot = {n: inputs.bits_to_f64(inputs.round_to_bits(
+        oracle.rope(inputs.bits_to_f64(bits[n], w.dtype), c[:getattr(w, "N" + n)].astype(np.float64),
+                    s[:getattr(w, "N" + n)].astype(np.float64), form).astype(np.float32), w.dtype),
+        w.dtype) for n in "qk"}
+    ref = oracle.attention(rot["q"], rot["k"], inputs.bits_to_f64(bits["v"], w.dtype), w.scale,
+                           w.causal)
+    parity.describe(w)
+    parity.assert_parity(parity.compare(inputs.from_torch(fused), ref, w.dtype), False, w.name)

@@ -1,4 +1,5 @@
-"""Build libfa.so (the sm_103a attention kernels and their C interface) in place with nvcc."""
+"""Build libfa.so (the sm_103a attention kernels and their C interface) in place with nvcc, and
+libfa_debug.so, the same library with every global store bounds-checked (FA_DEBUG_BOUNDS)."""
 from __future__ import annotations
 
 import os
@@ -11,6 +12,7 @@ PKG = Path(__file__).resolve().parent
 ROOT = PKG.parent
 CSRC = PKG / "csrc"
 LIB = PKG / "libfa.so"
+DEBUG_LIB = PKG / "libfa_debug.so"
 SOURCES = [CSRC / "fa_api.cu"]
 
 NVCC_FLAGS = [
@@ -30,18 +32,28 @@ def nvcc() -> str:
 
 
 def build(verbose: bool = False) -> Path:
-    """Compile every CUDA source into libfa.so next to this file; return its path."""
-    tmp = LIB.with_suffix(".so.tmp")
-    cmd = [nvcc(), *NVCC_FLAGS, "-o", str(tmp), *map(str, SOURCES)]
-    r = subprocess.run(cmd, capture_output=True, text=True)
-    log = r.stdout + r.stderr
-    (PKG / "build.log").write_text(" ".join(cmd) + "\n" + log)
-    if r.returncode != 0:
-        sys.stderr.write(log)
-        raise RuntimeError(f"nvcc failed ({r.returncode}); see {PKG / 'build.log'}")
-    if verbose:
-        sys.stderr.write(log)
-    tmp.replace(LIB)
+    """Compile every CUDA source into libfa.so and libfa_debug.so next to this file (two nvcc
+    processes in parallel); return the path of libfa.so."""
+    jobs = [(LIB, [], PKG / "build.log"), (DEBUG_LIB, ["-DFA_DEBUG_BOUNDS"], PKG / "build_debug.log")]
+    procs = []
+    for out, extra, log in jobs:
+        tmp = out.with_suffix(".so.tmp")
+        cmd = [nvcc(), *NVCC_FLAGS, *extra, "-o", str(tmp), *map(str, SOURCES)]
+        procs.append((out, tmp, log, cmd, subprocess.Popen(cmd, stdout=subprocess.PIPE,
+                                                            stderr=subprocess.PIPE, text=True)))
+    failed = []
+    for out, tmp, log, cmd, proc in procs:
+        stdout, stderr = proc.communicate()
+        log.write_text(" ".join(cmd) + "\n" + stdout + stderr)
+        if proc.returncode != 0:
+            sys.stderr.write(stdout + stderr)
+            failed.append(f"{out.name}: nvcc failed ({proc.returncode}); see {log}")
+            continue
+        if verbose:
+            sys.stderr.write(stdout + stderr)
+        tmp.replace(out)
+    if failed:
+        raise RuntimeError("; ".join(failed))
     return LIB
 
 

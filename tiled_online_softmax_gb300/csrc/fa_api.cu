@@ -21,7 +21,6 @@
 namespace {
 
 constexpr int MAX_DEVICES = 64;
-constexpr int64_t NUM_SMS = 152;  // GB300
 
 thread_local char g_msg[512] = "";
 
@@ -75,9 +74,6 @@ void timer_end(cudaStream_t s, int i) {
     if (i >= 0) cudaEventRecord(g_timer.ev[2 * i + 1], s);
 }
 
-std::mutex g_mutex;
-int* g_err_word[MAX_DEVICES] = {};         // device error word per device (16 bytes)
-int g_arch_ok[MAX_DEVICES] = {};           // 0 unknown, 1 sm_103, -1 other
 unsigned g_attr_set[MAX_DEVICES] = {};     // bit per kernel instance: smem attribute applied
 float g_rescale_threshold = 32.0f;         // lazy-rescale threshold (log2 units)
 // fp16 weights P <= 2^threshold must stay below the fp16 maximum (65504 < 2^16); bf16 has
@@ -152,8 +148,8 @@ fa_status validate(const void* Q, const void* K, const void* V, void* O, int64_t
     return FA_OK;
 }
 
-fa_status encode_map(CUtensorMap* map, const void* base, int64_t bh, int64_t n, int64_t D,
-                     int dtype) {
+fa_status encode_map_uncached(CUtensorMap* map, const void* base, int64_t bh, int64_t n,
+                              int64_t D, int dtype) {
     auto fn = encode_fn();
     if (!fn) return fail(FA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const cuuint64_t dims[3] = {cuuint64_t(D), cuuint64_t(n), cuuint64_t(bh)};
@@ -170,24 +166,85 @@ fa_status encode_map(CUtensorMap* map, const void* base, int64_t bh, int64_t n, 
     return FA_OK;
 }
 
-// Per-device state: architecture check and the error word. Called with no lock held.
-fa_status device_state(int* dev_out, int** err_out) {
+// Tensor maps of recent calls. A map is a pure function of (base address, slice count, rows,
+// D, dtype), so a cached map stays valid whatever happened to the memory since; the cache only
+// saves re-encoding for callers that reuse their buffers. Round-robin replacement.
+struct MapCache {
+    static constexpr int ENTRIES = 64;
+    struct Entry {
+        const void* base;
+        int64_t bh, n, D;
+        int dtype;
+        bool valid;
+        CUtensorMap map;
+    };
+    std::mutex mu;
+    Entry e[ENTRIES] = {};
+    int next = 0;
+};
+MapCache g_maps;
+
+fa_status encode_map(CUtensorMap* map, const void* base, int64_t bh, int64_t n, int64_t D,
+                     int dtype) {
+    {
+        std::lock_guard<std::mutex> lock(g_maps.mu);
+        for (const auto& x : g_maps.e)
+            if (x.valid && x.base == base && x.bh == bh && x.n == n && x.D == D && x.dtype == dtype) {
+                *map = x.map;
+                return FA_OK;
+            }
+    }
+    fa_status s = encode_map_uncached(map, base, bh, n, D, dtype);
+    if (s != FA_OK) return s;
+    std::lock_guard<std::mutex> lock(g_maps.mu);
+    auto& x = g_maps.e[g_maps.next];
+    g_maps.next = (g_maps.next + 1) % MapCache::ENTRIES;
+    x.base = base;
+    x.bh = bh;
+    x.n = n;
+    x.D = D;
+    x.dtype = dtype;
+    x.map = *map;
+    x.valid = true;
+    return FA_OK;
+}
+
+std::mutex g_mutex;
+int* g_err_word[MAX_DEVICES] = {};         // device error word per device (16 bytes)
+int g_arch_ok[MAX_DEVICES] = {};           // 0 unknown, 1 sm_103, -1 other
+int g_num_sms[MAX_DEVICES] = {};           // streaming multiprocessors of each device
+
+// The current device, checked to be an sm_103 GPU; its SM count is read once and cached.
+// Called with g_mutex held.
+fa_status arch_check_locked(int* dev_out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= MAX_DEVICES) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
-    std::lock_guard<std::mutex> lock(g_mutex);
     if (g_arch_ok[dev] == 0) {
-        int major = 0, minor = 0;
+        int major = 0, minor = 0, sms = 0;
         if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
+            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess ||
+            (e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
             return cuda_fail(e, "cudaDeviceGetAttribute");
+        g_num_sms[dev] = sms > 0 ? sms : 1;
         g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
     }
     if (g_arch_ok[dev] != 1)
         return fail(FA_ERR_UNSUPPORTED, "device %d is not an sm_103 GPU; libfa is built for sm_103a", dev);
+    *dev_out = dev;
+    return FA_OK;
+}
+
+// Per-device state: architecture check and the error word. Called with no lock held.
+fa_status device_state(int* dev_out, int** err_out) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int dev = 0;
+    fa_status s = arch_check_locked(&dev);
+    if (s != FA_OK) return s;
     if (!g_err_word[dev]) {
         int* w = nullptr;
+        cudaError_t e;
         if ((e = cudaMalloc(&w, 16)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(error word)");
         if ((e = cudaMemset(w, 0, 16)) != cudaSuccess) {
             cudaFree(w);
@@ -254,9 +311,16 @@ struct Split {
     float* ml_part = nullptr;
 };
 
+// Rotary embedding of Q applied inside the attention kernel (cos == nullptr: none).
+struct QRope {
+    const float* cos = nullptr;
+    const float* sin = nullptr;
+    int form = 0;
+};
+
 fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
                  int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, int dtype,
-                 cudaStream_t stream, const Split& split = Split()) {
+                 cudaStream_t stream, const Split& split = Split(), const QRope& rope = QRope()) {
     int dev = 0;
     int* err = nullptr;
     fa_status s = device_state(&dev, &err);
@@ -287,6 +351,9 @@ fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LS
     p.split_units = splitting ? split.split_units : 0;
     p.o_part = split.o_part;
     p.ml_part = split.ml_part;
+    p.rope_cos = rope.cos;
+    p.rope_sin = rope.sin;
+    p.rope_form = rope.form;
     const bool bf16 = dtype == FA_BF16;
     const int inst = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
     switch (inst) {
@@ -346,24 +413,14 @@ constexpr size_t NOALLOC_RECORD_BYTES = 16;  // what the kernel needs: one error
 int* g_noalloc_addr[MAX_DEVICES] = {};
 
 fa_status noalloc_device_state(int* dev_out, int** scratch_out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= MAX_DEVICES) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
     std::lock_guard<std::mutex> lock(g_mutex);
-    if (g_arch_ok[dev] == 0) {
-        int major = 0, minor = 0;
-        if ((e = cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev)) != cudaSuccess ||
-            (e = cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev)) != cudaSuccess)
-            return cuda_fail(e, "cudaDeviceGetAttribute");
-        g_arch_ok[dev] = (major == 10 && minor == 3) ? 1 : -1;
-    }
-    if (g_arch_ok[dev] != 1)
-        return fail(FA_ERR_UNSUPPORTED, "device %d is not an sm_103 GPU; libfa is built for sm_103a", dev);
+    int dev = 0;
+    fa_status s = arch_check_locked(&dev);
+    if (s != FA_OK) return s;
     if (!g_noalloc_addr[dev]) {
         void* addr = nullptr;
-        if ((e = cudaGetSymbolAddress(&addr, g_noalloc_scratch)) != cudaSuccess)
-            return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
+        cudaError_t e = cudaGetSymbolAddress(&addr, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(scratch)");
         g_noalloc_addr[dev] = static_cast<int*>(addr);
     }
     *dev_out = dev;
@@ -377,9 +434,10 @@ struct SplitPlan {
     int tiles_per_split;
 };
 
-SplitPlan plan_splits(int64_t units, int64_t Nk, int64_t want) {
+// `want` key ranges per unit (0: enough to cover `sms` SMs), clamped to [1, key tiles].
+SplitPlan plan_splits(int64_t units, int64_t Nk, int64_t want, int64_t sms) {
     const int64_t nkt = (Nk + fa::BN - 1) / fa::BN;
-    if (want <= 0) want = units >= NUM_SMS ? 1 : (NUM_SMS + units - 1) / units;  // cover the SMs
+    if (want <= 0) want = units >= sms ? 1 : (sms + units - 1) / units;  // cover the SMs
     want = want < 1 ? 1 : (want > nkt ? nkt : want);
     const int64_t per = (nkt + want - 1) / want;
     return SplitPlan{static_cast<int>((nkt + per - 1) / per), static_cast<int>(per)};
@@ -387,6 +445,15 @@ SplitPlan plan_splits(int64_t units, int64_t Nk, int64_t want) {
 
 int64_t units_of(int64_t B, int64_t H, int64_t Nq) {
     return B * H * ((Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS);
+}
+
+// SM count of the current device for host-side sizing queries; `fallback` when there is no
+// usable sm_103 device (such a query then describes a GPU with that many SMs).
+int64_t current_sms_or(int64_t fallback) {
+    std::lock_guard<std::mutex> lock(g_mutex);
+    int dev = 0;
+    if (arch_check_locked(&dev) != FA_OK) return fallback;
+    return g_num_sms[dev];
 }
 
 // Bytes of partial state for `split_units` units split `splits` ways.
@@ -402,7 +469,7 @@ size_t workspace_bytes(int64_t split_units, int64_t Nq, int64_t D, int splits) {
 fa_status launch_split(const void* Q, const void* K, const void* V, void* O, float* LSE,
                        int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale,
                        int dtype, cudaStream_t strm, const SplitPlan& plan, int64_t split_begin,
-                       int64_t split_units, void* workspace) {
+                       int64_t split_units, void* workspace, const QRope& rope = QRope()) {
     const int64_t split_rows = Nq < fa::UNIT_ROWS ? Nq : fa::UNIT_ROWS;
     const size_t rows = size_t(split_units) * size_t(split_rows);
     if (rows > size_t(INT32_MAX) / 32) return fail(FA_ERR_UNSUPPORTED, "too many rows to split");
@@ -415,11 +482,12 @@ fa_status launch_split(const void* Q, const void* K, const void* V, void* O, flo
     sp.ml_part = reinterpret_cast<float*>(
         static_cast<uint8_t*>(workspace) +
         ((size_t(plan.num_splits) * rows * size_t(D) * 4 + 255) & ~size_t(255)));
-    fa_status s = launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, 0, dtype, strm, sp);
+    fa_status s = launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, 0, dtype, strm, sp, rope);
     if (s != FA_OK) return s;
     const fa::MergeMap map{static_cast<int>(split_begin),
                            static_cast<int>((Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS),
-                           static_cast<int>(split_rows), static_cast<int>(Nq)};
+                           static_cast<int>(split_rows), static_cast<int>(Nq),
+                           static_cast<int>(B * H)};
     const unsigned blocks = static_cast<unsigned>((rows * 32 + 255) / 256);
     const int64_t nrows = static_cast<int64_t>(rows);
     const bool bf16 = dtype == FA_BF16;
@@ -457,74 +525,159 @@ fa_status launch_split(const void* Q, const void* K, const void* V, void* O, flo
 // products, epilogue: about five key steps) and a row of partial state to write and merge.
 constexpr int64_t MIN_SPLIT_TILES = 2;
 
-// Work balancing for fa_fwd / fa_fwd_lse (non-causal), by splitting units over keys:
-//  - fewer units than half the SMs: every unit is split into floor(SMs / units) key ranges of at
+// Work balancing for fa_fwd / fa_fwd_lse (non-causal) on a device with `sms` SMs, by splitting
+// units over keys:
+//  - fewer units than half the SMs: every unit is split into floor(sms / units) key ranges of at
 //    least MIN_SPLIT_TILES tiles, so that one wave covers (nearly) all SMs;
 //  - a partial last wave of at most half the SMs: its units are split into 2-4 ranges, so that
 //    the wave runs on (about) all SMs for a fraction of the time.
-// Returns false when nothing is worth splitting.
-bool plan_balance(int64_t units, int64_t Nk, SplitPlan* plan, int64_t* begin, int64_t* count) {
+// Either way the split units times their ranges number at most `sms` CTAs, which bounds the
+// partial state (balance_workspace_bytes). Returns false when nothing is worth splitting.
+bool plan_balance(int64_t units, int64_t Nk, int64_t sms, SplitPlan* plan, int64_t* begin,
+                  int64_t* count) {
     const int64_t nkt = (Nk + fa::BN - 1) / fa::BN;
-    if (units <= NUM_SMS / 2) {
-        int64_t want = NUM_SMS / units;
+    if (sms < 2) return false;
+    if (units <= sms / 2) {
+        int64_t want = sms / units;
         if (want > nkt / MIN_SPLIT_TILES) want = nkt / MIN_SPLIT_TILES;
         if (want < 2) return false;
-        *plan = plan_splits(units, Nk, want);
+        *plan = plan_splits(units, Nk, want, sms);
         if (plan->num_splits < 2) return false;
         *begin = 0;
         *count = units;
         return true;
     }
-    const int64_t tail = units % NUM_SMS;
-    if (units <= NUM_SMS || tail == 0 || tail > NUM_SMS / 2) return false;
-    int64_t want = NUM_SMS / tail;
+    const int64_t tail = units % sms;
+    if (units <= sms || tail == 0 || tail > sms / 2) return false;
+    int64_t want = sms / tail;
     if (want > 4) want = 4;
     if (nkt < 2 * want) return false;
-    *plan = plan_splits(tail, Nk, want);
+    *plan = plan_splits(tail, Nk, want, sms);
     if (plan->num_splits < 2) return false;
     *begin = units - tail;
     *count = tail;
     return true;
 }
 
-struct Workspace {
+// Largest partial state plan_balance can ask for on `sms` SMs: at most `sms` split CTAs, each
+// with at most 256 rows of D = 128 fp32 columns and an (m, l) pair.
+size_t balance_workspace_bytes(int64_t sms) {
+    const size_t rows = size_t(sms) * fa::UNIT_ROWS;
+    return ((rows * 128 * 4 + 255) & ~size_t(255)) + rows * 8;
+}
+
+// Workspaces of fa_fwd's key splits: per device, a pool of fixed-size slots allocated together on
+// the first split call and kept until process exit (never grown or freed by a call). A call
+// takes the slot its stream used last, else a slot never used, else a slot whose last use has
+// finished on the GPU (its event has completed); the slot's event is recorded after the call's
+// merge launch. A call that finds every slot in use by other streams' unfinished work, or whose
+// stream is being captured into a CUDA graph (a graph may be replayed at any time, concurrently
+// with anything), runs as one unsplit launch instead: correct, with no shared state.
+constexpr int WS_SLOTS = 4;
+struct WsSlot {
     void* buf = nullptr;
-    size_t bytes = 0;
+    cudaEvent_t done = nullptr;      // recorded after the last call's merge launch
+    unsigned long long last = 0;     // id of that call's stream (unique for the process lifetime)
+    bool used = false;               // `done` has been recorded at least once
+    bool claimed = false;            // a host thread is launching with this slot right now
 };
-Workspace g_workspace[MAX_DEVICES];
+struct WsPool {
+    bool ready = false;
+    bool failed = false;
+    size_t slot_bytes = 0;
+    void* base = nullptr;
+    WsSlot slot[WS_SLOTS];
+};
+WsPool g_ws_pool[MAX_DEVICES];
 bool g_tail_split = true;
 
-// The library's own workspace on the current device, grown to at least `bytes`.
-fa_status library_workspace(size_t bytes, void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    std::lock_guard<std::mutex> lock(g_mutex);
-    Workspace& w = g_workspace[dev];
-    if (w.bytes < bytes) {
-        if (w.buf) cudaFree(w.buf);
-        w = Workspace{};
-        if ((e = cudaMalloc(&w.buf, bytes)) != cudaSuccess) return cuda_fail(e, "cudaMalloc(workspace)");
-        w.bytes = bytes;
+// Set up the pool of device `dev` (g_mutex held). False if it cannot be (then no call splits).
+bool ws_pool_ready_locked(int dev) {
+    WsPool& pool = g_ws_pool[dev];
+    if (pool.ready) return true;
+    if (pool.failed) return false;
+    const size_t bytes = balance_workspace_bytes(g_num_sms[dev]);
+    void* base = nullptr;
+    if (cudaMalloc(&base, bytes * WS_SLOTS) != cudaSuccess) {
+        cudaGetLastError();
+        pool.failed = true;
+        return false;
     }
-    *out = w.buf;
-    return FA_OK;
+    for (int i = 0; i < WS_SLOTS; ++i) {
+        if (cudaEventCreateWithFlags(&pool.slot[i].done, cudaEventDisableTiming) != cudaSuccess) {
+            cudaGetLastError();
+            for (int j = 0; j < i; ++j) cudaEventDestroy(pool.slot[j].done);
+            cudaFree(base);
+            pool.failed = true;
+            return false;
+        }
+        pool.slot[i].buf = static_cast<uint8_t*>(base) + size_t(i) * bytes;
+    }
+    pool.base = base;
+    pool.slot_bytes = bytes;
+    pool.ready = true;
+    return true;
+}
+
+// Claim a slot for a split call on the stream with id `sid` (g_mutex held), or nullptr to run
+// unsplit. A slot last used by the same stream needs no wait: the stream orders the calls.
+WsSlot* ws_claim_locked(int dev, unsigned long long sid, size_t need) {
+    if (!ws_pool_ready_locked(dev)) return nullptr;
+    WsPool& pool = g_ws_pool[dev];
+    if (need > pool.slot_bytes) return nullptr;
+    WsSlot* pick = nullptr;
+    for (WsSlot& sl : pool.slot)
+        if (!pick && !sl.claimed && sl.used && sl.last == sid) pick = &sl;
+    for (WsSlot& sl : pool.slot)
+        if (!pick && !sl.claimed && !sl.used) pick = &sl;
+    for (WsSlot& sl : pool.slot) {
+        if (pick || sl.claimed) continue;
+        const cudaError_t q = cudaEventQuery(sl.done);
+        if (q == cudaSuccess) pick = &sl;
+        else if (q != cudaErrorNotReady) cudaGetLastError();
+    }
+    if (pick) pick->claimed = true;
+    return pick;
 }
 
 // fa_fwd / fa_fwd_lse: one launch, or some units split over keys and merged.
 fa_status forward(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
                   int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,
-                  int dtype, cudaStream_t strm) {
-    SplitPlan plan;
-    int64_t begin = 0, count = 0;
-    if (!causal && g_tail_split && plan_balance(units_of(B, H, Nq), Nk, &plan, &begin, &count)) {
-        void* ws = nullptr;
-        fa_status s = library_workspace(workspace_bytes(count, Nq, D, plan.num_splits), &ws);
+                  int dtype, cudaStream_t strm, const QRope& rope = QRope()) {
+    if (!causal && g_tail_split) {
+        int dev = 0;
+        int* err = nullptr;
+        fa_status s = device_state(&dev, &err);
         if (s != FA_OK) return s;
-        return launch_split(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, dtype, strm, plan, begin,
-                            count, ws);
+        cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+        cudaError_t e = cudaStreamIsCapturing(strm, &cap);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+        SplitPlan plan;
+        int64_t begin = 0, count = 0;
+        WsSlot* slot = nullptr;
+        unsigned long long sid = 0;
+        if (cap == cudaStreamCaptureStatusNone &&
+            plan_balance(units_of(B, H, Nq), Nk, g_num_sms[dev], &plan, &begin, &count)) {
+            if ((e = cudaStreamGetId(strm, &sid)) != cudaSuccess) return cuda_fail(e, "cudaStreamGetId");
+            std::lock_guard<std::mutex> lock(g_mutex);
+            slot = ws_claim_locked(dev, sid, workspace_bytes(count, Nq, D, plan.num_splits));
+        }
+        if (slot) {
+            s = launch_split(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, dtype, strm, plan, begin,
+                             count, slot->buf, rope);
+            std::lock_guard<std::mutex> lock(g_mutex);
+            slot->claimed = false;
+            // Recorded even after a failed launch: whatever was enqueued is covered by it.
+            if ((e = cudaEventRecord(slot->done, strm)) == cudaSuccess) {
+                slot->last = sid;
+                slot->used = true;
+            } else if (s == FA_OK) {
+                return cuda_fail(e, "cudaEventRecord(workspace)");
+            }
+            return s;
+        }
     }
-    return launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, causal, dtype, strm);
+    return launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, causal, dtype, strm, Split(), rope);
 }
 
 fa_status launch_rope(const void* X, void* Y, const float* cos_t, const float* sin_t,
@@ -532,7 +685,8 @@ fa_status launch_rope(const void* X, void* Y, const float* cos_t, const float* s
                       cudaStream_t strm) {
     const int64_t work = rows_total * (D / 16);
     int64_t blocks = (work + 255) / 256;
-    if (blocks > 152 * 16) blocks = 152 * 16;
+    const int64_t max_blocks = current_sms_or(152) * 16;  // 16 blocks of 256 threads per SM
+    if (blocks > max_blocks) blocks = max_blocks;
     if (blocks < 1) blocks = 1;
     auto x = static_cast<const uint16_t*>(X);
     auto y = static_cast<uint16_t*>(Y);
@@ -603,6 +757,14 @@ fa_status launch_bwd_instance(int dev, const CUtensorMap& mq, const CUtensorMap&
     timer_end(strm, ti);
     if (e != cudaSuccess) return cuda_fail(e, "backward dQ launch");
     return FA_OK;
+}
+
+// One block of two threads: thread 0 stores at index 8 of `buf` and thread 1 at index 40, both
+// checked against a stated bound of 32 elements. `buf` holds 64, so neither store can leave it;
+// in the checked build the second is recorded as a violation and skipped.
+__global__ void fa_bounds_selftest_kernel(int* buf) {
+    const long long idx = threadIdx.x == 0 ? 8 : 40;
+    if (fa::in_bounds(idx < 32, fa::BOUNDS_SELFTEST, idx)) buf[idx] = 1;
 }
 
 }  // namespace
@@ -688,7 +850,47 @@ size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, 
                                   int num_splits) {
     if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || D < 1) return 0;
     const int64_t units = units_of(B, H, Nq);
-    return workspace_bytes(units, Nq, D, plan_splits(units, Nk, num_splits).num_splits);
+    return workspace_bytes(units, Nq, D,
+                           plan_splits(units, Nk, num_splits, current_sms_or(152)).num_splits);
+}
+
+fa_status fa_fwd_plan(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, int causal,
+                      int num_sms, fa_plan* out) {
+    if (!out) return fail(FA_ERR_INVALID_ARGUMENT, "null plan pointer");
+    if (B < 1 || H < 1 || Nq < 1 || Nk < 1)
+        return fail(FA_ERR_INVALID_ARGUMENT, "sizes must be >= 1");
+    if (causal != 0 && causal != 1) return fail(FA_ERR_INVALID_ARGUMENT, "causal must be 0 or 1");
+    if (D != 64 && D != 128) return fail(FA_ERR_UNSUPPORTED, "head dimension %lld not supported", (long long)D);
+    if (num_sms < 0) return fail(FA_ERR_INVALID_ARGUMENT, "num_sms must be >= 0");
+    int64_t sms = num_sms;
+    if (sms == 0) {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        int dev = 0;
+        fa_status s = arch_check_locked(&dev);
+        if (s != FA_OK) return s;
+        sms = g_num_sms[dev];
+    }
+    const int64_t units = units_of(B, H, Nq);
+    fa_plan p{};
+    p.units = units;
+    p.split_begin = units;
+    p.num_splits = 1;
+    p.tiles_per_split = static_cast<int>((Nk + fa::BN - 1) / fa::BN);
+    p.ctas = units;
+    p.launches = 1;
+    SplitPlan plan;
+    int64_t begin = 0, count = 0;
+    if (!causal && g_tail_split && plan_balance(units, Nk, sms, &plan, &begin, &count)) {
+        p.split_begin = begin;
+        p.split_units = count;
+        p.num_splits = plan.num_splits;
+        p.tiles_per_split = plan.tiles_per_split;
+        p.ctas = begin + count * plan.num_splits;
+        p.launches = 2;
+        p.workspace_bytes = workspace_bytes(count, Nq, D, plan.num_splits);
+    }
+    *out = p;
+    return FA_OK;
 }
 
 fa_status fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, float* LSE,
@@ -700,7 +902,7 @@ fa_status fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, f
     if (LSE && reinterpret_cast<uintptr_t>(LSE) % 4 != 0)
         return fail(FA_ERR_MISALIGNED, "LSE pointer is not 4-byte aligned");
     const int64_t units = units_of(B, H, Nq);
-    const SplitPlan plan = plan_splits(units, Nk, num_splits);
+    const SplitPlan plan = plan_splits(units, Nk, num_splits, current_sms_or(152));
     auto strm = static_cast<cudaStream_t>(stream);
     if (plan.num_splits <= 1) return launch(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, 0, int(dtype), strm);
     const size_t need = workspace_bytes(units, Nq, D, plan.num_splits);
@@ -724,8 +926,7 @@ fa_status fa_rope(const void* X, void* Y, const float* cos_t, const float* sin_t
 
 size_t fa_rope_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D) {
     if (B < 1 || H < 1 || Nq < 1 || Nk < 1 || D < 1) return 0;
-    const size_t q = (size_t(B * H) * size_t(Nq) * size_t(D) * 2 + 255) & ~size_t(255);
-    return q + size_t(B * H) * size_t(Nk) * size_t(D) * 2;
+    return size_t(B * H) * size_t(Nk) * size_t(D) * 2;  // the rotated K
 }
 
 fa_status fa_fwd_rope(const void* Q, const void* K, const void* V, void* O, float* LSE,
@@ -743,17 +944,20 @@ fa_status fa_fwd_rope(const void* Q, const void* K, const void* V, void* O, floa
         return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
     if (LSE && reinterpret_cast<uintptr_t>(LSE) % 4 != 0)
         return fail(FA_ERR_MISALIGNED, "LSE pointer is not 4-byte aligned");
-    void* qr = workspace;
-    void* kr = static_cast<uint8_t*>(workspace) +
-               ((size_t(B * H) * size_t(Nq) * size_t(D) * 2 + 255) & ~size_t(255));
-    if ((s = validate_rope(Q, qr, cos_q, sin_q, B * H * Nq, Nq, D, rope_form, int(dtype))) != FA_OK ||
+    // K is rotated once by its own pass (every query block of a slice reads all of K); Q is
+    // rotated inside the attention kernel, in shared memory, right after each tile's load.
+    void* kr = workspace;
+    if ((s = validate_rope(Q, Q, cos_q, sin_q, B * H * Nq, Nq, D, rope_form, int(dtype))) != FA_OK ||
         (s = validate_rope(K, kr, cos_k, sin_k, B * H * Nk, Nk, D, rope_form, int(dtype))) != FA_OK)
         return s;
     auto strm = static_cast<cudaStream_t>(stream);
-    if ((s = launch_rope(Q, qr, cos_q, sin_q, B * H * Nq, Nq, D, rope_form, int(dtype), strm)) != FA_OK ||
-        (s = launch_rope(K, kr, cos_k, sin_k, B * H * Nk, Nk, D, rope_form, int(dtype), strm)) != FA_OK)
+    if ((s = launch_rope(K, kr, cos_k, sin_k, B * H * Nk, Nk, D, rope_form, int(dtype), strm)) != FA_OK)
         return s;
-    return forward(qr, kr, V, O, LSE, B, H, Nq, Nk, D, scale, causal, int(dtype), strm);
+    QRope rope;
+    rope.cos = cos_q;
+    rope.sin = sin_q;
+    rope.form = rope_form;
+    return forward(Q, kr, V, O, LSE, B, H, Nq, Nk, D, scale, causal, int(dtype), strm, rope);
 }
 
 size_t fa_bwd_workspace_bytes(int64_t B, int64_t H, int64_t Nq) {
@@ -900,9 +1104,15 @@ fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int6
     auto* hv = static_cast<const uint8_t*>(V);
     auto* ho = static_cast<uint8_t*>(O);
     if ((e = cudaEventRecord(hp->start, strm)) != cudaSuccess) return cuda_fail(e, "cudaEventRecord");
+    // After an error part-way through, copies and launches already queued on the pipeline
+    // streams would keep using the staging buffer and O: wait for them before returning.
+    auto drain = [&](fa_status st) {
+        for (int i = 0; i < HOST_PIPE_STREAMS; ++i) cudaStreamSynchronize(hp->s[i]);
+        return st;
+    };
     for (int i = 0; i < HOST_PIPE_STREAMS; ++i)
         if ((e = cudaStreamWaitEvent(hp->s[i], hp->start, 0)) != cudaSuccess)
-            return cuda_fail(e, "cudaStreamWaitEvent");
+            return drain(cuda_fail(e, "cudaStreamWaitEvent"));
     for (int64_t c0 = 0, c = 0; c0 < bh; c0 += per, ++c) {
         const int64_t n = (bh - c0 < per) ? bh - c0 : per;
         cudaStream_t x = hp->s[c % HOST_PIPE_STREAMS];
@@ -910,21 +1120,21 @@ fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int6
         if ((e = cudaMemcpyAsync(dq + qo, hq + qo, size_t(n) * q_slice, cudaMemcpyHostToDevice, x)) != cudaSuccess ||
             (e = cudaMemcpyAsync(dk + ko, hk + ko, size_t(n) * kv_slice, cudaMemcpyHostToDevice, x)) != cudaSuccess ||
             (e = cudaMemcpyAsync(dv + ko, hv + ko, size_t(n) * kv_slice, cudaMemcpyHostToDevice, x)) != cudaSuccess)
-            return cuda_fail(e, "cudaMemcpyAsync(host to device)");
-        // One launch per chunk, without the last-wave split (its workspace is shared, and the
-        // chunks run concurrently).
+            return drain(cuda_fail(e, "cudaMemcpyAsync(host to device)"));
+        // One launch per chunk, without the key split (the chunks run concurrently on three
+        // streams, each a whole-GPU-sized piece of work already).
         s = launch(dq + qo, dk + ko, dv + ko, dout + qo, nullptr, 1, n, Nq, Nk, D, scale, causal,
                    int(dtype), x);
-        if (s != FA_OK) return s;
+        if (s != FA_OK) return drain(s);
         if ((e = cudaMemcpyAsync(ho + qo, dout + qo, size_t(n) * q_slice, cudaMemcpyDeviceToHost, x)) != cudaSuccess)
-            return cuda_fail(e, "cudaMemcpyAsync(device to host)");
+            return drain(cuda_fail(e, "cudaMemcpyAsync(device to host)"));
     }
     for (int i = 0; i < HOST_PIPE_STREAMS; ++i) {
         if ((e = cudaEventRecord(hp->done[i], hp->s[i])) != cudaSuccess ||
             (e = cudaStreamWaitEvent(strm, hp->done[i], 0)) != cudaSuccess)
-            return cuda_fail(e, "host pipeline join");
+            return drain(cuda_fail(e, "host pipeline join"));
     }
-    if ((e = cudaStreamSynchronize(strm)) != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    if ((e = cudaStreamSynchronize(strm)) != cudaSuccess) return drain(cuda_fail(e, "cudaStreamSynchronize"));
     return FA_OK;
 }
 
@@ -998,22 +1208,77 @@ fa_status fa_wait_selftest(unsigned long long timeout_ns, void* stream) {
     return FA_OK;
 }
 
+fa_status fa_wait_selftest_noalloc(unsigned long long timeout_ns, void* stream) {
+    if (timeout_ns == 0 || timeout_ns > 1000000000ull)
+        return fail(FA_ERR_INVALID_ARGUMENT, "selftest timeout must be in (0, 1e9] ns");
+    int dev = 0;
+    int* scratch = nullptr;
+    fa_status st = noalloc_device_state(&dev, &scratch);
+    if (st != FA_OK) return st;
+    fa::fa_wait_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(scratch, timeout_ns);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "selftest launch");
+    return FA_OK;
+}
+
 fa_status fa_last_device_error(void* stream, int* site) {
     if (site) *site = 0;
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
     int dev = 0;
     if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev < 0 || dev >= MAX_DEVICES || !g_err_word[dev]) return FA_OK;
+    if (dev < 0 || dev >= MAX_DEVICES) return FA_OK;
+    // The error word of the ordinary entry points, then the record of fa_fwd_noalloc (the static
+    // array, reached through the device address looked up on that entry's first call). Reading
+    // and clearing either allocates nothing.
     int word = 0;
-    if ((e = cudaMemcpy(&word, g_err_word[dev], sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
-        return cuda_fail(e, "cudaMemcpy(error word)");
+    for (int* w : {g_err_word[dev], g_noalloc_addr[dev]}) {
+        if (!w) continue;
+        int x = 0;
+        if ((e = cudaMemcpy(&x, w, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpy(error word)");
+        if (x == 0) continue;
+        if ((e = cudaMemset(w, 0, sizeof(int))) != cudaSuccess)
+            return cuda_fail(e, "cudaMemset(error word)");
+        if (word == 0) word = x;
+    }
     if (word == 0) return FA_OK;
     if (site) *site = word;
-    if ((e = cudaMemset(g_err_word[dev], 0, 16)) != cudaSuccess) return cuda_fail(e, "cudaMemset(error word)");
     if (word == fa::SITE_BWD_SMEM_LAYOUT)
         return fail(FA_ERR_UNSUPPORTED, "the dK/dV kernel could not align its shared memory (site %d)", word);
     return fail(FA_ERR_TIMEOUT, "a kernel gave up waiting at site %d", word);
+}
+
+int fa_debug_bounds_enabled(void) { return fa::kBoundsChecked ? 1 : 0; }
+
+fa_status fa_debug_bounds_report(int* site, long long* index) {
+    if (!site || !index) return fail(FA_ERR_INVALID_ARGUMENT, "null output pointer");
+    *site = 0;
+    *index = 0;
+#ifdef FA_DEBUG_BOUNDS
+    unsigned long long rec[2] = {0, 0};
+    cudaError_t e = cudaMemcpyFromSymbol(rec, fa::g_bounds_record, sizeof(rec));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyFromSymbol(bounds record)");
+    if (rec[0] != 0) {
+        const unsigned long long zero[2] = {0, 0};
+        if ((e = cudaMemcpyToSymbol(fa::g_bounds_record, zero, sizeof(zero))) != cudaSuccess)
+            return cuda_fail(e, "cudaMemcpyToSymbol(bounds record)");
+        *site = static_cast<int>(rec[0]);
+        *index = static_cast<long long>(rec[1]);
+    }
+#endif
+    return FA_OK;
+}
+
+fa_status fa_debug_bounds_selftest(int* buf, void* stream) {
+    if (!fa::kBoundsChecked)
+        return fail(FA_ERR_UNSUPPORTED, "this build does not check bounds (see libfa_debug.so)");
+    if (!buf) return fail(FA_ERR_INVALID_ARGUMENT, "null buffer");
+    if (reinterpret_cast<uintptr_t>(buf) % 4 != 0) return fail(FA_ERR_MISALIGNED, "buffer not 4-byte aligned");
+    fa_bounds_selftest_kernel<<<1, 2, 0, static_cast<cudaStream_t>(stream)>>>(buf);
+    cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return cuda_fail(e, "bounds selftest launch");
+    return FA_OK;
 }
 
 const char* fa_status_string(fa_status status) {

@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(256) fa_bwd_prep_kernel(const void* __restrict
     // Sum over the TPR threads of the row (aligned groups within the warp).
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, off);
-    if (live && sub == 0) {
+    if (live && sub == 0 && in_bounds(h < bh && r < nq_pad, BOUNDS_BWD_PREP, w)) {
         if (r < nq) {
             delta[w] = acc;
             lse2[w] = lse[h * nq + r] * 1.4426950408889634f;
@@ -506,15 +506,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         }
         // Epilogue: dV and scale * dK for this thread's key row.
         const size_t row_off = (static_cast<size_t>(bh) * p.nk + kr) * D * 2;
+        const bool row_ok = kr >= p.nk || in_bounds(bh >= 0 && bh < p.bh && kr >= 0,
+                                                    BOUNDS_BWD_DKDV,
+                                                    static_cast<long long>(bh) * p.nk + kr);
         if (n == 0) {
-            if (kr < p.nk) {
+            if (kr < p.nk && row_ok) {
                 zero_row<D>(static_cast<uint8_t*>(p.dv) + row_off);
                 zero_row<D>(static_cast<uint8_t*>(p.dk) + row_off);
             }
         } else if (ok && wait_bar_warp(bar(L::B_MMA_DONE), 0, ctl, SITE_BWD_COMPUTE)) {
             ptx::tc_fence_after();
-            store_row<D, BF16>(tmem + lanes + BWD_TMEM_A, 1.f, static_cast<uint8_t*>(p.dv) + row_off, kr < p.nk);
-            store_row<D, BF16>(tmem + lanes + BWD_TMEM_B, p.scale, static_cast<uint8_t*>(p.dk) + row_off, kr < p.nk);
+            store_row<D, BF16>(tmem + lanes + BWD_TMEM_A, 1.f, static_cast<uint8_t*>(p.dv) + row_off, kr < p.nk && row_ok);
+            store_row<D, BF16>(tmem + lanes + BWD_TMEM_B, p.scale, static_cast<uint8_t*>(p.dk) + row_off, kr < p.nk && row_ok);
         }
         ptx::tmem_wait_st();
     }
@@ -774,7 +777,9 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
             ptx::tc_fence_after();
             store_row<D, BF16>(tmem + lanes + DQ_TMEM_DQ, p.scale,
                                static_cast<uint8_t*>(p.dq) + (static_cast<size_t>(bh) * p.nq + row) * D * 2,
-                               row < p.nq);
+                               row < p.nq && in_bounds(bh >= 0 && bh < p.bh && row >= 0,
+                                                       BOUNDS_BWD_DQ,
+                                                       static_cast<long long>(bh) * p.nq + row));
         }
         ptx::tmem_wait_st();
     }

@@ -58,6 +58,8 @@
 
 #include <cstdint>
 
+#include "fa_bounds.cuh"
+#include "fa_rope_kernel.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -93,6 +95,7 @@ enum WaitSite : int {
     SITE_EPI_O_READY = 9,
     SITE_DRAIN = 10,
     SITE_EPI_O_STAGED = 14,
+    SITE_ROPE_Q_FULL = 15,
     SITE_SELFTEST = 30,   // fa_wait_selftest: a barrier that nothing arrives on
 };
 
@@ -125,6 +128,11 @@ struct Params {
     float scale_log2;          // scale * log2(e)
     float rescale_threshold;   // lazy-rescale threshold, log2 units (0 = rescale on every rise)
     unsigned long long timeout_ns;
+    // Rotary embedding of Q inside the kernel (null: none): angle tables [nq][D/2] fp32 of the
+    // query rows, and the pair form (0 rotate-half, 1 interleaved pairs).
+    const float* rope_cos;
+    const float* rope_sin;
+    int rope_form;
 };
 
 template <int D>
@@ -148,7 +156,8 @@ struct Smem {
     static constexpr int B_P_FULL = B_P_HALF + Q_TILES;         // [2] softmax -> MMA (keys 64-127)
     static constexpr int B_O_READY = B_P_FULL + Q_TILES;        // [2] MMA -> epilogue
     static constexpr int B_O_STAGED = B_O_READY + Q_TILES;      // [2] O_t in smem (4 warps)
-    static constexpr int B_DRAIN = B_O_STAGED + Q_TILES;
+    static constexpr int B_Q_ROT = B_O_STAGED + Q_TILES;        // [2] Q_t rotated (8 warps)
+    static constexpr int B_DRAIN = B_Q_ROT + Q_TILES;
     static constexpr int NUM_BARS = B_DRAIN + 1;
     static constexpr int TMEM_SLOT_OFF = BAR_OFF + NUM_BARS * 8;
     static constexpr int ABORT_OFF = TMEM_SLOT_OFF + 4;
@@ -257,23 +266,28 @@ __device__ __forceinline__ void epilogue(int t, uint32_t tmem, uint32_t sbase, c
         const int tu = bh * p.num_units + q0 / UNIT_ROWS - p.split_begin;
         const size_t prow =
             (static_cast<size_t>(split) * p.split_units + tu) * split_rows + (row - q0);
+        const bool part_ok =
+            row >= p.nq || in_bounds(split < p.num_splits && tu >= 0 && tu < p.split_units &&
+                                         row - q0 < split_rows,
+                                     BOUNDS_FWD_PART, static_cast<long long>(prow));
 #pragma unroll 1
         for (int q = 0; q < D / 32; ++q) {
             uint32_t o[32];
             ptx::tmem_ld32(o_cols + q * 32, o);
             ptx::tmem_wait_ld();
             ptx::reg_fence(o);
-            if (row < p.nq) {
+            if (row < p.nq && part_ok) {
                 uint4* dst = reinterpret_cast<uint4*>(p.o_part + prow * D + q * 32);
 #pragma unroll
                 for (int v = 0; v < 8; ++v)
                     dst[v] = make_uint4(o[4 * v], o[4 * v + 1], o[4 * v + 2], o[4 * v + 3]);
             }
         }
-        if (row < p.nq) reinterpret_cast<float2*>(p.ml_part)[prow] = make_float2(m_ref, l);
+        if (row < p.nq && part_ok) reinterpret_cast<float2*>(p.ml_part)[prow] = make_float2(m_ref, l);
         return;
     }
-    if (p.lse != nullptr && row < p.nq) {
+    if (p.lse != nullptr && row < p.nq &&
+        in_bounds(bh >= 0 && bh < p.bh, BOUNDS_FWD_LSE, static_cast<long long>(bh) * p.nq + row)) {
         // L = m + log l in natural-log units ("Flash Attention 2", "Write the data back to
         // HBM"): the kernel's m and l are in base 2 relative to the reference maximum.
         p.lse[static_cast<size_t>(bh) * p.nq + row] = (m_ref + __log2f(l)) * 0.6931471805599453f;
@@ -316,12 +330,92 @@ __device__ __forceinline__ void epilogue(int t, uint32_t tmem, uint32_t sbase, c
     if ((threadIdx.x & 31) == 0) ptx::mbar_arrive(bar(L::B_O_STAGED + t));
     if (r == 0) {
         if (!wait_bar(bar(L::B_O_STAGED + t), 0, ctl, SITE_EPI_O_STAGED)) return;
+        // The tensor map clips rows past Nq (a decoding shape's second tile is wholly past it);
+        // the unit itself must start inside the tensor.
+        if (!in_bounds(bh >= 0 && bh < p.bh && q0 >= 0 && q0 < p.nq, BOUNDS_FWD_O,
+                       static_cast<long long>(bh) * p.nq + q0))
+            return;
 #pragma unroll
         for (int cb = 0; cb < D / 64; ++cb)
             ptx::tma_store_3d(tm_o, stage + cb * (BM * 128), cb * 64, q0 + t * BM, bh);
         ptx::bulk_commit_group();
         ptx::bulk_wait_group_read0();  // shared memory stays allocated until the copy has read it
     }
+}
+
+// ---------------------------------------------------------------------------------------------
+// rotary embedding of the Q tiles in shared memory ("Attention", phobos stdlib docs, "Rotary
+// position embeddings"), by both softmax warpgroups before their key loops. The work of a tile is
+// 128 rows x D/8 items of 4 pairs (pairs 4g .. 4g+3 of a row, angles cos/sin[row][4g .. 4g+4));
+// thread x of the 256 takes items x, x + 256, ..., so consecutive lanes take consecutive items of
+// one row: their angle loads are coalesced, and their shared-memory accesses cover whole 128-byte
+// rows. Tile 0 is rotated first, then tile 1; after each, every warp signals B_Q_ROT_t, which the
+// MMA warp waits on instead of the load. The producer loads both Q tiles before K_0 in this mode,
+// so the rotation overlaps K_0's load. All angles are loaded before the first wait. Rows past Nq
+// (zero fill, never stored) are left as they are.
+// ---------------------------------------------------------------------------------------------
+template <int D, bool BF16>
+__device__ __forceinline__ bool rotate_q(uint32_t sbase, const Params& p, const Ctl& ctl, int q0) {
+    using L = Smem<D>;
+    constexpr int ITEMS_PER_ROW = D / 8;                   // items of 4 pairs per row
+    constexpr int PER_THREAD = BM * ITEMS_PER_ROW / 256;   // items per thread and tile
+    const int x = threadIdx.x;                             // 0..255
+    float4 cs[Q_TILES][PER_THREAD], sn[Q_TILES][PER_THREAD];
+#pragma unroll
+    for (int t = 0; t < Q_TILES; ++t)
+#pragma unroll
+        for (int k = 0; k < PER_THREAD; ++k) {
+            const int item = k * 256 + x, r = item / ITEMS_PER_ROW, g = item % ITEMS_PER_ROW;
+            const int row = q0 + t * BM + r;
+            if (row < p.nq) {
+                const size_t off = static_cast<size_t>(row) * (D / 2) + 4 * g;
+                cs[t][k] = __ldg(reinterpret_cast<const float4*>(p.rope_cos + off));
+                sn[t][k] = __ldg(reinterpret_cast<const float4*>(p.rope_sin + off));
+            }
+        }
+#pragma unroll
+    for (int t = 0; t < Q_TILES; ++t) {
+        const uint32_t q_full = sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(L::B_Q_FULL + t);
+        if (!wait_bar_warp(q_full, 0, ctl, SITE_ROPE_Q_FULL)) return false;
+        const uint32_t tile = sbase + L::Q_OFF + t * L::Q_TILE_BYTES;
+#pragma unroll
+        for (int k = 0; k < PER_THREAD; ++k) {
+            const int item = k * 256 + x, r = item / ITEMS_PER_ROW, g = item % ITEMS_PER_ROW;
+            if (q0 + t * BM + r >= p.nq) continue;
+            // Logical 16-byte chunk c (elements 8c .. 8c+7) of row r: column block c / 8,
+            // swizzled position (c % 8) ^ (r % 8) within the row's 128 bytes.
+            auto chunk = [&](int c) {
+                return tile + (c / 8) * (BM * 128) + r * 128 +
+                       ((static_cast<uint32_t>(c % 8) ^ (r & 7)) << 4);
+            };
+            const float c4[4] = {cs[t][k].x, cs[t][k].y, cs[t][k].z, cs[t][k].w};
+            const float s4[4] = {sn[t][k].x, sn[t][k].y, sn[t][k].z, sn[t][k].w};
+            if (p.rope_form == 0) {
+                // pair i = (x_i, x_{i+D/2}): elements 4g .. 4g+3 (half g % 2 of chunk g / 2) with
+                // the same 8 bytes of chunk g / 2 + D/16
+                const uint32_t a_addr = chunk(g / 2) + (g % 2) * 8;
+                const uint32_t b_addr = chunk(g / 2 + D / 16) + (g % 2) * 8;
+                const uint2 a = ptx::ld_shared_v2(a_addr), b = ptx::ld_shared_v2(b_addr);
+                const uint32_t av[2] = {a.x, a.y}, bv[2] = {b.x, b.y};
+                uint32_t ao[2], bo[2];
+                rope_half4<BF16>(av, bv, c4, s4, ao, bo);
+                ptx::st_shared_v2(a_addr, ao[0], ao[1]);
+                ptx::st_shared_v2(b_addr, bo[0], bo[1]);
+            } else {
+                // pair i = (x_{2i}, x_{2i+1}): pairs 4g .. 4g+3 are chunk g
+                const uint4 v = ptx::ld_shared_v4(chunk(g));
+                const uint32_t xv[4] = {v.x, v.y, v.z, v.w};
+                uint32_t y[4];
+                rope_pairs_n<BF16, 4>(xv, c4, s4, y);
+                ptx::st_shared_v4(chunk(g), y[0], y[1], y[2], y[3]);
+            }
+        }
+        ptx::fence_proxy_async_smem();  // the S products read the tile through the async proxy
+        __syncwarp();
+        if ((threadIdx.x & 31) == 0)
+            ptx::mbar_arrive(sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(L::B_Q_ROT + t));
+    }
+    return true;
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -517,6 +611,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(bar(L::B_P_FULL + t), BM);
             ptx::mbar_init(bar(L::B_O_READY + t), 1);
             ptx::mbar_init(bar(L::B_O_STAGED + t), 4);
+            ptx::mbar_init(bar(L::B_Q_ROT + t), 8);
         }
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(bar(L::B_K_FULL + s), 1);
@@ -565,9 +660,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                                          q0 + t * BM, bh, bar(L::B_Q_FULL + t));
                 };
                 // Q_0, then K_0, then the other Q tiles: the first product S_0(0) needs only the
-                // first two.
+                // first two. When the kernel rotates Q, both Q tiles come first, so that their
+                // rotation overlaps K_0's load.
                 load_q(0);
                 int q_loaded = 1;
+                const bool q_first = p.rope_cos != nullptr;
+                if (q_first) {
+                    for (int t = 1; t < Q_TILES; ++t) load_q(t);
+                    q_loaded = Q_TILES;
+                }
                 const int n = n_tiles[Q_TILES - 1];
                 int issued = 0;
                 for (int j = 0; j < n; ++j) {
@@ -579,7 +680,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ptx::tma_load_3d(sk + st * L::KV_BYTES + c * (BN * 128), &tm_k, c * 64,
                                          (kv0 + j) * BN, bh, bar(L::B_K_FULL + st));
                     issued = 2 * j + 1;
-                    if (j == 0) {
+                    if (j == 0 && !q_first) {
                         for (int t = 1; t < Q_TILES; ++t) load_q(t);
                         q_loaded = Q_TILES;
                     }
@@ -643,13 +744,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // Per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1). S_t(j+1) overwrites the TMEM
             // columns P_t(j) occupies, so it follows PV_t(j) (MMAs of one thread run in order).
             const int n0 = n_tiles[0], n1 = n_tiles[Q_TILES - 1];
-            bool ok = wait_bar_warp(bar(L::B_Q_FULL + 0), 0, ctl, SITE_MMA_Q_FULL) &&
+            // Q_t is ready once loaded, or once rotated when the kernel applies the rotary
+            // embedding to it.
+            const int q_ready = p.rope_cos != nullptr ? L::B_Q_ROT : L::B_Q_FULL;
+            bool ok = wait_bar_warp(bar(q_ready + 0), 0, ctl, SITE_MMA_Q_FULL) &&
                       wait_bar_warp(bar(L::B_K_FULL + 0), 0, ctl, SITE_MMA_K_FULL);
             if (ok) {
                 ptx::tc_fence_after();
                 issue_s(0, 0);
                 commit(L::B_S_FULL + 0);
-                ok = wait_bar_warp(bar(L::B_Q_FULL + 1), 0, ctl, SITE_MMA_Q_FULL);
+                ok = wait_bar_warp(bar(q_ready + 1), 0, ctl, SITE_MMA_Q_FULL);
             }
             if (ok) {
                 ptx::tc_fence_after();
@@ -692,8 +796,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else {
         ptx::regs_inc<REG_SOFTMAX>();
-        softmax_role<D, BF16, CAUSAL>(wg, tmem, sbase, p, ctl, bh, q0, split, kv0, n_tiles[wg],
-                                      &tm_o);
+        if (p.rope_cos == nullptr || rotate_q<D, BF16>(sbase, p, ctl, q0))
+            softmax_role<D, BF16, CAUSAL>(wg, tmem, sbase, p, ctl, bh, q0, split, kv0, n_tiles[wg],
+                                          &tm_o);
         ptx::tmem_wait_st();  // no TMEM store of this warp may be pending at dealloc
     }
 

@@ -14,6 +14,7 @@
 
 #include <cstdint>
 
+#include "fa_bounds.cuh"
 #include "sm103_ptx.cuh"
 
 namespace fa {
@@ -22,6 +23,7 @@ namespace fa {
 // bh * num_units + u, whose rows are u * 256 + r for r < split_rows = min(256, nq).
 struct MergeMap {
     int split_begin, num_units, split_rows, nq;
+    int bh;  // slices of O (B * H)
 };
 
 // One warp per merged row; lane i owns D/32 consecutive columns.
@@ -44,6 +46,7 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__
     const int q_row = (unit - bh * map.num_units) * 256 + (row - tu * map.split_rows);
     if (q_row >= map.nq) return;
     const int64_t out_row = static_cast<int64_t>(bh) * map.nq + q_row;
+    if (!in_bounds(bh < map.bh, BOUNDS_MERGE_O, out_row)) return;
     const float2* ml = reinterpret_cast<const float2*>(ml_part);
     float m = -INFINITY, l = 0.f;
     float acc[E];

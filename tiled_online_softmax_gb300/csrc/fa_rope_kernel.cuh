@@ -15,6 +15,8 @@
 
 #include <cstdint>
 
+#include "fa_bounds.cuh"
+
 namespace fa {
 
 template <bool BF16>
@@ -34,6 +36,56 @@ __device__ __forceinline__ uint32_t from_f2(float lo, float hi) {
     } else {
         __half2 v = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&v);
+    }
+}
+
+// One pair rotated in fp32: (x0, x1) -> (x0 cos - x1 sin, x1 cos + x0 sin). Each second product
+// is rounded and the first is fused with the sum (explicit intrinsics, so that every kernel that
+// rotates -- this pass and the attention kernel's prologue on Q -- gives the same bits).
+__device__ __forceinline__ float2 rope_rotate(float x0, float x1, float c, float s) {
+    return make_float2(__fmaf_rn(x0, c, -__fmul_rn(x1, s)), __fmaf_rn(x1, c, __fmul_rn(x0, s)));
+}
+
+// Rotate-half: four 32-bit words of the first half (a) and of the second half (b) of a row,
+// 8 pairs whose angles are cs[0..8), sn[0..8).
+template <bool BF16>
+__device__ __forceinline__ void rope_half8(const uint32_t (&a)[4], const uint32_t (&b)[4],
+                                           const float* cs, const float* sn, uint32_t (&ao)[4],
+                                           uint32_t (&bo)[4]) {
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+        const float2 fa = to_f2<BF16>(a[w]), fb = to_f2<BF16>(b[w]);
+        const float2 lo = rope_rotate(fa.x, fb.x, cs[2 * w], sn[2 * w]);
+        const float2 hi = rope_rotate(fa.y, fb.y, cs[2 * w + 1], sn[2 * w + 1]);
+        ao[w] = from_f2<BF16>(lo.x, hi.x);
+        bo[w] = from_f2<BF16>(lo.y, hi.y);
+    }
+}
+
+// Rotate-half, 4 pairs: two 32-bit words of the first half (a) and of the second half (b).
+template <bool BF16>
+__device__ __forceinline__ void rope_half4(const uint32_t (&a)[2], const uint32_t (&b)[2],
+                                           const float* cs, const float* sn, uint32_t (&ao)[2],
+                                           uint32_t (&bo)[2]) {
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+        const float2 fa = to_f2<BF16>(a[w]), fb = to_f2<BF16>(b[w]);
+        const float2 lo = rope_rotate(fa.x, fb.x, cs[2 * w], sn[2 * w]);
+        const float2 hi = rope_rotate(fa.y, fb.y, cs[2 * w + 1], sn[2 * w + 1]);
+        ao[w] = from_f2<BF16>(lo.x, hi.x);
+        bo[w] = from_f2<BF16>(lo.y, hi.y);
+    }
+}
+
+// Interleaved pairs: n 32-bit words, one pair each, angles cs[0..n), sn[0..n).
+template <bool BF16, int N>
+__device__ __forceinline__ void rope_pairs_n(const uint32_t (&x)[N], const float* cs,
+                                             const float* sn, uint32_t (&y)[N]) {
+#pragma unroll
+    for (int w = 0; w < N; ++w) {
+        const float2 f = to_f2<BF16>(x[w]);
+        const float2 r = rope_rotate(f.x, f.y, cs[w], sn[w]);
+        y[w] = from_f2<BF16>(r.x, r.y);
     }
 }
 
@@ -73,20 +125,14 @@ __global__ void __launch_bounds__(256) fa_rope_kernel(const uint16_t* x, uint16_
         const float sn[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
         const uint16_t* src = x + row * d;
         uint16_t* dst = y + row * d;
+        if (!in_bounds(row < rows_total && nrow < n && i0 + 8 <= half, BOUNDS_ROPE, row)) continue;
         if constexpr (FORM == 0) {
             // 8 elements of each half: a_i0.. and b_i0..
             const uint4 a = *reinterpret_cast<const uint4*>(src + i0);
             const uint4 b = *reinterpret_cast<const uint4*>(src + half + i0);
             const uint32_t av[4] = {a.x, a.y, a.z, a.w}, bv[4] = {b.x, b.y, b.z, b.w};
             uint32_t ao[4], bo[4];
-#pragma unroll
-            for (int w = 0; w < 4; ++w) {
-                const float2 fa = to_f2<BF16>(av[w]), fb = to_f2<BF16>(bv[w]);
-                const float c_lo = cs[2 * w], c_hi = cs[2 * w + 1];
-                const float s_lo = sn[2 * w], s_hi = sn[2 * w + 1];
-                ao[w] = from_f2<BF16>(fa.x * c_lo - fb.x * s_lo, fa.y * c_hi - fb.y * s_hi);
-                bo[w] = from_f2<BF16>(fb.x * c_lo + fa.x * s_lo, fb.y * c_hi + fa.y * s_hi);
-            }
+            rope_half8<BF16>(av, bv, cs, sn, ao, bo);
             *reinterpret_cast<uint4*>(dst + i0) = make_uint4(ao[0], ao[1], ao[2], ao[3]);
             *reinterpret_cast<uint4*>(dst + half + i0) = make_uint4(bo[0], bo[1], bo[2], bo[3]);
         } else {
@@ -95,11 +141,7 @@ __global__ void __launch_bounds__(256) fa_rope_kernel(const uint16_t* x, uint16_
             const uint4 p1 = *reinterpret_cast<const uint4*>(src + 2 * i0 + 8);
             const uint32_t pv[8] = {p0.x, p0.y, p0.z, p0.w, p1.x, p1.y, p1.z, p1.w};
             uint32_t po[8];
-#pragma unroll
-            for (int w = 0; w < 8; ++w) {
-                const float2 f = to_f2<BF16>(pv[w]);
-                po[w] = from_f2<BF16>(f.x * cs[w] - f.y * sn[w], f.y * cs[w] + f.x * sn[w]);
-            }
+            rope_pairs_n<BF16, 8>(pv, cs, sn, po);
             *reinterpret_cast<uint4*>(dst + 2 * i0) = make_uint4(po[0], po[1], po[2], po[3]);
             *reinterpret_cast<uint4*>(dst + 2 * i0 + 8) = make_uint4(po[4], po[5], po[6], po[7]);
         }

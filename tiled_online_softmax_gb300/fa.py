@@ -8,6 +8,7 @@ import math
 from pathlib import Path
 
 LIB_PATH = Path(__file__).resolve().with_name("libfa.so")
+DEBUG_LIB_PATH = Path(__file__).resolve().with_name("libfa_debug.so")
 
 FA_F16, FA_BF16 = 0, 1
 STATUS = {0: "FA_OK", 1: "FA_ERR_INVALID_ARGUMENT", 2: "FA_ERR_UNSUPPORTED",
@@ -17,7 +18,17 @@ EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_e
            "fa_set_rescale_threshold", "fa_get_rescale_threshold", "fa_fwd_lse",
            "fa_splitkv_workspace_bytes", "fa_fwd_splitkv", "fa_set_tail_split", "fa_rope",
            "fa_rope_workspace_bytes", "fa_fwd_rope", "fa_bwd_workspace_bytes", "fa_bwd",
-           "fa_wait_selftest", "fa_timer_start", "fa_timer_stop", "fa_timer_read")
+           "fa_wait_selftest", "fa_wait_selftest_noalloc", "fa_timer_start", "fa_timer_stop",
+           "fa_timer_read", "fa_fwd_plan", "fa_debug_bounds_enabled", "fa_debug_bounds_report",
+           "fa_debug_bounds_selftest")
+
+
+class Plan(ctypes.Structure):
+    """struct fa_plan: how fa_fwd divides a shape into launches."""
+    _fields_ = [("units", ctypes.c_int64), ("split_begin", ctypes.c_int64),
+                ("split_units", ctypes.c_int64), ("num_splits", ctypes.c_int),
+                ("tiles_per_split", ctypes.c_int), ("ctas", ctypes.c_int64),
+                ("launches", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
 
 
 class FaError(RuntimeError):
@@ -27,16 +38,30 @@ class FaError(RuntimeError):
 
 
 _lib: ctypes.CDLL | None = None
+_debug_lib: ctypes.CDLL | None = None
 
 
 def lib() -> ctypes.CDLL:
     """The loaded libfa.so with its signatures declared."""
     global _lib
-    if _lib is not None:
-        return _lib
-    if not LIB_PATH.exists():
-        raise RuntimeError(f"{LIB_PATH} is not built: run tiled_online_softmax_gb300.build.build()")
-    L = ctypes.CDLL(str(LIB_PATH))
+    if _lib is None:
+        _lib = _load(LIB_PATH)
+    return _lib
+
+
+def debug_lib() -> ctypes.CDLL:
+    """The bounds-checked build, libfa_debug.so (same functions, same results; every global store
+    checked against its tensor's extent)."""
+    global _debug_lib
+    if _debug_lib is None:
+        _debug_lib = _load(DEBUG_LIB_PATH)
+    return _debug_lib
+
+
+def _load(path: Path) -> ctypes.CDLL:
+    if not path.exists():
+        raise RuntimeError(f"{path} is not built: run tiled_online_softmax_gb300.build.build()")
+    L = ctypes.CDLL(str(path))
     i64, vp = ctypes.c_int64, ctypes.c_void_p
     sig = [vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float, ctypes.c_int, ctypes.c_int, vp]
     L.fa_fwd.argtypes = sig
@@ -73,6 +98,11 @@ def lib() -> ctypes.CDLL:
     L.fa_last_device_error.restype = ctypes.c_int
     L.fa_wait_selftest.argtypes = [ctypes.c_ulonglong, vp]
     L.fa_wait_selftest.restype = ctypes.c_int
+    L.fa_wait_selftest_noalloc.argtypes = [ctypes.c_ulonglong, vp]
+    L.fa_wait_selftest_noalloc.restype = ctypes.c_int
+    L.fa_fwd_plan.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                              ctypes.POINTER(Plan)]
+    L.fa_fwd_plan.restype = ctypes.c_int
     L.fa_timer_start.argtypes = []
     L.fa_timer_start.restype = ctypes.c_int
     L.fa_timer_stop.argtypes = []
@@ -88,7 +118,12 @@ def lib() -> ctypes.CDLL:
     L.fa_set_rescale_threshold.restype = ctypes.c_int
     L.fa_get_rescale_threshold.argtypes = []
     L.fa_get_rescale_threshold.restype = ctypes.c_float
-    _lib = L
+    L.fa_debug_bounds_enabled.argtypes = []
+    L.fa_debug_bounds_enabled.restype = ctypes.c_int
+    L.fa_debug_bounds_report.argtypes = [ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_longlong)]
+    L.fa_debug_bounds_report.restype = ctypes.c_int
+    L.fa_debug_bounds_selftest.argtypes = [vp, vp]
+    L.fa_debug_bounds_selftest.restype = ctypes.c_int
     return L
 
 
@@ -361,6 +396,22 @@ def wait_selftest(timeout_ns: int, stream=None) -> None:
     _raise_if(lib().fa_wait_selftest(int(timeout_ns), stream.cuda_stream))
 
 
+def wait_selftest_noalloc(timeout_ns: int, stream=None) -> None:
+    """The same self-test aimed at fa_fwd_noalloc's static record (allocates nothing)."""
+    import torch
+
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    _raise_if(lib().fa_wait_selftest_noalloc(int(timeout_ns), stream.cuda_stream))
+
+
+def plan(B: int, H: int, Nq: int, Nk: int, D: int, causal: bool = False, num_sms: int = 0) -> dict:
+    """How forward() divides a shape into launches on `num_sms` SMs (0: the current device)."""
+    p = Plan()
+    _raise_if(lib().fa_fwd_plan(B, H, Nq, Nk, D, int(bool(causal)), int(num_sms), ctypes.byref(p)))
+    return {name: getattr(p, name) for name, _ in Plan._fields_}
+
+
 def set_rescale_threshold(log2_threshold: float) -> None:
     """Process-wide lazy-rescale threshold (log2 units, [0, 64]; 0 = rescale on every rise;
     fp16 launches use at most 15)."""
@@ -375,6 +426,17 @@ def set_tail_split(enable: bool) -> None:
 
 def get_rescale_threshold() -> float:
     return float(lib().fa_get_rescale_threshold())
+
+
+def bounds_report(L: ctypes.CDLL | None = None) -> tuple[int, int]:
+    """(site, index) of the first bounds violation the checked build recorded since the last
+    report, (0, 0) if none; read and cleared. Synchronise the device first."""
+    L = L or debug_lib()
+    site, index = ctypes.c_int(0), ctypes.c_longlong(0)
+    st = L.fa_debug_bounds_report(ctypes.byref(site), ctypes.byref(index))
+    if st != 0:
+        raise FaError(st, L.fa_last_error_message().decode())
+    return site.value, index.value
 
 
 def status_string(status: int) -> str:
