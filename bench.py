@@ -127,7 +127,9 @@ def profiled_traffic(workload_name: str):
 class ClockSampler:
     """nvidia-smi clock and throttle-reason samples while the GPU works. mark(name) opens a phase
     (closing the previous one); stop() gives the median SM clock of the whole run and of each
-    phase, matched by the samples' own timestamps."""
+    phase, matched by the samples' own timestamps. Samples come every 100 ms: a timed phase of a
+    few milliseconds usually holds none, so each workload's 1 s pre-heat of the same work, right
+    before its timed steps, gives the clock they ran at."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
@@ -261,6 +263,8 @@ def time_extra(w, dev, stream, steps, warmup, peak, sampler=None):
     for i in range(warmup):
         step(i)
     torch.cuda.synchronize(dev)
+    if sampler:
+        sampler.mark(f"{w.name}:preheat")
     t_end = time.perf_counter() + 1.0
     i = 0
     while time.perf_counter() < t_end:
@@ -523,6 +527,8 @@ def main():
         step(i)
     torch.cuda.synchronize(dev)
     sampler = ClockSampler(dev.index) if not args.profile else None
+    if sampler:
+        sampler.mark(f"{w.name}:preheat")
     t_end = time.perf_counter() + (0.0 if args.profile else 1.0)
     i = 0
     while time.perf_counter() < t_end:
@@ -536,7 +542,7 @@ def main():
     barrier()
     torch.cuda.synchronize(dev)
     if sampler:
-        sampler.mark("headline:timed")
+        sampler.mark(f"{w.name}:timed")
     ev0.record(stream)
     for i in range(args.steps):
         step(i)
@@ -545,7 +551,7 @@ def main():
     barrier()
     ms_total = ev0.elapsed_time(ev1)
     if sampler:
-        sampler.mark("headline:kernel_timer")
+        sampler.mark(f"{w.name}:kernel_timer")
     # The same K steps again with the library's kernel timer on: CUDA events around each launch,
     # on its stream, give every kernel's own device time. The events add small gaps between
     # launches, so this pass is kept out of the timed region above.

@@ -49,7 +49,7 @@ def main(path: str) -> None:
               f"{max(r['max_err'] for r in others):.3e}.")
     bwd = [r for r in recs if "rel_norm_err" in r]
     if bwd:
-        print("\n| backward gradient | shape | elements | norm error / norm | max error / max |g| |")
+        print("\n| backward gradient | shape | elements | norm error / norm | max error / largest magnitude |")
         print("|---|---|---|---|---|")
         for r in bwd:
             print(f"| {r['what']} | {r['shape']} | {r['elements']:,} | {r['rel_norm_err']:.3e} |"
