@@ -396,6 +396,15 @@ def run_other_pass(args, w):
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize(dev)
+    # About a second of the same work first, as for the forward pass, so that the timed steps
+    # run at the clock this load settles to.
+    sampler = ClockSampler(dev.index)
+    sampler.mark(f"{w.name}:preheat")
+    t_end = time.perf_counter() + 1.0
+    while time.perf_counter() < t_end:
+        step()
+        torch.cuda.synchronize(dev)
+    sampler.mark(None)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
@@ -442,7 +451,7 @@ def run_other_pass(args, w):
                      "kernel_ms_per_step": top_ms,
                      "kernels_ms_per_step": {k: v[0] / args.steps for k, v in kernels.items()},
                      "peak_kind": f"{kind} " + ("bf16 dense (burst)" if unit == "TFLOP/s" else "copy bandwidth")},
-        "separate_passes": separate,
+        "separate_passes": separate, "clocks": sampler.stop(),
         "gpu_launches": sum(n for _, n in kernels.values())}), flush=True)
     return 0
 
