@@ -21,7 +21,8 @@ Every named N(0, 1) workload is held to the literal max and mean; the large-magn
 the rounding max and the literal mean; edge shapes to the rounding max and the auto mean.
 
 Set FA_PARITY_REPORT to a file path to append one JSON line per comparison (name, shape, rows,
-literal max and mean, rounding floor, the readings asserted).
+literal max and mean, rounding floor, the readings asserted; for the full-size workloads also
+the oracle's wall-clock seconds and thread count on this host).
 """
 import json
 import os
@@ -80,13 +81,14 @@ def mean_bound(stats: dict, mean: str) -> float:
     raise ValueError(mean)
 
 
-def assert_parity(stats: dict, literal: bool = True, what: str = "", mean: str | None = None) -> None:
+def assert_parity(stats: dict, literal: bool = True, what: str = "", mean: str | None = None,
+                  extra: dict | None = None) -> None:
     """literal: the max reading ("literal" if True, "rounding" if False). mean: "literal",
     "floor" or "auto"; default "literal" with the literal max, "auto" with the rounding max."""
     if mean is None:
         mean = "literal" if literal else "auto"
     mb = mean_bound(stats, mean)
-    _report(what, stats, literal, mean, mb)
+    _report(what, stats, literal, mean, mb, extra or {})
     assert stats["finite"], f"{what}: non-finite output"
     assert stats["mean_err"] <= mb, f"{what}: mean |err| {stats['mean_err']:.3g} > {mb:.3g}"
     if literal:
@@ -107,7 +109,7 @@ def describe(w) -> None:
                           f"{' causal' if w.causal else ''}", D=w.D)
 
 
-def _report(what, stats, literal, mean, mb) -> None:
+def _report(what, stats, literal, mean, mb, extra) -> None:
     path = os.environ.get("FA_PARITY_REPORT")
     if not path:
         return
@@ -115,6 +117,6 @@ def _report(what, stats, literal, mean, mb) -> None:
                elements=stats["n"], max_err=stats["max_err"], mean_err=stats["mean_err"],
                rounding_floor=stats["rounding_floor"], mean_floor=stats["mean_floor"],
                max_reading="literal" if literal else "rounding", mean_reading=mean,
-               mean_bound=mb, worst_excess=stats["worst_excess"])
+               mean_bound=mb, worst_excess=stats["worst_excess"], **extra)
     with open(path, "a") as f:
         f.write(json.dumps(rec) + "\n")

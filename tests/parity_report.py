@@ -29,15 +29,17 @@ def main(path: str) -> None:
         if r.get("what") in NAMED and r.get("shape") == shape(inputs.WORKLOADS[r["what"]]):
             fwd[r["what"]] = r
     print("| workload | shape | rows compared | max abs err | mean abs err | rounding floor (max) |"
-          " rounding floor (mean) | max reading | mean reading (bound) |")
-    print("|---|---|---|---|---|---|---|---|---|")
+          " rounding floor (mean) | max reading | mean reading (bound) | oracle on the host |")
+    print("|---|---|---|---|---|---|---|---|---|---|")
     for name in NAMED:
         r = fwd.get(name)
         if r is None:
             continue
+        host = (f"{r['oracle_seconds']:.2f} s, {r['oracle_threads']} threads"
+                if "oracle_seconds" in r else "")
         print(f"| {name} | {r['shape']} | {r['rows']:,} | {r['max_err']:.3e} | {r['mean_err']:.3e} |"
               f" {r['rounding_floor']:.3e} | {r['mean_floor']:.2e} | {r['max_reading']} |"
-              f" {r['mean_reading']} ({r['mean_bound']:.2e}) |")
+              f" {r['mean_reading']} ({r['mean_bound']:.2e}) | {host} |")
     others = [r for r in recs if r.get("shape") and "rel_norm_err" not in r
               and fwd.get(r.get("what")) is not r]
     if others:

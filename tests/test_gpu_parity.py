@@ -5,6 +5,7 @@ times and is compared with the oracle element by element on every output. The la
 are compared a few (batch, head) slices at a time, so that the oracle's fp64 copies stay small.
 """
 import math
+import time
 
 import numpy as np
 import pytest
@@ -50,13 +51,18 @@ def full_check(fa, orc, w: inputs.Workload, literal=True, mean=None, slices_per_
     o = inputs.from_torch(run_gpu(fa, bits, w)).reshape(w.B * w.H, w.Nq, w.D)
     q, k, v = (bits[n].reshape(w.B * w.H, -1, w.D) for n in "qkv")
     parts = []
+    oracle_s = 0.0
     for c0 in range(0, w.B * w.H, slices_per_chunk):
         c1 = min(c0 + slices_per_chunk, w.B * w.H)
-        ref = orc.attention(*(inputs.bits_to_f64(x[c0:c1], w.dtype) for x in (q, k, v)), w.scale,
-                            w.causal)
+        args = [inputs.bits_to_f64(x[c0:c1], w.dtype) for x in (q, k, v)]
+        t0 = time.perf_counter()
+        ref = orc.attention(*args, w.scale, w.causal)
+        oracle_s += time.perf_counter() - t0
         parts.append(parity.compare(o[c0:c1], ref, w.dtype))
     stats = parity.merge(parts)
-    parity.assert_parity(stats, literal, w.name, mean)
+    parity.assert_parity(stats, literal, w.name, mean,
+                         extra=dict(oracle_seconds=oracle_s, oracle_threads=orc.num_threads(),
+                                    gflop=w.flops / 1e9))
     return stats
 
 

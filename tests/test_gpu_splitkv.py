@@ -191,3 +191,30 @@ def test_last_wave_split_workspace_is_reused_across_calls(fa):
             ref = oracle.attention(*(inputs.bits_to_f64(bits[n][0, h], w.dtype) for n in "qkv"),
                                    w.scale, False)
             parity.assert_parity(parity.compare(got[0, h], ref, w.dtype), True, f"{w.name} head {h}")
+
+
+@pytest.mark.parametrize("shape", [
+    (1, 32, 4096, 4096, 128, False),   # last wave split
+    (1, 8, 128, 65536, 128, False),    # few units, every unit split
+    (2, 4, 1000, 1000, 64, False),     # ragged, split in 4
+    (1, 32, 2048, 2048, 128, True),    # causal: one launch
+    (1, 2, 200, 380, 64, False),       # too few key tiles to split
+    (64, 32, 128, 1024, 64, False),    # 2048 units, last wave of 72 split
+], ids=str)
+def test_plan_matches_the_launches(fa, shape):
+    """fa_fwd_plan on the current device (its SM count read from the device) describes the
+    launches fa_fwd then makes: one attention launch, plus a merge launch when it splits."""
+    B, H, Nq, Nk, D, causal = shape
+    props = torch.cuda.get_device_properties(0)
+    plan = fa.plan(B, H, Nq, Nk, D, causal)
+    assert plan == fa.plan(B, H, Nq, Nk, D, causal, num_sms=props.multi_processor_count)
+    q = torch.zeros(B, H, Nq, D, dtype=torch.bfloat16, device="cuda")
+    k = torch.zeros(B, H, Nk, D, dtype=torch.bfloat16, device="cuda")
+    fa.forward(q, k, k, causal=causal)
+    torch.cuda.synchronize()
+    fa.timer_start()
+    fa.forward(q, k, k, causal=causal)
+    kernels = fa.timer_stop()
+    assert kernels["fwd"][1] == 1
+    assert kernels.get("merge", (0.0, 0))[1] == plan["launches"] - 1
+    assert fa.last_device_error() == (0, 0)
