@@ -413,3 +413,28 @@ def test_results_are_ordered_in_the_stream(fa, w):
         alone = fa.forward(copy, k, v, causal=w.causal, scale=w.scale)
         torch.cuda.synchronize()
         assert torch.equal(alone.view(torch.int16), o2.view(torch.int16))
+
+
+def test_million_keys(fa, orc):
+    """128 queries against 2^20 keys (256 MB each of K and V): the default entry splits the one
+    unit across every SM (ranges of 54-55 key tiles) and merges; the first, middle and last rows
+    of the slice are compared with the oracle, which computes them one by one."""
+    w = inputs.Workload("million_keys", 1, 1, 128, 1 << 20, 128, "bf16", False, seed=23)
+    bits = inputs.draw(w)
+    plan = fa.plan(w.B, w.H, w.Nq, w.Nk, w.D, w.causal)
+    assert plan["launches"] == 2 and plan["split_units"] * plan["num_splits"] > 100
+    o = inputs.from_torch(run_gpu(fa, bits, w))
+    rows = np.array([0, 1, 63, 64, 126, 127])
+    ref = orc.attention_rows(inputs.bits_to_f64(bits["q"][0, 0, rows], w.dtype), rows,
+                             inputs.bits_to_f64(bits["k"][0, 0], w.dtype),
+                             inputs.bits_to_f64(bits["v"][0, 0], w.dtype), w.scale, False)
+    parity.describe(w)
+    parity.assert_parity(parity.compare(o[0, 0, rows], ref, w.dtype), True, w.name)
+
+
+def test_many_tiny_slices(fa, orc):
+    """65 536 (batch, head) slices of 3 queries and 5 keys (65 536 CTAs, each one partial tile):
+    every output compared, causal and not."""
+    for causal in (False, True):
+        w = inputs.Workload("tiny_slices", 64, 1024, 3, 5, 64, "f16", causal, seed=24 + causal)
+        full_check(fa, orc, w, literal=False, mean="auto", slices_per_chunk=65536)
