@@ -97,7 +97,9 @@ typedef enum fa_status {
  * and records an event on `stream` after its merge: calls on different streams never share
  * partial states, with no ordering required between them. A call runs as one unsplit launch
  * instead (no workspace; rows differ only by rounding) when its stream is being captured into a
- * CUDA graph, or when all 4 workspaces are still in use by other streams' unfinished calls.
+ * CUDA graph, or when all 4 workspaces are still in use by other streams' unfinished calls, or
+ * while the pool cannot be allocated (out of device memory: from then on; another host thread
+ * capturing a graph in global mode, which forbids allocation: until a later call succeeds).
  * fa_set_tail_split(0) turns the balancing off (always one launch).
  */
 fa_status fa_fwd(const void* Q, const void* K, const void* V, void* O, int64_t B, int64_t H,

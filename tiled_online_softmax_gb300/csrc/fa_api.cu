@@ -591,16 +591,20 @@ struct WsPool {
 WsPool g_ws_pool[MAX_DEVICES];
 bool g_tail_split = true;
 
-// Set up the pool of device `dev` (g_mutex held). False if it cannot be (then no call splits).
+// Set up the pool of device `dev` (g_mutex held). False if it cannot be now (that call runs
+// unsplit).
 bool ws_pool_ready_locked(int dev) {
     WsPool& pool = g_ws_pool[dev];
     if (pool.ready) return true;
     if (pool.failed) return false;
     const size_t bytes = balance_workspace_bytes(g_num_sms[dev]);
     void* base = nullptr;
-    if (cudaMalloc(&base, bytes * WS_SLOTS) != cudaSuccess) {
+    const cudaError_t e = cudaMalloc(&base, bytes * WS_SLOTS);
+    if (e != cudaSuccess) {
         cudaGetLastError();
-        pool.failed = true;
+        // Out of memory stays out of memory: stop trying. Anything else (another thread capturing
+        // a CUDA graph in global mode forbids allocation meanwhile) is retried by a later call.
+        if (e == cudaErrorMemoryAllocation) pool.failed = true;
         return false;
     }
     for (int i = 0; i < WS_SLOTS; ++i) {
