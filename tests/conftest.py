@@ -19,3 +19,21 @@ def _parity_report_context():
 
     parity._context.clear()
     yield
+
+
+@pytest.fixture(scope="session", autouse=True)
+def _checked_build_records_no_violation():
+    """With FA_CHECKED_BUILD=1 every test runs on libfa_debug.so, whose kernels check each global
+    store against its tensor's extent; at the end of the session no violation may be recorded
+    (the planted one of the bounds self-test is read and cleared by its own test)."""
+    yield
+    if os.environ.get("FA_CHECKED_BUILD") != "1":
+        return
+    import torch
+
+    from tiled_online_softmax_gb300 import fa
+
+    if not torch.cuda.is_available():
+        return
+    torch.cuda.synchronize()
+    assert fa.bounds_report(fa.lib()) == (0, 0), "a kernel recorded an out-of-bounds store"

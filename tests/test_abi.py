@@ -109,11 +109,12 @@ def test_checked_build_exports_the_same_interface(fa):
     """libfa_debug.so (every global store bounds-checked) exports everything fa.h declares and says
     it checks; the release build says it does not and refuses the bounds self-test."""
     dbg = fa.debug_lib()
+    rel = fa._load(fa.LIB_PATH)
     missing = [n for n in declared_functions() if not hasattr(dbg, n)]
     assert not missing, missing
     assert dbg.fa_debug_bounds_enabled() == 1
-    assert fa.lib().fa_debug_bounds_enabled() == 0
-    assert fa.lib().fa_debug_bounds_selftest(A, None) == 2  # FA_ERR_UNSUPPORTED
+    assert rel.fa_debug_bounds_enabled() == 0
+    assert rel.fa_debug_bounds_selftest(A, None) == 2  # FA_ERR_UNSUPPORTED
     assert dbg.fa_debug_bounds_selftest(None, None) == 1    # null buffer
     assert dbg.fa_debug_bounds_selftest(A + 2, None) == 3   # misaligned
-    assert fa.lib().fa_debug_bounds_report(None, None) == 1
+    assert rel.fa_debug_bounds_report(None, None) == 1

@@ -5,6 +5,7 @@ from __future__ import annotations
 
 import ctypes
 import math
+import os
 from pathlib import Path
 
 LIB_PATH = Path(__file__).resolve().with_name("libfa.so")
@@ -42,10 +43,11 @@ _debug_lib: ctypes.CDLL | None = None
 
 
 def lib() -> ctypes.CDLL:
-    """The loaded libfa.so with its signatures declared."""
+    """The loaded libfa.so with its signatures declared; libfa_debug.so, the bounds-checked
+    build, instead when the environment sets FA_CHECKED_BUILD=1."""
     global _lib
     if _lib is None:
-        _lib = _load(LIB_PATH)
+        _lib = debug_lib() if os.environ.get("FA_CHECKED_BUILD") == "1" else _load(LIB_PATH)
     return _lib
 
 
