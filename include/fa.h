@@ -118,6 +118,17 @@ fa_status fa_fwd_lse(const void* Q, const void* K, const void* V, void* O, float
                      fa_dtype dtype, void* stream);
 
 /*
+ * fa_fwd_f32out -- fa_fwd_lse with O written in fp32, unrounded: O32 [B, H, Nq, D] float,
+ * device pointer, 16-byte aligned, not overlapping any input (LSE optional, as in fa_fwd_lse).
+ * A checking aid: it separates the kernel's arithmetic error from the rounding of O to 16 bits,
+ * which alone costs up to half an ulp of |O| (0.0156 for bf16 at |O| >= 4). Always one
+ * launch (no key split); the arithmetic up to the output is that of fa_fwd's single launch.
+ */
+fa_status fa_fwd_f32out(const void* Q, const void* K, const void* V, float* O32, float* LSE,
+                        int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale,
+                        int causal, fa_dtype dtype, void* stream);
+
+/*
  * fa_fwd_plan -- how fa_fwd and fa_fwd_lse divide a shape into launches (host only, no GPU work).
  *   num_sms  the SM count to plan for; 0 = the current device's (FA_ERR_UNSUPPORTED without an
  *            sm_103 device).

@@ -320,7 +320,8 @@ struct QRope {
 
 fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LSE, int64_t B,
                  int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal, int dtype,
-                 cudaStream_t stream, const Split& split = Split(), const QRope& rope = QRope()) {
+                 cudaStream_t stream, const Split& split = Split(), const QRope& rope = QRope(),
+                 float* o_f32 = nullptr) {
     int dev = 0;
     int* err = nullptr;
     fa_status s = device_state(&dev, &err);
@@ -354,6 +355,7 @@ fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LS
     p.rope_cos = rope.cos;
     p.rope_sin = rope.sin;
     p.rope_form = rope.form;
+    p.o_f32 = o_f32;
     const bool bf16 = dtype == FA_BF16;
     const int inst = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
     switch (inst) {
@@ -848,6 +850,25 @@ fa_status fa_fwd_lse(const void* Q, const void* K, const void* V, void* O, float
         return fail(FA_ERR_INVALID_ARGUMENT, "LSE overlaps another tensor");
     return forward(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, causal, int(dtype),
                    static_cast<cudaStream_t>(stream));
+}
+
+fa_status fa_fwd_f32out(const void* Q, const void* K, const void* V, float* O32, float* LSE,
+                        int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale,
+                        int causal, fa_dtype dtype, void* stream) {
+    fa_status s = validate(Q, K, V, O32, B, H, Nq, Nk, D, scale, causal, int(dtype), true);
+    if (s != FA_OK) return s;
+    if (LSE && reinterpret_cast<uintptr_t>(LSE) % 4 != 0)
+        return fail(FA_ERR_MISALIGNED, "LSE pointer is not 4-byte aligned");
+    const size_t q_bytes = size_t(B * H) * size_t(Nq) * size_t(D) * 2;
+    const size_t kv_bytes = size_t(B * H) * size_t(Nk) * size_t(D) * 2;
+    const size_t o_bytes = size_t(B * H) * size_t(Nq) * size_t(D) * 4;
+    const size_t lse_bytes = size_t(B * H) * size_t(Nq) * 4;
+    if (overlaps(O32, o_bytes, Q, q_bytes) || overlaps(O32, o_bytes, K, kv_bytes) ||
+        overlaps(O32, o_bytes, V, kv_bytes) || (LSE && overlaps(LSE, lse_bytes, O32, o_bytes)))
+        return fail(FA_ERR_INVALID_ARGUMENT, "output overlaps another tensor");
+    // The kernel's 16-bit output map is built on Q; in this mode nothing is stored through it.
+    return launch(Q, K, V, const_cast<void*>(Q), LSE, B, H, Nq, Nk, D, scale, causal, int(dtype),
+                  static_cast<cudaStream_t>(stream), Split(), QRope(), O32);
 }
 
 size_t fa_splitkv_workspace_bytes(int64_t B, int64_t H, int64_t Nq, int64_t Nk, int64_t D,

@@ -133,6 +133,9 @@ struct Params {
     const float* rope_cos;
     const float* rope_sin;
     int rope_form;
+    // fp32 output (null: none): O / l written unrounded as fp32 [bh][nq][D] instead of the
+    // 16-bit O, to check the arithmetic apart from the output rounding.
+    float* o_f32;
 };
 
 template <int D>
@@ -291,6 +294,30 @@ __device__ __forceinline__ void epilogue(int t, uint32_t tmem, uint32_t sbase, c
         // L = m + log l in natural-log units ("Flash Attention 2", "Write the data back to
         // HBM"): the kernel's m and l are in base 2 relative to the reference maximum.
         p.lse[static_cast<size_t>(bh) * p.nq + row] = (m_ref + __log2f(l)) * 0.6931471805599453f;
+    }
+    if (p.o_f32 != nullptr) {
+        // O_t / l in fp32, one row per thread, unrounded.
+        const float inv_l32 = (l > 0.f) ? 1.f / l : 0.f;
+        const bool keep = row < p.nq && in_bounds(bh >= 0 && bh < p.bh, BOUNDS_FWD_O,
+                                                  static_cast<long long>(bh) * p.nq + row);
+        float* dst_row = p.o_f32 + (static_cast<size_t>(bh) * p.nq + row) * D;
+#pragma unroll 1
+        for (int q = 0; q < D / 32; ++q) {
+            uint32_t o[32];
+            ptx::tmem_ld32(o_cols + q * 32, o);
+            ptx::tmem_wait_ld();
+            ptx::reg_fence(o);
+            if (keep) {
+                float4* dst = reinterpret_cast<float4*>(dst_row + q * 32);
+#pragma unroll
+                for (int v = 0; v < 8; ++v)
+                    dst[v] = make_float4(__uint_as_float(o[4 * v]) * inv_l32,
+                                         __uint_as_float(o[4 * v + 1]) * inv_l32,
+                                         __uint_as_float(o[4 * v + 2]) * inv_l32,
+                                         __uint_as_float(o[4 * v + 3]) * inv_l32);
+            }
+        }
+        return;
     }
     // O_t / l, rounded, staged in shared memory over Q_t (whose last reader, S_t of the last key
     // tile, finished before O_READY_t) in the 128-byte-swizzled layout of the tensor map, then

@@ -21,7 +21,7 @@ EXPORTS = ("fa_fwd", "fa_fwd_host", "fa_release_host_buffers", "fa_last_device_e
            "fa_rope_workspace_bytes", "fa_fwd_rope", "fa_bwd_workspace_bytes", "fa_bwd",
            "fa_wait_selftest", "fa_wait_selftest_noalloc", "fa_timer_start", "fa_timer_stop",
            "fa_timer_read", "fa_fwd_plan", "fa_debug_bounds_enabled", "fa_debug_bounds_report",
-           "fa_debug_bounds_selftest")
+           "fa_debug_bounds_selftest", "fa_fwd_f32out")
 
 
 class Plan(ctypes.Structure):
@@ -74,6 +74,8 @@ def _load(path: Path) -> ctypes.CDLL:
     L.fa_fwd_noalloc.restype = ctypes.c_int
     L.fa_fwd_lse.argtypes = sig[:4] + [vp] + sig[4:]
     L.fa_fwd_lse.restype = ctypes.c_int
+    L.fa_fwd_f32out.argtypes = sig[:4] + [vp] + sig[4:]
+    L.fa_fwd_f32out.restype = ctypes.c_int
     L.fa_splitkv_workspace_bytes.argtypes = [i64, i64, i64, i64, i64, ctypes.c_int]
     L.fa_splitkv_workspace_bytes.restype = ctypes.c_size_t
     L.fa_fwd_splitkv.argtypes = [vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, ctypes.c_float,
@@ -225,6 +227,27 @@ def forward_lse(q, k, v, causal: bool = False, scale: float | None = None, out=N
                                    lse.data_ptr(), B, H, Nq, Nk, D, float(scale),
                                    int(bool(causal)), code, stream.cuda_stream))
     return out, lse
+
+
+def forward_f32(q, k, v, causal: bool = False, scale: float | None = None, lse=None, stream=None):
+    """O in fp32, unrounded (a checking aid: the arithmetic without the 16-bit output rounding),
+    for CUDA tensors; one launch."""
+    import torch
+
+    B, H, Nq, Nk, D = _shape(q, k, v)
+    if not q.is_cuda:
+        raise ValueError("forward_f32() takes CUDA tensors")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    out = torch.empty(B, H, Nq, D, dtype=torch.float32, device=q.device)
+    if stream is None:
+        stream = torch.cuda.current_stream(q.device)
+    with torch.cuda.device(q.device):
+        _raise_if(lib().fa_fwd_f32out(q.data_ptr(), k.data_ptr(), v.data_ptr(), out.data_ptr(),
+                                      lse.data_ptr() if lse is not None else None, B, H, Nq, Nk,
+                                      D, float(scale), int(bool(causal)), _dtype_code(q),
+                                      stream.cuda_stream))
+    return out
 
 
 def splitkv_workspace_bytes(B: int, H: int, Nq: int, Nk: int, D: int, num_splits: int = 0) -> int:
