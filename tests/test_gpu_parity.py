@@ -473,3 +473,31 @@ def test_rescale_stress_fp32_output_meets_the_literal_bar(fa, orc):
     stats = dict(max_err=max_err, mean_err=sum_err / n, rounding_floor=0.0, mean_floor=0.0, n=n,
                  finite=bool(np.all(np.isfinite(got))), worst_excess=max_err - parity.MAX_ERR)
     parity.assert_parity(stats, True, "rescale_stress fp32 output")
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_random_shapes(fa, orc, seed):
+    """Seeded random problems: B, H in 1..5, Nq and Nk in 1..700, either head dimension and
+    16-bit type, causal or not, scale of either sign and size 0.02-2 / sqrt(D). Every output
+    element compared with the oracle, through the default entry (which may split over keys) and,
+    non-causal, through the split-KV entry with a random number of ranges."""
+    rng = np.random.default_rng(1000 + seed)
+    for case in range(5):
+        D = int(rng.choice([64, 128]))
+        dtype = str(rng.choice(["f16", "bf16"]))
+        causal = bool(rng.integers(2))
+        B, H = int(rng.integers(1, 6)), int(rng.integers(1, 6))
+        Nq, Nk = int(rng.integers(1, 701)), int(rng.integers(1, 701))
+        scale = float(np.float32(rng.choice([-1.0, 1.0]) * rng.uniform(0.02, 2.0) / math.sqrt(D)))
+        w = inputs.Workload(f"random_{seed}_{case}", B, H, Nq, Nk, D, dtype, causal,
+                            seed=seed * 100 + case, scale=scale)
+        full_check(fa, orc, w, literal=False, mean="auto")
+        if not causal:
+            bits = inputs.draw(w)
+            q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+            o = fa.forward_splitkv(q, k, v, num_splits=int(rng.integers(1, 9)), scale=w.scale)
+            torch.cuda.synchronize()
+            assert fa.last_device_error() == (0, 0)
+            ref = orc.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"), w.scale)
+            parity.assert_parity(parity.compare(inputs.from_torch(o), ref, w.dtype), False,
+                                 f"{w.name} split-KV", mean="auto")
