@@ -154,3 +154,32 @@ def test_backward_results_are_ordered_in_the_stream(fa, causal):
         assert fa.last_device_error()[0] == 0
         for name, g, c in zip(("dq", "dk", "dv"), grads, copies):
             assert torch.equal(g.view(torch.int16), c.view(torch.int16)), name
+
+
+@pytest.mark.parametrize("seed", range(3))
+def test_backward_random_shapes(fa, seed):
+    """Seeded random problems (B, H in 1..3, Nq and Nk in 1..400, either D and 16-bit type, causal
+    or not, scale of either sign): the GPU's forward and backward against the oracle's exact
+    gradients, to the same per-dtype bound."""
+    rng = np.random.default_rng(2000 + seed)
+    for case in range(4):
+        D = int(rng.choice([64, 128]))
+        dtype = str(rng.choice(["f16", "bf16"]))
+        causal = bool(rng.integers(2))
+        B, H = int(rng.integers(1, 4)), int(rng.integers(1, 4))
+        Nq, Nk = int(rng.integers(1, 401)), int(rng.integers(1, 401))
+        scale = float(np.float32(rng.choice([-1.0, 1.0]) * rng.uniform(0.3, 1.5) / np.sqrt(D)))
+        w = inputs.Workload(f"bwd_random_{seed}_{case}", B, H, Nq, Nk, D, dtype, causal,
+                            seed=500 + seed * 10 + case, scale=scale)
+        bits = inputs.draw(w)
+        dout_bits = inputs.draw(w.with_(seed=w.seed + 1000))["q"]
+        q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+        do = inputs.to_torch(dout_bits, w.dtype).cuda()
+        o, lse = fa.forward_lse(q, k, v, causal=w.causal, scale=w.scale)
+        grads = fa.backward(q, k, v, o, lse, do, causal=w.causal, scale=w.scale)
+        torch.cuda.synchronize()
+        assert fa.last_device_error()[0] == 0
+        f = lambda x: inputs.bits_to_f64(x, w.dtype)
+        ref = oracle.attention_backward(f(bits["q"]), f(bits["k"]), f(bits["v"]), f(dout_bits),
+                                        w.scale, w.causal)
+        check_grads(w, [f(inputs.from_torch(g)) for g in grads], ref, w.name)

@@ -108,3 +108,30 @@ def test_fused_q_rotation_equals_the_two_pass_form(fa, w, form):
                            w.causal)
     parity.describe(w)
     parity.assert_parity(parity.compare(inputs.from_torch(fused), ref, w.dtype), False, w.name)
+
+
+@pytest.mark.parametrize("seed", range(2))
+def test_fused_rotation_random_shapes(fa, seed):
+    """Seeded random problems through fa_fwd_rope (Q rotated in the attention kernel, K by its
+    pass): equal bit for bit to the three-pass form, both pair forms, ragged shapes."""
+    rng = np.random.default_rng(3000 + seed)
+    for case in range(4):
+        D = int(rng.choice([64, 128]))
+        dtype = str(rng.choice(["f16", "bf16"]))
+        causal = bool(rng.integers(2))
+        form = int(rng.integers(2))
+        B, H = int(rng.integers(1, 4)), int(rng.integers(1, 4))
+        Nq, Nk = int(rng.integers(1, 701)), int(rng.integers(1, 701))
+        w = inputs.Workload(f"rope_random_{seed}_{case}", B, H, Nq, Nk, D, dtype, causal,
+                            seed=700 + seed * 10 + case)
+        bits = inputs.draw(w)
+        c, s = tables(max(Nq, Nk), D, offset=int(rng.integers(0, 1000)))
+        q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+        cq, sq = torch.from_numpy(c[:Nq]).cuda(), torch.from_numpy(s[:Nq]).cuda()
+        ck, sk = torch.from_numpy(c[:Nk]).cuda(), torch.from_numpy(s[:Nk]).cuda()
+        fused = fa.forward_rope(q, k, v, cq, sq, ck, sk, form=form, causal=causal, scale=w.scale)
+        two_pass = fa.forward(fa.rope(q, cq, sq, form=form), fa.rope(k, ck, sk, form=form), v,
+                              causal=causal, scale=w.scale)
+        torch.cuda.synchronize()
+        assert fa.last_device_error() == (0, 0)
+        assert torch.equal(fused.view(torch.int16), two_pass.view(torch.int16)), w.name
