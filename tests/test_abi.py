@@ -118,3 +118,25 @@ def test_checked_build_exports_the_same_interface(fa):
     assert dbg.fa_debug_bounds_selftest(None, None) == 1    # null buffer
     assert dbg.fa_debug_bounds_selftest(A + 2, None) == 3   # misaligned
     assert rel.fa_debug_bounds_report(None, None) == 1
+
+
+def test_workspaces_must_not_overlap_tensors(fa):
+    """Caller-owned workspaces of the split-KV, rotary and backward entries are rejected when they
+    overlap any tensor of the call (checked before any CUDA call, on fake addresses)."""
+    L = fa.lib()
+    B, H, N, D = 1, 2, 256, 128
+    t = B * H * N * D * 2  # bytes of one 16-bit tensor
+    q, k, v, o = A, A + t, A + 2 * t, A + 3 * t
+    ws_bad = A + t + 256  # starts inside K
+    need = L.fa_splitkv_workspace_bytes(B, H, N, N, D, 2)
+    assert L.fa_fwd_splitkv(q, k, v, o, None, B, H, N, N, D, 0.1, 2, 1, ws_bad, need, None) == 1
+    assert b"overlaps" in L.fa_last_error_message()
+    need = L.fa_rope_workspace_bytes(B, H, N, N, D)
+    tab = A + 16 * t
+    assert L.fa_fwd_rope(q, k, v, o, None, tab, tab, tab, tab, 0, B, H, N, N, D, 0.1, 0, 1,
+                         o + 256, need, None) == 1
+    need = L.fa_bwd_workspace_bytes(B, H, N)
+    lse, do, dq, dk, dv = A + 4 * t, A + 5 * t, A + 6 * t, A + 7 * t, A + 9 * t
+    assert L.fa_bwd(q, k, v, o, do, lse, dq, dk, dv, B, H, N, N, D, 0.1, 0, 1, dq + 512, need,
+                    None) == 1
+    assert b"overlaps" in L.fa_last_error_message()

@@ -936,6 +936,14 @@ fa_status fa_fwd_splitkv(const void* Q, const void* K, const void* V, void* O, f
                     need, plan.num_splits, workspace_bytes_given);
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
         return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+    {
+        const size_t qb = size_t(B * H) * size_t(Nq) * size_t(D) * 2;
+        const size_t kb = size_t(B * H) * size_t(Nk) * size_t(D) * 2;
+        if (overlaps(workspace, need, Q, qb) || overlaps(workspace, need, K, kb) ||
+            overlaps(workspace, need, V, kb) || overlaps(workspace, need, O, qb) ||
+            (LSE && overlaps(workspace, need, LSE, size_t(B * H) * size_t(Nq) * 4)))
+            return fail(FA_ERR_INVALID_ARGUMENT, "workspace overlaps a tensor");
+    }
     return launch_split(Q, K, V, O, LSE, B, H, Nq, Nk, D, scale, int(dtype), strm, plan, 0, units,
                         workspace);
 }
@@ -969,6 +977,14 @@ fa_status fa_fwd_rope(const void* Q, const void* K, const void* V, void* O, floa
         return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
     if (LSE && reinterpret_cast<uintptr_t>(LSE) % 4 != 0)
         return fail(FA_ERR_MISALIGNED, "LSE pointer is not 4-byte aligned");
+    {
+        const size_t qb = size_t(B * H) * size_t(Nq) * size_t(D) * 2;
+        const size_t kb = size_t(B * H) * size_t(Nk) * size_t(D) * 2;
+        if (overlaps(workspace, need, Q, qb) || overlaps(workspace, need, K, kb) ||
+            overlaps(workspace, need, V, kb) || overlaps(workspace, need, O, qb) ||
+            (LSE && overlaps(workspace, need, LSE, size_t(B * H) * size_t(Nq) * 4)))
+            return fail(FA_ERR_INVALID_ARGUMENT, "workspace overlaps a tensor");
+    }
     // K is rotated once by its own pass (every query block of a slice reads all of K); Q is
     // rotated inside the attention kernel, in shared memory, right after each tile's load.
     void* kr = workspace;
@@ -1020,6 +1036,12 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
         return fail(FA_ERR_INVALID_ARGUMENT, "workspace of %zu bytes needed (got %zu)", need, workspace_bytes_given);
     if (reinterpret_cast<uintptr_t>(workspace) % 256 != 0)
         return fail(FA_ERR_MISALIGNED, "workspace is not 256-byte aligned");
+    for (int a = 0; a < 6; ++a)
+        if (overlaps(workspace, need, ins[a], in_bytes[a]))
+            return fail(FA_ERR_INVALID_ARGUMENT, "workspace overlaps an input");
+    for (int a = 0; a < 3; ++a)
+        if (overlaps(workspace, need, outs[a], out_bytes[a]))
+            return fail(FA_ERR_INVALID_ARGUMENT, "workspace overlaps a gradient output");
     int dev = 0;
     int* err = nullptr;
     if ((s = device_state(&dev, &err)) != FA_OK) return s;
