@@ -245,7 +245,7 @@ def rotating_sets(w, dev):
     return bits, sets, set_bytes
 
 
-def time_extra(w, dev, stream, steps, warmup, peak, sampler=None):
+def time_extra(w, dev, stream, steps, warmup, peak, sampler=None, peak_burst=None):
     """One more workload timed the way the headline is (rotating inputs, W warm-up steps and about
     a second of the same work, then K steps between synchronizes with CUDA events on the
     launching stream, then the same K steps with the kernel timer on). Not part of `value`."""
@@ -297,6 +297,7 @@ def time_extra(w, dev, stream, steps, warmup, peak, sampler=None):
     del sets
     return {"workload": workload_desc(w), "flops_per_step": w.flops, "ms_per_step": ms,
             "tflops": tflops, "pct_of_measured_peak": 100 * tflops / peak,
+            "pct_of_measured_burst_peak": 100 * tflops / (peak_burst or peak),
             "kernel_ms": kernel_ms, "kernel_tflops": kernel_tflops,
             "kernel_frac": kernel_tflops / peak, "launches_per_step": sum(c for _, c in kernels.values()) / steps,
             "l2": f"{n} rotating input sets of {set_bytes / 2**20:.0f} MiB"}
@@ -437,7 +438,8 @@ def run_other_pass(args, w):
         separate = {"form": "fa_rope(Q), fa_rope(K), fa_fwd: three passes", "ms_per_step": ms_sep,
                     "tflops": work / (ms_sep * 1e-3) / 1e12}
     peaks, kind = load_peaks()
-    peak = float(peaks["bf16_tflops"] if unit == "TFLOP/s" else peaks["hbm_gbs"])
+    # Pre-heated like the forward pass: the sustained figure for tensor work.
+    peak = float(peaks["bf16_tflops_sustained"] if unit == "TFLOP/s" else peaks["hbm_gbs"])
     # Roofline of the dominant kernel: its work per step over its own event-timed device time.
     top = max(kernel_work, key=lambda k: kernels[k][0])
     top_ms = kernels[top][0] / args.steps
@@ -450,7 +452,8 @@ def run_other_pass(args, w):
                      "peak": peak, "unit": unit, "frac": achieved / peak, "kernel": top,
                      "kernel_ms_per_step": top_ms,
                      "kernels_ms_per_step": {k: v[0] / args.steps for k, v in kernels.items()},
-                     "peak_kind": f"{kind} " + ("bf16 dense (burst)" if unit == "TFLOP/s" else "copy bandwidth")},
+                     "peak_kind": f"{kind} " + ("bf16 dense, sustained" if unit == "TFLOP/s" else "copy bandwidth"),
+                     "frac_of_burst_peak": (achieved / float(peaks["bf16_tflops"])) if unit == "TFLOP/s" else None},
         "separate_passes": separate, "clocks": sampler.stop(),
         "gpu_launches": sum(n for _, n in kernels.values())}), flush=True)
     return 0
@@ -574,14 +577,18 @@ def main():
     # The other workloads the target names (L >= 4096, and causal prefill), timed the same way
     # while the clock sampler still runs.
     peaks, peaks_kind = load_peaks()
-    peak = float(peaks["bf16_tflops"])
+    # The timed steps run back to back after a second of the same work, in the power-capped
+    # steady state, like the sustained GEMM loop of the peak measurement: that is the denominator
+    # (the burst figure, taken on a cold GPU at its highest clocks, is reported beside it).
+    peak = float(peaks["bf16_tflops_sustained"])
+    peak_burst = float(peaks["bf16_tflops"])
     extra = {}
     if not args.profile and not args.no_extra and args.workload == "headline":
         del sets
         torch.cuda.empty_cache()
         for name in EXTRA_WORKLOADS:
             extra[name] = time_extra(inputs.WORKLOADS[name], dev, stream, args.steps, args.warmup,
-                                     peak, sampler)
+                                     peak, sampler, peak_burst)
             torch.cuda.empty_cache()
     clocks = sampler.stop() if sampler else None
     ms_total = max_over_ranks(ms_total, dev)
@@ -630,7 +637,9 @@ def main():
                 "kernels_ms_per_step": {k: v[0] / args.steps for k, v in kernels.items()},
                 "fwd_share_of_kernel_time": fwd_ms / all_ms if all_ms else None,
                 "frac": achieved / peak, "traffic": traffic, "traffic_source": traffic_src,
-                "peak_kind": f"{peaks_kind} bf16 dense (burst)",
+                "peak_kind": f"{peaks_kind} bf16 dense, sustained (the kernel is timed back to back "
+                             f"after 1 s of the same work, power-capped)",
+                "frac_of_burst_peak": achieved / peak_burst, "burst_peak": peak_burst,
                 "frac_of_datasheet": achieved / DATASHEET_DENSE_BF16_TFLOPS}
 
     cpu = None
@@ -649,6 +658,7 @@ def main():
                    "l2": f"{n_sets} rotating input sets of {set_bytes / 2**20:.0f} MiB "
                          f"(> L2 between consecutive steps)",
                    "pct_of_measured_peak": 100 * value / peak,
+                   "pct_of_measured_burst_peak": 100 * value / peak_burst,
                    "kernel_pct_of_measured_peak": 100 * achieved / peak,
                    "key_splits": args.splits if use_split else "auto",
                    "extra": extra or None},
