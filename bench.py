@@ -124,34 +124,101 @@ def profiled_traffic(workload_name: str):
         return None
 
 
+class _Nvml:
+    """Read-only NVML queries (SM clock, clock-event reasons, power draw) through the driver's
+    libnvidia-ml, for a sampling thread. The device is found by its UUID, so the index NVML uses
+    does not matter."""
+
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown"}
+
+    def __init__(self, uuid: str):
+        import ctypes
+
+        self.ct = ctypes
+        self.lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        if self.lib.nvmlDeviceGetHandleByUUID(uuid.encode(), ctypes.byref(self.handle)) != 0:
+            raise OSError(f"no NVML device with UUID {uuid}")
+        self.reasons_fn = (getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None)
+                           or self.lib.nvmlDeviceGetCurrentClocksThrottleReasons)
+
+    def sample(self):
+        ct = self.ct
+        clk, reasons, mw = ct.c_uint(), ct.c_ulonglong(), ct.c_uint()
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, 1, ct.byref(clk)) != 0:  # NVML_CLOCK_SM
+            raise OSError("nvmlDeviceGetClockInfo failed")
+        self.reasons_fn(self.handle, ct.byref(reasons))
+        self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(mw))
+        return float(clk.value), int(reasons.value), mw.value / 1000.0
+
+
+def gpu_uuid(dev) -> str | None:
+    import torch
+
+    u = getattr(torch.cuda.get_device_properties(dev), "uuid", None)
+    if u is None:
+        return None
+    u = str(u)
+    return u if u.startswith("GPU-") else "GPU-" + u
+
+
 class ClockSampler:
-    """nvidia-smi clock and throttle-reason samples while the GPU works. mark(name) opens a phase
-    (closing the previous one); stop() gives the median SM clock of the whole run and of each
-    phase, matched by the samples' own timestamps. Samples come every 100 ms: a timed phase of a
-    few milliseconds usually holds none, so each workload's 1 s pre-heat of the same work, right
-    before its timed steps, gives the clock they ran at."""
+    """Clock and throttle-reason samples while the GPU works, from two sources: nvidia-smi every
+    100 ms (timestamps, power, the reasons), and an NVML thread in this process every ~2 ms, so
+    that even a timed region of a few milliseconds holds samples. mark(name) opens a phase
+    (closing the previous one). stop(primary) gives per phase the median SM clock of each source,
+    and as `sm_mhz` the median NVML clock of the phase `<primary>:timed` (the timed steps of the
+    headline workload); failing that, its pre-heat's (a second of the same work just before)."""
 
     FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index: int):
+    def __init__(self, gpu_index: int, uuid: str | None = None):
+        import threading
+
         self.proc = None
-        self.phases = []  # (name, t_start, t_end) in epoch seconds
+        self.phases = []  # [name, epoch start, epoch end, perf start, perf end]
+        self.fast = []    # (perf_counter, sm MHz, reason bits, W)
+        self.nvml_error = None
         try:
             self.proc = subprocess.Popen(
-                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}",
+                ["nvidia-smi", f"--id={uuid or gpu_index}", f"--query-gpu={self.FIELDS}",
                  "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
+        self.nvml = None
+        if uuid is not None:
+            try:
+                self.nvml = _Nvml(uuid)
+            except OSError as e:
+                self.nvml_error = str(e)
+        self._halt = threading.Event()
+        self._thread = None
+        if self.nvml is not None:
+            self._thread = threading.Thread(target=self._loop, daemon=True)
+            self._thread.start()
+
+    def _loop(self):
+        while not self._halt.is_set():
+            t = time.perf_counter()
+            try:
+                self.fast.append((t, *self.nvml.sample()))
+            except OSError as e:
+                self.nvml_error = str(e)
+                return
+            self._halt.wait(0.002)
 
     def mark(self, name: str | None):
-        now = time.time()
+        now, perf = time.time(), time.perf_counter()
         if self.phases and self.phases[-1][2] is None:
-            self.phases[-1] = (self.phases[-1][0], self.phases[-1][1], now)
+            self.phases[-1][2], self.phases[-1][4] = now, perf
         if name is not None:
-            self.phases.append((name, now, None))
+            self.phases.append([name, now, None, perf, None])
 
     @staticmethod
     def _epoch(ts: str):
@@ -161,38 +228,58 @@ class ClockSampler:
         except ValueError:
             return None
 
-    def stop(self):
+    def stop(self, primary: str | None = None):
         self.mark(None)
-        if self.proc is None:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        self.proc.terminate()
-        try:
-            out, _ = self.proc.communicate(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-            out, _ = self.proc.communicate()
+        self._halt.set()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
         rows, reasons = [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for row in csv.reader(io.StringIO(out)):
-            if len(row) < 10:
-                continue
+        if self.proc is not None:
+            self.proc.terminate()
             try:
-                rows.append((self._epoch(row[0]), float(row[2]), float(row[3]), float(row[4])))
-            except ValueError:
-                continue
-            for name, val in zip(names, row[6:10]):
-                if val.strip().lower() == "active":
-                    reasons.add(name)
-        sm = [r[1] for r in rows]
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for row in csv.reader(io.StringIO(out)):
+                if len(row) < 10:
+                    continue
+                try:
+                    rows.append((self._epoch(row[0]), float(row[2]), float(row[3]), float(row[4])))
+                except ValueError:
+                    continue
+                for name, val in zip(names, row[6:10]):
+                    if val.strip().lower() == "active":
+                        reasons.add(name)
+        if not rows and not self.fast:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no clock samples"]}
         phases = {}
-        for name, t0, t1 in self.phases:
-            inside = [r[1] for r in rows if r[0] is not None and t0 <= r[0] <= (t1 or t0)]
-            phases[name] = {"sm_mhz": statistics.median(inside) if inside else None,
-                            "samples": len(inside), "seconds": (t1 or t0) - t0}
-        return {"sm_mhz": statistics.median(sm) if sm else None,
+        for name, t0, t1, p0, p1 in self.phases:
+            smi = [r[1] for r in rows if r[0] is not None and t0 <= r[0] <= t1]
+            fast = [f for f in self.fast if p0 <= f[0] <= p1]
+            for f in fast:
+                reasons.update(n for bit, n in _Nvml.REASONS.items() if f[2] & bit)
+            phases[name] = {"sm_mhz": statistics.median(smi) if smi else None, "samples": len(smi),
+                            "sm_mhz_nvml": statistics.median(f[1] for f in fast) if fast else None,
+                            "nvml_samples": len(fast),
+                            "sm_mhz_nvml_min": min(f[1] for f in fast) if fast else None,
+                            "seconds": t1 - t0}
+        sm_mhz, source = None, None
+        if primary is not None:
+            timed, pre = phases.get(f"{primary}:timed"), phases.get(f"{primary}:preheat")
+            if timed and timed["sm_mhz_nvml"] is not None:
+                sm_mhz, source = timed["sm_mhz_nvml"], f"{primary}:timed, NVML every ~2 ms"
+            elif pre and (pre["sm_mhz_nvml"] or pre["sm_mhz"]) is not None:
+                sm_mhz = pre["sm_mhz_nvml"] or pre["sm_mhz"]
+                source = f"{primary}:preheat (the second of the same work before the timed steps)"
+        all_smi = [r[1] for r in rows]
+        return {"sm_mhz": sm_mhz, "sm_mhz_source": source,
+                "sm_mhz_all_samples": statistics.median(all_smi) if all_smi else None,
                 "sm_max_mhz": max(r[2] for r in rows) if rows else None,
                 "power_w_max": max(r[3] for r in rows) if rows else None,
-                "samples": len(sm), "reasons": sorted(reasons), "phases": phases}
+                "samples": len(all_smi), "nvml_samples": len(self.fast),
+                "nvml_error": self.nvml_error, "reasons": sorted(reasons), "phases": phases}
 
 
 class OracleSample:
@@ -399,19 +486,20 @@ def run_other_pass(args, w):
     torch.cuda.synchronize(dev)
     # About a second of the same work first, as for the forward pass, so that the timed steps
     # run at the clock this load settles to.
-    sampler = ClockSampler(dev.index)
+    sampler = ClockSampler(dev.index, gpu_uuid(dev))
     sampler.mark(f"{w.name}:preheat")
     t_end = time.perf_counter() + 1.0
     while time.perf_counter() < t_end:
         step()
         torch.cuda.synchronize(dev)
-    sampler.mark(None)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler.mark(f"{w.name}:timed")
     e0.record(stream)
     for _ in range(args.steps):
         step()
     e1.record(stream)
     torch.cuda.synchronize(dev)
+    sampler.mark(None)
     # Per-kernel device times from a second pass with the library's kernel timer on (its events
     # add small gaps between launches, so it stays out of the timed region).
     fa.timer_start()
@@ -426,17 +514,25 @@ def run_other_pass(args, w):
     value = work / (ms * 1e-3) / (1e12 if unit == "TFLOP/s" else 1e9)
     separate = None
     if args.which == "rope_fwd":
+        # The two forms alternate in blocks of K steps (6 rounds), so that both see the same
+        # clocks under the power cap; the medians are compared.
         for _ in range(args.warmup):
             step_separate()
         torch.cuda.synchronize(dev)
-        e0.record(stream)
-        for _ in range(args.steps):
-            step_separate()
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        ms_sep = e0.elapsed_time(e1) / args.steps
-        separate = {"form": "fa_rope(Q), fa_rope(K), fa_fwd: three passes", "ms_per_step": ms_sep,
-                    "tflops": work / (ms_sep * 1e-3) / 1e12}
+        blocks = {"fused": [], "separate": []}
+        for _ in range(6):
+            for form, fn in (("fused", step), ("separate", step_separate)):
+                e0.record(stream)
+                for _ in range(args.steps):
+                    fn()
+                e1.record(stream)
+                torch.cuda.synchronize(dev)
+                blocks[form].append(e0.elapsed_time(e1) / args.steps)
+        med = {f: float(np.median(v)) for f, v in blocks.items()}
+        separate = {"form": "fa_rope(Q), fa_rope(K), fa_fwd: three passes",
+                    "ms_per_step": med["separate"], "tflops": work / (med["separate"] * 1e-3) / 1e12,
+                    "interleaved_rounds": 6, "fused_ms_per_step_interleaved": med["fused"],
+                    "fused_over_separate_time": med["fused"] / med["separate"]}
     peaks, kind = load_peaks()
     # Pre-heated like the forward pass: the sustained figure for tensor work.
     peak = float(peaks["bf16_tflops_sustained"] if unit == "TFLOP/s" else peaks["hbm_gbs"])
@@ -454,7 +550,7 @@ def run_other_pass(args, w):
                      "kernels_ms_per_step": {k: v[0] / args.steps for k, v in kernels.items()},
                      "peak_kind": f"{kind} " + ("bf16 dense, sustained" if unit == "TFLOP/s" else "copy bandwidth"),
                      "frac_of_burst_peak": (achieved / float(peaks["bf16_tflops"])) if unit == "TFLOP/s" else None},
-        "separate_passes": separate, "clocks": sampler.stop(),
+        "separate_passes": separate, "clocks": sampler.stop(w.name),
         "gpu_launches": sum(n for _, n in kernels.values())}), flush=True)
     return 0
 
@@ -538,7 +634,7 @@ def main():
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize(dev)
-    sampler = ClockSampler(dev.index) if not args.profile else None
+    sampler = ClockSampler(dev.index, gpu_uuid(dev)) if not args.profile else None
     if sampler:
         sampler.mark(f"{w.name}:preheat")
     t_end = time.perf_counter() + (0.0 if args.profile else 1.0)
@@ -590,7 +686,7 @@ def main():
             extra[name] = time_extra(inputs.WORKLOADS[name], dev, stream, args.steps, args.warmup,
                                      peak, sampler, peak_burst)
             torch.cuda.empty_cache()
-    clocks = sampler.stop() if sampler else None
+    clocks = sampler.stop(w.name) if sampler else None
     ms_total = max_over_ranks(ms_total, dev)
     ms_per_step = ms_total / args.steps
     value = job_throughput(w.flops, world, ms_per_step * 1e-3)

@@ -1,5 +1,5 @@
 """Host-side logic of bench.py that needs no GPU: which profile summary's DRAM traffic the
-roofline line may quote."""
+roofline line may quote, and how the clock record is summarised."""
 import importlib.util
 import pathlib
 import sys
@@ -36,7 +36,7 @@ def test_committed_headline_profile_matches_the_kernel_code():
     b = _bench()
     traffic = b.profiled_traffic("headline")
     if traffic is None:
-        pytest.skip("profiles/fa_fwd_kernel_headline.md predates the kernel code: re-take it")
+        pytest.skip("the committed ncu summary of the headline launch predates the kernel code")
     # Q, K, V read once and O written once at the headline shape: 134.2 MB; the summary's DRAM
     # bytes lie between the reads alone and that.
     assert 100e6 < traffic <= 135e6
@@ -54,3 +54,29 @@ def test_profile_summary_with_another_hash_is_ignored(tmp_path, monkeypatch):
         (tmp_path / s).write_text((ROOT / s).read_text())
     monkeypatch.setattr(b, "ROOT", tmp_path)
     assert b.profiled_traffic("headline") is None
+
+
+def test_clock_record_takes_the_timed_phase(monkeypatch):
+    """The line's sm_mhz is the median fast (NVML) sample inside the headline's timed phase; with
+    no sample there, the pre-heat's; throttle reasons seen inside any phase are listed."""
+    b = _bench()
+
+    def no_smi(*a, **k):
+        raise OSError("nvidia-smi is not started in this test")
+
+    monkeypatch.setattr(b.subprocess, "Popen", no_smi)  # only injected samples are summarised
+    c = b.ClockSampler(0, None)
+    c.phases = [["headline:preheat", 0.0, 1.0, 10.0, 11.0], ["headline:timed", 1.0, 1.01, 11.0, 11.01]]
+    c.fast = [(10.2, 1900.0, 0x4, 1300.0), (10.6, 1920.0, 0x4, 1350.0),
+              (11.002, 1950.0, 0x0, 1200.0), (11.006, 1960.0, 0x8, 1200.0), (11.008, 1955.0, 0, 1.0),
+              (12.0, 2070.0, 0x1, 100.0)]
+    r = c.stop("headline")
+    assert r["sm_mhz"] == 1955.0 and "timed" in r["sm_mhz_source"]
+    assert r["phases"]["headline:preheat"]["sm_mhz_nvml"] == 1910.0
+    assert r["phases"]["headline:timed"]["nvml_samples"] == 3
+    assert r["reasons"] == ["hw_slowdown", "sw_power_cap"]
+    c2 = b.ClockSampler(0, None)
+    c2.phases = [["headline:preheat", 0.0, 1.0, 10.0, 11.0], ["headline:timed", 1.0, 1.01, 11.0, 11.01]]
+    c2.fast = [(10.5, 1880.0, 0x4, 1300.0)]
+    r2 = c2.stop("headline")
+    assert r2["sm_mhz"] == 1880.0 and "preheat" in r2["sm_mhz_source"]
