@@ -245,8 +245,9 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
  * `stream`: while one chunk computes, the next is copied in and the previous copied out. Each
  * chunk is one attention launch (no key split). The device staging buffers grow to the
  * largest request seen and are kept until process exit (or fa_release_host_buffers); the
- * streams live until process exit. Not thread-safe: concurrent calls from several host
- * threads must be serialised by the caller. On an error the contents of O are undefined.
+ * streams live until process exit. Calls from several host threads on one device run one after
+ * another (a per-device lock held for the whole call, which is synchronous anyway). On an error
+ * the contents of O are undefined.
  */
 fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int64_t B,
                       int64_t H, int64_t Nq, int64_t Nk, int64_t D, float scale, int causal,

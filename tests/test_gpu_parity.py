@@ -271,6 +271,48 @@ def test_host_buffer_pipeline_uneven_chunks(fa):
     assert np.array_equal(inputs.from_torch(oh), dev)
 
 
+def test_host_buffer_entry_from_two_threads(fa):
+    """fa_fwd_host from two host threads at once, with shapes that make the shared staging buffer
+    grow between calls: the calls run one after another, and each result equals the device
+    entry's bit for bit."""
+    import threading
+
+    ws = [inputs.Workload("host_t0", 1, 6, 700, 900, 128, "bf16", False, seed=14),
+          inputs.Workload("host_t1", 2, 5, 1500, 1300, 64, "f16", True, seed=15)]
+    cases = []
+    try:
+        fa.set_tail_split(False)  # the host entry runs each chunk as one launch, unsplit
+        for w in ws:
+            bits = inputs.draw(w)
+            dev = inputs.from_torch(run_gpu(fa, bits, w))
+            host = [inputs.to_torch(bits[n], w.dtype).pin_memory() for n in "qkv"]
+            cases.append((w, dev, host))
+    finally:
+        fa.set_tail_split(True)
+    fa.release_host_buffers()
+    errors, outs = [], {}
+
+    def worker(i):
+        w, _, (qh, kh, vh) = cases[i]
+        try:
+            for r in range(3):
+                oh = torch.empty_like(qh).pin_memory()
+                fa.forward_host(qh, kh, vh, oh, causal=w.causal, scale=w.scale)
+                outs[(i, r)] = inputs.from_torch(oh)
+        except Exception as e:  # noqa: BLE001 - reported below
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=300)
+    assert not errors, errors
+    for (i, r), o in outs.items():
+        assert np.array_equal(o, cases[i][1]), (i, r)
+    assert len(outs) == 6
+
+
 def test_long_context_chunk_full_size(fa, orc):
     """128 queries against 65536 keys: sampled rows of two heads against the oracle, from the
     split-KV entry, from the default entry (which splits the 8 units over keys by itself) and

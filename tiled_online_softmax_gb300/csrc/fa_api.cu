@@ -376,6 +376,9 @@ struct Staging {
     size_t bytes = 0;
 };
 Staging g_staging[MAX_DEVICES];
+// Held for the whole of an fa_fwd_host call (and by fa_release_host_buffers): calls from several
+// host threads on one device run one after another over the shared staging buffer and streams.
+std::mutex g_host_mu[MAX_DEVICES];
 
 // Streams and events of fa_fwd_host's copy/compute pipeline, per device, made on first use.
 constexpr int HOST_PIPE_STREAMS = 3;
@@ -1114,6 +1117,7 @@ fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int6
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
     if (dev < 0 || dev >= MAX_DEVICES) return fail(FA_ERR_UNSUPPORTED, "device index %d", dev);
+    std::lock_guard<std::mutex> host_lock(g_host_mu[dev]);
     const size_t q_bytes = size_t(B * H) * size_t(Nq) * size_t(D) * 2;
     const size_t kv_bytes = size_t(B * H) * size_t(Nk) * size_t(D) * 2;
     auto round_up = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -1189,7 +1193,9 @@ fa_status fa_release_host_buffers(void) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (dev >= 0 && dev < MAX_DEVICES && g_staging[dev].buf) {
+    if (dev < 0 || dev >= MAX_DEVICES) return FA_OK;
+    std::lock_guard<std::mutex> host_lock(g_host_mu[dev]);
+    if (g_staging[dev].buf) {
         e = cudaFree(g_staging[dev].buf);
         g_staging[dev] = Staging{};
         if (e != cudaSuccess) return cuda_fail(e, "cudaFree(staging)");

@@ -380,6 +380,14 @@ def forward_host(q, k, v, out, causal: bool = False, scale: float | None = None,
     return out
 
 
+def release_host_buffers(device: int = 0) -> None:
+    """Free the device staging buffers forward_host() keeps on `device`."""
+    import torch
+
+    with torch.cuda.device(device):
+        _raise_if(lib().fa_release_host_buffers())
+
+
 def last_device_error(stream=None) -> tuple[int, int]:
     """Synchronise `stream` and return (status, wait-site code) of the device error word."""
     import torch
