@@ -8,6 +8,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstdlib>
+#include <atomic>
 #include <cstring>
 #include <mutex>
 #include <utility>
@@ -75,14 +76,13 @@ void timer_end(cudaStream_t s, int i) {
 }
 
 unsigned g_attr_set[MAX_DEVICES] = {};     // bit per kernel instance: smem attribute applied
-float g_rescale_threshold = 32.0f;         // lazy-rescale threshold (log2 units)
+std::atomic<float> g_rescale_threshold{32.0f};  // lazy-rescale threshold (log2 units)
 // fp16 weights P <= 2^threshold must stay below the fp16 maximum (65504 < 2^16); bf16 has
 // fp32's exponent range, and the fp32 accumulators O and l hold far larger values.
 constexpr float FP16_RESCALE_THRESHOLD_MAX = 15.0f;
 float rescale_threshold_for(int dtype) {
-    return dtype == FA_F16 && g_rescale_threshold > FP16_RESCALE_THRESHOLD_MAX
-               ? FP16_RESCALE_THRESHOLD_MAX
-               : g_rescale_threshold;
+    const float t = g_rescale_threshold.load(std::memory_order_relaxed);
+    return dtype == FA_F16 && t > FP16_RESCALE_THRESHOLD_MAX ? FP16_RESCALE_THRESHOLD_MAX : t;
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
@@ -594,7 +594,7 @@ struct WsPool {
     WsSlot slot[WS_SLOTS];
 };
 WsPool g_ws_pool[MAX_DEVICES];
-bool g_tail_split = true;
+std::atomic<bool> g_tail_split{true};
 
 // Set up the pool of device `dev` (g_mutex held). False if it cannot be now (that call runs
 // unsplit).
@@ -1104,7 +1104,7 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
 
 fa_status fa_set_tail_split(int enable) {
     if (enable != 0 && enable != 1) return fail(FA_ERR_INVALID_ARGUMENT, "enable must be 0 or 1");
-    g_tail_split = enable != 0;
+    g_tail_split.store(enable != 0, std::memory_order_relaxed);
     return FA_OK;
 }
 
@@ -1284,8 +1284,14 @@ fa_status fa_last_device_error(void* stream, int* site) {
     // The error word of the ordinary entry points, then the record of fa_fwd_noalloc (the static
     // array, reached through the device address looked up on that entry's first call). Reading
     // and clearing either allocates nothing.
+    int* words[2];
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);  // both are set up under this lock
+        words[0] = g_err_word[dev];
+        words[1] = g_noalloc_addr[dev];
+    }
     int word = 0;
-    for (int* w : {g_err_word[dev], g_noalloc_addr[dev]}) {
+    for (int* w : words) {
         if (!w) continue;
         int x = 0;
         if ((e = cudaMemcpy(&x, w, sizeof(int), cudaMemcpyDeviceToHost)) != cudaSuccess)
@@ -1352,10 +1358,10 @@ fa_status fa_set_rescale_threshold(float log2_threshold) {
     if (!std::isfinite(log2_threshold) || log2_threshold < 0.f || log2_threshold > 64.f)
         return fail(FA_ERR_INVALID_ARGUMENT, "rescale threshold must be in [0, 64], got %g",
                     double(log2_threshold));
-    g_rescale_threshold = log2_threshold;
+    g_rescale_threshold.store(log2_threshold, std::memory_order_relaxed);
     return FA_OK;
 }
 
-float fa_get_rescale_threshold(void) { return g_rescale_threshold; }
+float fa_get_rescale_threshold(void) { return g_rescale_threshold.load(std::memory_order_relaxed); }
 
 }  // extern "C"
