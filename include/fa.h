@@ -241,8 +241,9 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
  * Q, K, V, O are host pointers with the layout above (pinned memory gives full copy speed and
  * lets copies overlap the computation). The call copies Q, K, V to device memory owned by
  * libfa, computes, copies O back and returns when O is complete. The (batch, head) slices are
- * processed in up to 6 chunks on three libfa-owned streams, ordered after the work already on
- * `stream`: while one chunk computes, the next is copied in and the previous copied out. Each
+ * processed in up to 6 chunks on libfa-owned streams, ordered after the work already on
+ * `stream`: one stream copies the chunks' inputs in back to back, two run each chunk's attention
+ * once its inputs are there, one copies each chunk's output back once it is complete. Each
  * chunk is one attention launch (no key split). The device staging buffers grow to the
  * largest request seen and are kept until process exit (or fa_release_host_buffers); the
  * streams live until process exit. Calls from several host threads on one device run one after

@@ -380,27 +380,48 @@ Staging g_staging[MAX_DEVICES];
 // host threads on one device run one after another over the shared staging buffer and streams.
 std::mutex g_host_mu[MAX_DEVICES];
 
-// Streams and events of fa_fwd_host's copy/compute pipeline, per device, made on first use.
-constexpr int HOST_PIPE_STREAMS = 3;
+// Streams and events of fa_fwd_host's copy/compute pipeline, per device, made on first use:
+// one stream copies every chunk's inputs in, back to back; two run the chunks' attention; one
+// copies every chunk's output back. Per chunk, one event marks its inputs on the device and one
+// its output complete, so no copy waits behind another chunk's computation or copy-out.
+constexpr int HOST_PIPE_COMPUTE = 2;
+constexpr int HOST_PIPE_MAX_CHUNKS = 16;
+constexpr int64_t HOST_CHUNKS = 6;  // chunks of (batch, head) slices per call, at most the above
+static_assert(HOST_CHUNKS <= HOST_PIPE_MAX_CHUNKS, "one pair of events per chunk");
 struct HostPipe {
     bool ready = false;
-    cudaStream_t s[HOST_PIPE_STREAMS] = {};
+    cudaStream_t in = nullptr, out = nullptr;
+    cudaStream_t comp[HOST_PIPE_COMPUTE] = {};
     cudaEvent_t start = nullptr;
-    cudaEvent_t done[HOST_PIPE_STREAMS] = {};
+    cudaEvent_t copied[HOST_PIPE_MAX_CHUNKS] = {};
+    cudaEvent_t computed[HOST_PIPE_MAX_CHUNKS] = {};
+    cudaEvent_t done_in = nullptr, done_out = nullptr;
+    cudaEvent_t done_comp[HOST_PIPE_COMPUTE] = {};
 };
 HostPipe g_host_pipe[MAX_DEVICES];
 
 fa_status host_pipe(int dev, HostPipe** out) {
     HostPipe& hp = g_host_pipe[dev];
     if (!hp.ready) {
-        cudaError_t e;
-        for (int i = 0; i < HOST_PIPE_STREAMS; ++i) {
-            if ((e = cudaStreamCreateWithFlags(&hp.s[i], cudaStreamNonBlocking)) != cudaSuccess ||
-                (e = cudaEventCreateWithFlags(&hp.done[i], cudaEventDisableTiming)) != cudaSuccess)
-                return cuda_fail(e, "host pipeline streams");
+        cudaError_t e = cudaSuccess;
+        auto stream = [&](cudaStream_t* x) {
+            if (e == cudaSuccess) e = cudaStreamCreateWithFlags(x, cudaStreamNonBlocking);
+        };
+        auto event = [&](cudaEvent_t* x) {
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(x, cudaEventDisableTiming);
+        };
+        stream(&hp.in);
+        stream(&hp.out);
+        for (auto& x : hp.comp) stream(&x);
+        event(&hp.start);
+        event(&hp.done_in);
+        event(&hp.done_out);
+        for (auto& x : hp.done_comp) event(&x);
+        for (int c = 0; c < HOST_PIPE_MAX_CHUNKS; ++c) {
+            event(&hp.copied[c]);
+            event(&hp.computed[c]);
         }
-        if ((e = cudaEventCreateWithFlags(&hp.start, cudaEventDisableTiming)) != cudaSuccess)
-            return cuda_fail(e, "host pipeline event");
+        if (e != cudaSuccess) return cuda_fail(e, "host pipeline streams and events");
         hp.ready = true;
     }
     *out = &hp;
@@ -1141,13 +1162,12 @@ fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int6
         std::lock_guard<std::mutex> lock(g_mutex);
         if ((s = host_pipe(dev, &hp)) != FA_OK) return s;
     }
-    // The (batch, head) slices are independent: in chunks of slices, the copy of chunk c + 1 in,
-    // the attention on chunk c and the copy of chunk c - 1 out run at the same time (the copy
-    // engines of the two directions and the SMs work in parallel). Chunks go round-robin over
-    // three streams; each stream copies in, computes and copies out its chunks in order.
+    // The (batch, head) slices are independent: in chunks of slices, the inputs of every chunk
+    // are copied in back to back on one stream (the link's bound), each chunk's attention runs as
+    // soon as its inputs are there, and its output is copied back while later chunks' inputs are
+    // still coming in (the two directions of the link work at once).
     const int64_t bh = B * H;
-    // Six chunks measured best on the headline shape (8: 5 % slower, 16: 10 % slower, 4: 2 %).
-    const int64_t chunks = bh < 6 ? bh : 6;
+    const int64_t chunks = bh < HOST_CHUNKS ? bh : HOST_CHUNKS;
     const int64_t per = (bh + chunks - 1) / chunks;
     const size_t q_slice = size_t(Nq) * size_t(D) * 2, kv_slice = size_t(Nk) * size_t(D) * 2;
     auto* hq = static_cast<const uint8_t*>(Q);
@@ -1158,33 +1178,42 @@ fa_status fa_fwd_host(const void* Q, const void* K, const void* V, void* O, int6
     // After an error part-way through, copies and launches already queued on the pipeline
     // streams would keep using the staging buffer and O: wait for them before returning.
     auto drain = [&](fa_status st) {
-        for (int i = 0; i < HOST_PIPE_STREAMS; ++i) cudaStreamSynchronize(hp->s[i]);
+        cudaStreamSynchronize(hp->in);
+        for (auto x : hp->comp) cudaStreamSynchronize(x);
+        cudaStreamSynchronize(hp->out);
         return st;
     };
-    for (int i = 0; i < HOST_PIPE_STREAMS; ++i)
-        if ((e = cudaStreamWaitEvent(hp->s[i], hp->start, 0)) != cudaSuccess)
+    for (cudaStream_t x : {hp->in, hp->comp[0], hp->comp[1], hp->out})
+        if ((e = cudaStreamWaitEvent(x, hp->start, 0)) != cudaSuccess)
             return drain(cuda_fail(e, "cudaStreamWaitEvent"));
     for (int64_t c0 = 0, c = 0; c0 < bh; c0 += per, ++c) {
         const int64_t n = (bh - c0 < per) ? bh - c0 : per;
-        cudaStream_t x = hp->s[c % HOST_PIPE_STREAMS];
         const size_t qo = size_t(c0) * q_slice, ko = size_t(c0) * kv_slice;
-        if ((e = cudaMemcpyAsync(dq + qo, hq + qo, size_t(n) * q_slice, cudaMemcpyHostToDevice, x)) != cudaSuccess ||
-            (e = cudaMemcpyAsync(dk + ko, hk + ko, size_t(n) * kv_slice, cudaMemcpyHostToDevice, x)) != cudaSuccess ||
-            (e = cudaMemcpyAsync(dv + ko, hv + ko, size_t(n) * kv_slice, cudaMemcpyHostToDevice, x)) != cudaSuccess)
+        cudaStream_t x = hp->comp[c % HOST_PIPE_COMPUTE];
+        if ((e = cudaMemcpyAsync(dq + qo, hq + qo, size_t(n) * q_slice, cudaMemcpyHostToDevice, hp->in)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(dk + ko, hk + ko, size_t(n) * kv_slice, cudaMemcpyHostToDevice, hp->in)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(dv + ko, hv + ko, size_t(n) * kv_slice, cudaMemcpyHostToDevice, hp->in)) != cudaSuccess ||
+            (e = cudaEventRecord(hp->copied[c], hp->in)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(x, hp->copied[c], 0)) != cudaSuccess)
             return drain(cuda_fail(e, "cudaMemcpyAsync(host to device)"));
-        // One launch per chunk, without the key split (the chunks run concurrently on three
-        // streams, each a whole-GPU-sized piece of work already).
+        // One launch per chunk, without the key split (chunks may run at the same time on the
+        // two compute streams).
         s = launch(dq + qo, dk + ko, dv + ko, dout + qo, nullptr, 1, n, Nq, Nk, D, scale, causal,
                    int(dtype), x);
         if (s != FA_OK) return drain(s);
-        if ((e = cudaMemcpyAsync(ho + qo, dout + qo, size_t(n) * q_slice, cudaMemcpyDeviceToHost, x)) != cudaSuccess)
+        if ((e = cudaEventRecord(hp->computed[c], x)) != cudaSuccess ||
+            (e = cudaStreamWaitEvent(hp->out, hp->computed[c], 0)) != cudaSuccess ||
+            (e = cudaMemcpyAsync(ho + qo, dout + qo, size_t(n) * q_slice, cudaMemcpyDeviceToHost, hp->out)) != cudaSuccess)
             return drain(cuda_fail(e, "cudaMemcpyAsync(device to host)"));
     }
-    for (int i = 0; i < HOST_PIPE_STREAMS; ++i) {
-        if ((e = cudaEventRecord(hp->done[i], hp->s[i])) != cudaSuccess ||
-            (e = cudaStreamWaitEvent(strm, hp->done[i], 0)) != cudaSuccess)
+    if ((e = cudaEventRecord(hp->done_in, hp->in)) != cudaSuccess ||
+        (e = cudaEventRecord(hp->done_comp[0], hp->comp[0])) != cudaSuccess ||
+        (e = cudaEventRecord(hp->done_comp[1], hp->comp[1])) != cudaSuccess ||
+        (e = cudaEventRecord(hp->done_out, hp->out)) != cudaSuccess)
+        return drain(cuda_fail(e, "host pipeline join"));
+    for (cudaEvent_t ev : {hp->done_in, hp->done_comp[0], hp->done_comp[1], hp->done_out})
+        if ((e = cudaStreamWaitEvent(strm, ev, 0)) != cudaSuccess)
             return drain(cuda_fail(e, "host pipeline join"));
-    }
     if ((e = cudaStreamSynchronize(strm)) != cudaSuccess) return drain(cuda_fail(e, "cudaStreamSynchronize"));
     return FA_OK;
 }
