@@ -136,6 +136,9 @@ struct Params {
     // fp32 output (null: none): O / l written unrounded as fp32 [bh][nq][D] instead of the
     // 16-bit O, to check the arithmetic apart from the output rounding.
     float* o_f32;
+    // CTAs below this index (the first wave) prefetch their first tiles into L2 before waiting
+    // for the previous kernel (0: none).
+    int prefetch_ctas;
 };
 
 template <int D>
@@ -655,6 +658,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tensormap(&tm_k);
         ptx::prefetch_tensormap(&tm_v);
         ptx::prefetch_tensormap(&tm_o);
+        // A first-wave CTA of a dependent launch starts while the previous kernel finishes and
+        // waits for it below. Prefetching its first Q, K and V tiles into L2 first overlaps their
+        // DRAM latency with that wait. The prefetch moves no data into the SM, and L2 holds the
+        // one coherent copy of global memory, so it cannot make a later load see anything older
+        // than what the previous kernel writes.
+        if (static_cast<int>(blockIdx.x) < p.prefetch_ctas) {
+            for (int c = 0; c < L::COL_BLOCKS; ++c) {
+                ptx::tma_prefetch_3d(&tm_q, c * 64, q0, bh);
+                ptx::tma_prefetch_3d(&tm_k, c * 64, kv0 * BN, bh);
+                ptx::tma_prefetch_3d(&tm_v, c * 64, kv0 * BN, bh);
+                ptx::tma_prefetch_3d(&tm_q, c * 64, q0 + BM, bh);
+            }
+        }
     }
     if (warp == MMA_WARP) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);

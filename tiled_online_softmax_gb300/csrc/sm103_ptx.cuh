@@ -88,6 +88,16 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
 
 // TMA: 3-D tiled tensor store from shared memory (bulk-group completion). Out-of-bounds parts of
 // the box are not written.
+// L2 prefetch of one box of a tiled tensor: a hint that brings the lines into L2; no data reaches
+// the SM and nothing completes on a barrier.
+__device__ __forceinline__ void tma_prefetch_3d(const CUtensorMap* map, int32_t c0, int32_t c1,
+                                                int32_t c2) {
+    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];" ::"l"(
+                     reinterpret_cast<uint64_t>(map)),
+                 "r"(c0), "r"(c1), "r"(c2)
+                 : "memory");
+}
+
 __device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, uint32_t src, int32_t c0,
                                              int32_t c1, int32_t c2) {
     asm volatile(
