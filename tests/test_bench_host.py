@@ -80,3 +80,13 @@ def test_clock_record_takes_the_timed_phase(monkeypatch):
     c2.fast = [(10.5, 1880.0, 0x4, 1300.0)]
     r2 = c2.stop("headline")
     assert r2["sm_mhz"] == 1880.0 and "preheat" in r2["sm_mhz_source"]
+
+
+def test_kernel_time_of_single_and_split_steps():
+    """One attention launch per step: the kernel's time is the timed region's per-step time. Two
+    launches per step (attention and merge): the per-launch events of the kernel timer."""
+    b = _bench()
+    ms, src, per_launch = b.kernel_time({"fwd": (35.0, 50), "merge": (0.0, 0)}, 0.6, 50)
+    assert ms == 0.6 and "over the timed region" in src and per_launch == 0.7
+    ms, src, per_launch = b.kernel_time({"fwd": (8.8, 50), "merge": (0.5, 50)}, 0.18, 50)
+    assert ms == per_launch == 8.8 / 50 and "around each attention launch" in src
