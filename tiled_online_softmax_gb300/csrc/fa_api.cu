@@ -361,6 +361,10 @@ fa_status launch(const void* Q, const void* K, const void* V, void* O, float* LS
     // prefetch switched at run time); non-causal shapes, whose first wave fetches the same K and V
     // tiles many times over, took 0.5-0.8 % more (also with Q alone prefetched).
     p.prefetch_ctas = causal ? g_num_sms[dev] : 0;
+    // Every CTA prefetches the first tiles of the CTA one wave later once its own loads are
+    // issued: 0.8-1.0 % less time at the headline shape, 0.65 % on causal prefill (same binary
+    // switched at run time, 40 rounds).
+    p.next_prefetch_stride = g_num_sms[dev];
     const bool bf16 = dtype == FA_BF16;
     const int inst = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
     switch (inst) {
@@ -841,6 +845,11 @@ fa_status fa_fwd_noalloc(const void* Q, const void* K, const void* V, void* O, i
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.rescale_threshold = rescale_threshold_for(int(dtype));
     p.timeout_ns = wait_timeout_ns();
+    {
+        std::lock_guard<std::mutex> lock(g_mutex);
+        p.prefetch_ctas = causal ? g_num_sms[dev] : 0;  // as in launch()
+        p.next_prefetch_stride = g_num_sms[dev];
+    }
     const int inst = (D == 128 ? 4 : 0) + (dtype == FA_BF16 ? 2 : 0) + (causal ? 1 : 0);
     switch (inst) {
         case 0: return launch_instance<64, false, false>(dev, inst, mq, mk, mv, mo, p, strm);

@@ -139,6 +139,9 @@ struct Params {
     // CTAs below this index (the first wave) prefetch their first tiles into L2 before waiting
     // for the previous kernel (0: none).
     int prefetch_ctas;
+    // After issuing its last loads, each CTA prefetches into L2 the first tiles of CTA
+    // blockIdx.x + next_prefetch_stride, one wave later (0: none).
+    int next_prefetch_stride;
 };
 
 template <int D>
@@ -585,6 +588,29 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
 }
 
 // ---------------------------------------------------------------------------------------------
+// work unit of CTA b: slice bh, unit u (query rows u * 256 ...), key range split (-1: all keys).
+// Causal: the longest units first, spread over all slices; otherwise the units of one slice are
+// adjacent so its K/V stay hot in L2, and the units from split_begin on run as num_splits CTAs.
+// ---------------------------------------------------------------------------------------------
+template <bool CAUSAL>
+__device__ __forceinline__ void unit_of_cta(int b, const Params& p, int& bh, int& u, int& split) {
+    split = -1;
+    if constexpr (CAUSAL) {
+        bh = b % p.bh;
+        u = p.num_units - 1 - b / p.bh;
+    } else {
+        int unit = b;
+        if (unit >= p.split_begin) {
+            const int idx = unit - p.split_begin;
+            unit = p.split_begin + idx / p.num_splits;
+            split = idx % p.num_splits;
+        }
+        u = unit % p.num_units;
+        bh = unit / p.num_units;
+    }
+}
+
+// ---------------------------------------------------------------------------------------------
 // the kernel
 // ---------------------------------------------------------------------------------------------
 template <int D, bool BF16, bool CAUSAL>
@@ -606,23 +632,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int lane = threadIdx.x & 31;
     const int wg = warp >> 2;
 
-    // Work unit. Causal: the longest units first, spread over all slices; otherwise the units of
-    // one slice are adjacent so its K/V stay hot in L2.
-    int bh, u, split = -1;  // split < 0: the whole key range, O written directly
+    // Work unit (split < 0: the whole key range, O written directly).
+    int bh, u, split;
+    unit_of_cta<CAUSAL>(static_cast<int>(blockIdx.x), p, bh, u, split);
     const int nkt = (p.nk + BN - 1) / BN;
-    if constexpr (CAUSAL) {
-        bh = blockIdx.x % p.bh;
-        u = p.num_units - 1 - static_cast<int>(blockIdx.x / p.bh);
-    } else {
-        int unit = blockIdx.x;
-        if (unit >= p.split_begin) {
-            const int idx = unit - p.split_begin;
-            unit = p.split_begin + idx / p.num_splits;
-            split = idx % p.num_splits;
-        }
-        u = unit % p.num_units;
-        bh = unit / p.num_units;
-    }
     const int q0 = u * UNIT_ROWS;
     // This CTA's key tiles: [kv0, kv0 + n_tiles[t]) for query tile t.
     const int kv0 = split < 0 ? 0 : split * p.kv_tiles_per_split;
@@ -733,6 +746,21 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         ptx::tma_load_3d(sv + st * L::KV_BYTES + c * (BN * 128), &tm_v, c * 64,
                                          (kv0 + j) * BN, bh, bar(L::B_V_FULL + st));
                     issued = 2 * j + 2;
+                }
+                // The CTA one wave later starts as this wave's CTAs leave. Its first tiles,
+                // prefetched into L2 now that this CTA has issued all its own loads (about two
+                // key steps before it ends), are there when it starts.
+                const int nb = static_cast<int>(blockIdx.x) + p.next_prefetch_stride;
+                if (p.next_prefetch_stride > 0 && nb < static_cast<int>(gridDim.x) && !*abort_flag) {
+                    int nbh, nu, nsplit;
+                    unit_of_cta<CAUSAL>(nb, p, nbh, nu, nsplit);
+                    const int nkv = nsplit < 0 ? 0 : nsplit * p.kv_tiles_per_split;
+                    for (int c = 0; c < L::COL_BLOCKS; ++c) {
+                        ptx::tma_prefetch_3d(&tm_q, c * 64, nu * UNIT_ROWS, nbh);
+                        ptx::tma_prefetch_3d(&tm_k, c * 64, nkv * BN, nbh);
+                        ptx::tma_prefetch_3d(&tm_v, c * 64, nkv * BN, nbh);
+                        ptx::tma_prefetch_3d(&tm_q, c * 64, nu * UNIT_ROWS + BM, nbh);
+                    }
                 }
                 if (*abort_flag) {
                     // Drain: every copy this thread started must land before the CTA's shared
