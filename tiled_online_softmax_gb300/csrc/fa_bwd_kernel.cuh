@@ -37,6 +37,9 @@ struct BwdParams {
     float scale;          // softmax scale
     float scale_log2;     // scale * log2(e)
     unsigned long long timeout_ns;
+    // After issuing its last loads, each CTA prefetches into L2 the resident and first streamed
+    // blocks of CTA blockIdx.x + next_prefetch_stride, one wave later (0: none).
+    int next_prefetch_stride;
 };
 
 constexpr int BWD_THREADS = 192;
@@ -339,6 +342,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                                bar(do_bar));
                 issued_do = it + 1;
             }
+            // The CTA one wave later starts as this wave's CTAs leave: its K and V blocks and its
+            // first Q and dO blocks, prefetched into L2 now that this CTA's loads are issued.
+            const int nb = static_cast<int>(blockIdx.x) + p.next_prefetch_stride;
+            if (p.next_prefetch_stride > 0 && nb < static_cast<int>(gridDim.x) && !*abort_flag) {
+                const int nbh = nb / nkb, nk0 = (nb % nkb) * 128, nq0 = CAUSAL ? nk0 : 0;
+                for (int c = 0; c < D / 64; ++c) {
+                    ptx::tma_prefetch_3d(&tm_k, c * 64, nk0, nbh);
+                    ptx::tma_prefetch_3d(&tm_v, c * 64, nk0, nbh);
+                    ptx::tma_prefetch_3d(&tm_q, c * 64, nq0, nbh);
+                    ptx::tma_prefetch_3d(&tm_do, c * 64, nq0, nbh);
+                }
+            }
             if (*abort_flag) {
                 // The newest copy into each buffer is its newest phase.
                 wait_bar(bar(L::B_RES_FULL), 0, ctl, SITE_BWD_DRAIN, false);
@@ -636,6 +651,18 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
                 ptx::mbar_arrive_expect_tx(bar(L::B_V_FULL + vs), L::TILE);
                 tma_tile<D>(sbase + L::V_OFF + vs * L::TILE, &tm_v, j * 128, bh, bar(L::B_V_FULL + vs));
                 v_issued = j + 1;
+            }
+            // The CTA one wave later: its Q and dO blocks and its first K and V blocks.
+            const int nb = static_cast<int>(blockIdx.x) + p.next_prefetch_stride;
+            if (p.next_prefetch_stride > 0 && nb < static_cast<int>(gridDim.x) && !*abort_flag) {
+                const int nbh = CAUSAL ? nb % p.bh : nb / nqb;
+                const int nq0 = (CAUSAL ? nqb - 1 - nb / p.bh : nb % nqb) * 128;
+                for (int c = 0; c < D / 64; ++c) {
+                    ptx::tma_prefetch_3d(&tm_q, c * 64, nq0, nbh);
+                    ptx::tma_prefetch_3d(&tm_do, c * 64, nq0, nbh);
+                    ptx::tma_prefetch_3d(&tm_k, c * 64, 0, nbh);
+                    ptx::tma_prefetch_3d(&tm_v, c * 64, 0, nbh);
+                }
             }
             if (*abort_flag) {
                 // Drain: the newest copy into each stage is its barrier's newest phase.
