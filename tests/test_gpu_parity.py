@@ -543,3 +543,48 @@ def test_random_shapes(fa, orc, seed):
             ref = orc.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"), w.scale)
             parity.assert_parity(parity.compare(inputs.from_torch(o), ref, w.dtype), False,
                                  f"{w.name} split-KV", mean="auto")
+
+
+def test_tensor_map_cache_eviction_and_reuse(fa, orc):
+    """The library keeps the last 64 tensor maps, keyed by (address, shape, dtype). Forty problems
+    on distinct buffers (160 maps, so entries are evicted and encoded again) run twice more in
+    other orders and give the same bits; one set of buffers used with two shapes in turn (same
+    addresses, other extents) gives each shape's own result, equal to a run on buffers of its
+    own."""
+    rng = np.random.default_rng(77)
+    ws = [inputs.Workload(f"cache_{i}", 1, 2, int(rng.integers(1, 300)), int(rng.integers(1, 300)),
+                          int(rng.choice([64, 128])), "f16", bool(i % 2), seed=700 + i)
+          for i in range(40)]
+    tensors = []
+    for w in ws:
+        bits = inputs.draw(w)
+        tensors.append(tuple(inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv"))
+    first = [fa.forward(q, k, v, causal=w.causal, scale=w.scale) for w, (q, k, v) in zip(ws, tensors)]
+    for order in (list(range(39, -1, -1)), list(rng.permutation(40))):
+        for i in order:
+            w, (q, k, v) = ws[i], tensors[i]
+            o = fa.forward(q, k, v, causal=w.causal, scale=w.scale)
+            assert torch.equal(o.view(torch.int16), first[i].view(torch.int16)), i
+    torch.cuda.synchronize()
+    assert fa.last_device_error() == (0, 0)
+
+    # Same base addresses, two shapes.
+    D, Nk = 64, 300
+    big = {n: torch.zeros(1 * 2 * 512 * D, dtype=torch.float16, device="cuda") for n in "qkvo"}
+    results = {}
+    for Nq in (512, 128, 512):
+        w = inputs.Workload(f"cache_shape_{Nq}", 1, 2, Nq, Nk, D, "f16", False, seed=790 + Nq)
+        bits = inputs.draw(w)
+        own = [inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv"]
+        q = big["q"][:2 * Nq * D].view(1, 2, Nq, D)
+        k = big["k"][:2 * Nk * D].view(1, 2, Nk, D)
+        v = big["v"][:2 * Nk * D].view(1, 2, Nk, D)
+        o = big["o"][:2 * Nq * D].view(1, 2, Nq, D)
+        q.copy_(own[0]); k.copy_(own[1]); v.copy_(own[2])
+        fa.forward(q, k, v, scale=w.scale, out=o)
+        ref = fa.forward(*own, scale=w.scale)
+        assert torch.equal(o.view(torch.int16), ref.view(torch.int16)), Nq
+        results[Nq] = inputs.from_torch(o.clone())
+        exact = orc.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"), w.scale)
+        parity.assert_parity(parity.compare(results[Nq], exact, w.dtype), False, w.name, mean="auto")
+    assert fa.last_device_error() == (0, 0)
