@@ -392,6 +392,55 @@ def test_cuda_graph_replay_matches_eager(fa, w):
         assert torch.equal(o2.view(torch.int16), want2.view(torch.int16))
 
 
+def test_more_streams_than_workspace_slots(fa, orc):
+    """Eight non-blocking streams (the pool has four workspace slots) enqueue split shapes with no
+    ordering. A call that finds every slot in use by other streams' unfinished work runs as one
+    unsplit launch: with the streams held back while the calls are enqueued, four streams split
+    and four run unsplit, every output equals the split or the unsplit result bit for bit, and
+    both match the oracle."""
+    w = inputs.Workload("slots_few", 1, 2, 300, 3000, 128, "bf16", False, seed=43)
+    assert fa.plan(w.B, w.H, w.Nq, w.Nk, w.D, w.causal)["launches"] == 2
+    bits = inputs.draw(w)
+    qkv = tuple(inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    split_ref = inputs.from_torch(fa.forward(*qkv, scale=w.scale))
+    try:
+        fa.set_tail_split(False)
+        whole_ref = inputs.from_torch(fa.forward(*qkv, scale=w.scale))
+    finally:
+        fa.set_tail_split(True)
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in range(8)]
+    # Hold every stream behind a fixed-length spin (about 10 ms) while the calls are enqueued, so
+    # that no slot's last use has finished: the first four streams take the four slots (and keep
+    # them: a stream's own slot needs no wait), the other four run unsplit.
+    torch.cuda._sleep(20_000_000)
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())
+    reps = 6
+    outs = [[torch.empty_like(qkv[0]) for _ in range(reps)] for _ in streams]
+    fa.timer_start()
+    for r in range(reps):
+        for i, s in enumerate(streams):
+            fa.forward(*qkv, scale=w.scale, out=outs[i][r], stream=s)
+    torch.cuda.synchronize()
+    kernels = fa.timer_stop()
+    assert fa.last_device_error() == (0, 0)
+    n_split = n_whole = 0
+    for i in range(len(streams)):
+        for r in range(reps):
+            got = inputs.from_torch(outs[i][r])
+            if np.array_equal(got, split_ref):
+                n_split += 1
+            else:
+                assert np.array_equal(got, whole_ref), f"stream {i} call {r}"
+                n_whole += 1
+    assert kernels["merge"][1] == n_split
+    assert n_split == 4 * reps and n_whole == 4 * reps, (n_split, n_whole)
+    ref = orc.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"), w.scale)
+    for got in (split_ref, whole_ref):
+        parity.assert_parity(parity.compare(got, ref, w.dtype), True, "slots_few")
+
+
 def test_unordered_streams_never_share_a_workspace(fa, orc):
     """Two non-blocking streams run split shapes back to back with no ordering between them: a
     shape whose last wave is split (40 heads x 8 units = 320 units, last wave of 16) and a shape
