@@ -142,6 +142,9 @@ struct Params {
     // After issuing its last loads, each CTA prefetches into L2 the first tiles of CTA
     // blockIdx.x + next_prefetch_stride, one wave later (0: none).
     int next_prefetch_stride;
+    // The TMA lane initialises the barriers itself and issues the first Q and K loads before the
+    // CTA-wide barrier, overlapping the rest of the set-up (0: after it, as the other roles).
+    int early_loads;
 };
 
 template <int D>
@@ -645,7 +648,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         n_tiles[t] = CAUSAL ? min(nkt, (q0 + t * BM + BM - 1) / BN + 1)
                             : (split < 0 ? nkt : min(nkt - kv0, p.kv_tiles_per_split));
 
-    if (threadIdx.x == 0) {
+    const bool early = p.early_loads != 0;
+    const uint32_t sq = sbase + L::Q_OFF, sk = sbase + L::K_OFF, sv = sbase + L::V_OFF;
+    // TMA loads of the producer lane: Q tile t, and K tile j into its stage.
+    auto load_q = [&](int t) {
+        ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL + t), L::Q_TILE_BYTES);
+        for (int c = 0; c < L::COL_BLOCKS; ++c)
+            ptx::tma_load_3d(sq + t * L::Q_TILE_BYTES + c * (BM * 128), &tm_q, c * 64, q0 + t * BM,
+                             bh, bar(L::B_Q_FULL + t));
+    };
+    auto load_k = [&](int j) {
+        const int st = j % STAGES;
+        ptx::mbar_arrive_expect_tx(bar(L::B_K_FULL + st), L::KV_BYTES);
+        for (int c = 0; c < L::COL_BLOCKS; ++c)
+            ptx::tma_load_3d(sk + st * L::KV_BYTES + c * (BN * 128), &tm_k, c * 64, (kv0 + j) * BN,
+                             bh, bar(L::B_K_FULL + st));
+    };
+    if (threadIdx.x == (early ? LOAD_WARP * 32 : 0)) {
         *abort_flag = 0;
         for (int t = 0; t < Q_TILES; ++t) {
             ptx::mbar_init(bar(L::B_Q_FULL + t), 1);
@@ -685,6 +704,23 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
     }
+    // Loads the producer lane issued before the CTA barrier (early mode): the Q tiles the first
+    // products need, and K_0. Its barriers are its own, initialised above by this same thread.
+    int pre_q = 0;
+    bool pre_k0 = false;
+    if (early && warp == LOAD_WARP && lane == 0) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        load_q(0);
+        pre_q = 1;
+        if (p.rope_cos != nullptr) {
+            for (int t = 1; t < Q_TILES; ++t) load_q(t);
+            pre_q = Q_TILES;
+        }
+        if (n_tiles[Q_TILES - 1] > 0) {
+            load_k(0);
+            pre_k0 = true;
+        }
+    }
     if (warp == MMA_WARP) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
         ptx::tmem_relinquish();
@@ -708,33 +744,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (warp == LOAD_WARP) {
             // -------------------------------------------------------------- TMA producer
             if (lane == 0) {
-                const uint32_t sq = sbase + L::Q_OFF, sk = sbase + L::K_OFF, sv = sbase + L::V_OFF;
-                auto load_q = [&](int t) {
-                    ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL + t), L::Q_TILE_BYTES);
-                    for (int c = 0; c < L::COL_BLOCKS; ++c)
-                        ptx::tma_load_3d(sq + t * L::Q_TILE_BYTES + c * (BM * 128), &tm_q, c * 64,
-                                         q0 + t * BM, bh, bar(L::B_Q_FULL + t));
-                };
                 // Q_0, then K_0, then the other Q tiles: the first product S_0(0) needs only the
                 // first two. When the kernel rotates Q, both Q tiles come first, so that their
-                // rotation overlaps K_0's load.
-                load_q(0);
-                int q_loaded = 1;
+                // rotation overlaps K_0's load. (In early mode some of these were issued before
+                // the CTA barrier.)
+                int q_loaded = pre_q;
+                if (q_loaded == 0) {
+                    load_q(0);
+                    q_loaded = 1;
+                }
                 const bool q_first = p.rope_cos != nullptr;
-                if (q_first) {
-                    for (int t = 1; t < Q_TILES; ++t) load_q(t);
+                if (q_first && q_loaded < Q_TILES) {
+                    for (int t = q_loaded; t < Q_TILES; ++t) load_q(t);
                     q_loaded = Q_TILES;
                 }
                 const int n = n_tiles[Q_TILES - 1];
-                int issued = 0;
+                int issued = pre_k0 ? 1 : 0;
                 for (int j = 0; j < n; ++j) {
                     const int st = j % STAGES;
                     const uint32_t ph = (j / STAGES) & 1;
-                    if (!wait_bar(bar(L::B_K_EMPTY + st), ph ^ 1, ctl, SITE_LOAD_K_EMPTY)) break;
-                    ptx::mbar_arrive_expect_tx(bar(L::B_K_FULL + st), L::KV_BYTES);
-                    for (int c = 0; c < L::COL_BLOCKS; ++c)
-                        ptx::tma_load_3d(sk + st * L::KV_BYTES + c * (BN * 128), &tm_k, c * 64,
-                                         (kv0 + j) * BN, bh, bar(L::B_K_FULL + st));
+                    if (!(j == 0 && pre_k0)) {
+                        if (!wait_bar(bar(L::B_K_EMPTY + st), ph ^ 1, ctl, SITE_LOAD_K_EMPTY)) break;
+                        load_k(j);
+                    }
                     issued = 2 * j + 1;
                     if (j == 0 && !q_first) {
                         for (int t = 1; t < Q_TILES; ++t) load_q(t);
