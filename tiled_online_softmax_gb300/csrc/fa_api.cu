@@ -1129,6 +1129,9 @@ fa_status fa_bwd(const void* Q, const void* K, const void* V, const void* O, con
     p.scale_log2 = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
     p.timeout_ns = wait_timeout_ns();
     p.next_prefetch_stride = g_num_sms[dev];
+    // The load lanes issue their first blocks before the CTA-wide barrier: 0.2-0.8 % less time
+    // (same binary switched at run time, 20 rounds).
+    p.early_loads = 1;
     const int inst = (D == 128 ? 4 : 0) + (bf16 ? 2 : 0) + (causal ? 1 : 0);
     switch (inst) {
         case 0: return launch_bwd_instance<64, false, false>(dev, mq, mk, mv, mdo, p, strm);

@@ -40,6 +40,9 @@ struct BwdParams {
     // After issuing its last loads, each CTA prefetches into L2 the resident and first streamed
     // blocks of CTA blockIdx.x + next_prefetch_stride, one wave later (0: none).
     int next_prefetch_stride;
+    // The load lane initialises the barriers itself and issues the resident and first streamed
+    // blocks before the CTA-wide barrier (0: after it).
+    int early_loads;
 };
 
 constexpr int BWD_THREADS = 192;
@@ -230,13 +233,15 @@ __device__ __forceinline__ void zero_row(void* dst_row) {
 }
 
 // Prologue of the dK/dV kernel: barriers, TMEM. Returns the TMEM base.
-template <int D, bool CAUSAL>
+template <int D, bool CAUSAL, typename Prologue>
 __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t sbase, uint32_t tmem_slot_addr,
-                                              uint32_t* tmem_slot, volatile int* abort_flag) {
+                                              uint32_t* tmem_slot, volatile int* abort_flag,
+                                              bool early, Prologue&& prologue) {
     using L = BwdSmem<D, CAUSAL>;
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
     const int warp = threadIdx.x >> 5;
-    if (threadIdx.x == 0) {
+    const int init_thread = early ? BWD_LOAD_WARP * 32 : 0;
+    if (threadIdx.x == init_thread) {
         *abort_flag = 0;
         ptx::mbar_init(bar(L::B_RES_FULL), 1);
         for (int s = 0; s < L::Q_STAGES; ++s) {
@@ -257,6 +262,8 @@ __device__ __forceinline__ uint32_t bwd_setup(uint8_t* smem, uint32_t sbase, uin
         ptx::fence_barrier_init();
         ptx::fence_proxy_async_smem();
     }
+    // Early mode: the load lane, which initialised the barriers just above, starts its loads now.
+    if (early && threadIdx.x == init_thread) prologue();
     if (warp == BWD_MMA_WARP) {
         ptx::tmem_alloc(tmem_slot_addr, TMEM_COLS);
         ptx::tmem_relinquish();
@@ -308,7 +315,41 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int k0 = kb * 128;
     const int i_begin = CAUSAL ? kb : 0;  // query blocks before the diagonal see none of these keys
     const int n = nqb > i_begin ? nqb - i_begin : 0;
-    const uint32_t tmem = bwd_setup<D, CAUSAL>(smem, sbase, ptx::smem_u32(tmem_slot), tmem_slot, abort_flag);
+    const bool early = p.early_loads != 0;
+    // Loads of the load lane: the resident K and V blocks; query block `it` of Q (with its lse2
+    // row) and of dO (with its delta row) into their stages.
+    auto load_res = [&]() {
+        ptx::mbar_arrive_expect_tx(bar(L::B_RES_FULL), 2 * L::TILE);
+        tma_tile<D>(sbase + L::R0_OFF, &tm_k, k0, bh, bar(L::B_RES_FULL));
+        tma_tile<D>(sbase + L::R1_OFF, &tm_v, k0, bh, bar(L::B_RES_FULL));
+    };
+    auto load_q_blk = [&](int it) {
+        const int qs = it % QS;
+        const size_t vo = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(i_begin + it) * 128;
+        ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL + qs), L::TILE + L::VEC_BYTES);
+        tma_tile<D>(sbase + L::A_OFF + qs * L::TILE, &tm_q, (i_begin + it) * 128, bh, bar(L::B_Q_FULL + qs));
+        ptx::bulk_load(sbase + L::LSE_OFF + qs * L::VEC_BYTES, p.lse2 + vo, L::VEC_BYTES,
+                       bar(L::B_Q_FULL + qs));
+    };
+    auto load_do_blk = [&](int it) {
+        const int ds = it % DS;
+        const size_t vo = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(i_begin + it) * 128;
+        ptx::mbar_arrive_expect_tx(bar(L::B_DO_FULL + ds), L::TILE + L::VEC_BYTES);
+        tma_tile<D>(sbase + L::B_OFF + ds * L::TILE, &tm_do, (i_begin + it) * 128, bh, bar(L::B_DO_FULL + ds));
+        ptx::bulk_load(sbase + L::DELTA_OFF + ds * L::VEC_BYTES, p.delta + vo, L::VEC_BYTES,
+                       bar(L::B_DO_FULL + ds));
+    };
+    bool pre = false;  // the resident blocks and query block 0 were issued before the barrier
+    const uint32_t tmem = bwd_setup<D, CAUSAL>(smem, sbase, ptx::smem_u32(tmem_slot), tmem_slot,
+                                               abort_flag, early, [&]() {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        if (n > 0) {
+            load_res();
+            load_q_blk(0);
+            load_do_blk(0);
+            pre = true;
+        }
+    });
     const Ctl ctl{abort_flag, p.err, p.timeout_ns};
     // Launched as a programmatic dependent of the preprocessing: its outputs (and Q, K, V, dO,
     // possibly from earlier kernels) are read only after it has completed.
@@ -320,26 +361,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 
     if (warp == BWD_LOAD_WARP) {
         if (lane == 0 && n > 0) {
-            ptx::mbar_arrive_expect_tx(bar(L::B_RES_FULL), 2 * L::TILE);
-            tma_tile<D>(sbase + L::R0_OFF, &tm_k, k0, bh, bar(L::B_RES_FULL));
-            tma_tile<D>(sbase + L::R1_OFF, &tm_v, k0, bh, bar(L::B_RES_FULL));
-            int issued_q = 0, issued_do = 0;
-            for (int it = 0; it < n; ++it) {
-                const int i = i_begin + it;
+            if (!pre) load_res();
+            int issued_q = pre ? 1 : 0, issued_do = pre ? 1 : 0;
+            for (int it = pre ? 1 : 0; it < n; ++it) {
                 const int qs = it % QS, ds = it % DS;
-                const size_t vo = static_cast<size_t>(bh) * p.nq_pad + static_cast<size_t>(i) * 128;
-                const int do_bar = L::B_DO_FULL + ds;
                 if (!wait_bar(bar(L::B_Q_EMPTY + qs), ((it / QS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
-                ptx::mbar_arrive_expect_tx(bar(L::B_Q_FULL + qs), L::TILE + L::VEC_BYTES);
-                tma_tile<D>(sbase + L::A_OFF + qs * L::TILE, &tm_q, i * 128, bh, bar(L::B_Q_FULL + qs));
-                ptx::bulk_load(sbase + L::LSE_OFF + qs * L::VEC_BYTES, p.lse2 + vo, L::VEC_BYTES,
-                               bar(L::B_Q_FULL + qs));
+                load_q_blk(it);
                 issued_q = it + 1;
                 if (!wait_bar(bar(L::B_DO_EMPTY + ds), ((it / DS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
-                ptx::mbar_arrive_expect_tx(bar(do_bar), L::TILE + L::VEC_BYTES);
-                tma_tile<D>(sbase + L::B_OFF + ds * L::TILE, &tm_do, i * 128, bh, bar(do_bar));
-                ptx::bulk_load(sbase + L::DELTA_OFF + ds * L::VEC_BYTES, p.delta + vo, L::VEC_BYTES,
-                               bar(do_bar));
+                load_do_blk(it);
                 issued_do = it + 1;
             }
             // The CTA one wave later starts as this wave's CTAs leave: its K and V blocks and its
@@ -604,7 +634,24 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
     const int q0 = qb * 128;
     const int n = CAUSAL ? min(nkb, qb + 1) : nkb;  // key blocks up to the diagonal
 
-    if (threadIdx.x == 0) {
+    const bool early = p.early_loads != 0;
+    // Loads of the load lane: the resident Q and dO blocks; key block j of K and of V.
+    auto load_res = [&]() {
+        ptx::mbar_arrive_expect_tx(bar(L::B_RES_FULL), 2 * L::TILE);
+        tma_tile<D>(sbase + L::Q_OFF, &tm_q, q0, bh, bar(L::B_RES_FULL));
+        tma_tile<D>(sbase + L::DO_OFF, &tm_do, q0, bh, bar(L::B_RES_FULL));
+    };
+    auto load_k_blk = [&](int j) {
+        const int ks = j % KS;
+        ptx::mbar_arrive_expect_tx(bar(L::B_K_FULL + ks), L::TILE);
+        tma_tile<D>(sbase + L::K_OFF + ks * L::TILE, &tm_k, j * 128, bh, bar(L::B_K_FULL + ks));
+    };
+    auto load_v_blk = [&](int j) {
+        const int vs = j % VS;
+        ptx::mbar_arrive_expect_tx(bar(L::B_V_FULL + vs), L::TILE);
+        tma_tile<D>(sbase + L::V_OFF + vs * L::TILE, &tm_v, j * 128, bh, bar(L::B_V_FULL + vs));
+    };
+    if (threadIdx.x == (early ? BWD_LOAD_WARP * 32 : 0)) {
         *abort_flag = 0;
         ptx::mbar_init(bar(L::B_RES_FULL), 1);
         for (int s = 0; s < KS; ++s) {
@@ -624,6 +671,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
         ptx::fence_barrier_init();
         ptx::fence_proxy_async_smem();
     }
+    // Early mode: the load lane, which initialised the barriers just above, starts its loads
+    // before the CTA barrier (this kernel reads nothing its predecessor in the stream writes).
+    bool pre = false;
+    if (early && threadIdx.x == BWD_LOAD_WARP * 32 && n > 0) {
+        load_res();
+        load_k_blk(0);
+        load_v_blk(0);
+        pre = true;
+    }
     if (warp == BWD_MMA_WARP) {
         ptx::tmem_alloc(ptx::smem_u32(tmem_slot), TMEM_COLS);
         ptx::tmem_relinquish();
@@ -637,19 +693,15 @@ __global__ void __launch_bounds__(BWD_THREADS, 1)
 
     if (warp == BWD_LOAD_WARP) {
         if (lane == 0) {
-            ptx::mbar_arrive_expect_tx(bar(L::B_RES_FULL), 2 * L::TILE);
-            tma_tile<D>(sbase + L::Q_OFF, &tm_q, q0, bh, bar(L::B_RES_FULL));
-            tma_tile<D>(sbase + L::DO_OFF, &tm_do, q0, bh, bar(L::B_RES_FULL));
-            int k_issued = 0, v_issued = 0;
-            for (int j = 0; j < n; ++j) {
+            if (!pre) load_res();
+            int k_issued = pre ? 1 : 0, v_issued = pre ? 1 : 0;
+            for (int j = pre ? 1 : 0; j < n; ++j) {
                 const int ks = j % KS, vs = j % VS;
                 if (!wait_bar(bar(L::B_K_EMPTY + ks), ((j / KS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
-                ptx::mbar_arrive_expect_tx(bar(L::B_K_FULL + ks), L::TILE);
-                tma_tile<D>(sbase + L::K_OFF + ks * L::TILE, &tm_k, j * 128, bh, bar(L::B_K_FULL + ks));
+                load_k_blk(j);
                 k_issued = j + 1;
                 if (!wait_bar(bar(L::B_V_EMPTY + vs), ((j / VS) & 1) ^ 1, ctl, SITE_BWD_LOAD)) break;
-                ptx::mbar_arrive_expect_tx(bar(L::B_V_FULL + vs), L::TILE);
-                tma_tile<D>(sbase + L::V_OFF + vs * L::TILE, &tm_v, j * 128, bh, bar(L::B_V_FULL + vs));
+                load_v_blk(j);
                 v_issued = j + 1;
             }
             // The CTA one wave later: its Q and dO blocks and its first K and V blocks.
