@@ -33,8 +33,11 @@
 //                            through rings of stages.
 //   warps 10-11              idle.
 // The grid is launched as a programmatic dependent of the stream's previous kernel; its set-up
-// may overlap that kernel's end, and nothing in global memory is touched before
-// griddepcontrol.wait.
+// may overlap that kernel's end, and no global memory is read or written before
+// griddepcontrol.wait (the first wave of a causal launch issues L2 prefetch hints for its first
+// tiles before it, which move no data into the SM). The TMA lane initialises the barriers and
+// issues the first Q and K loads before the CTA-wide barrier; once its own loads are issued it
+// prefetches into L2 the first tiles of the CTA one wave later.
 // The MMA warp issues, per key tile j: PV_0(j) in two halves (keys 0-63 as soon as the softmax
 // releases them, then 64-127), S_0(j+1), PV_1(j) likewise, S_1(j+1). While one tile's softmax
 // runs, the tensor cores work on the other tile's products.
@@ -731,8 +734,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = *tmem_slot;
     const Ctl ctl{abort_flag, p.err, p.timeout_ns};
     // This grid is launched as a programmatic dependent of the stream's previous kernel: the set-up
-    // above (shared memory, TMEM, tensor-map prefetch) may overlap that kernel's last CTAs, and
-    // nothing in global memory is touched before it has completed and its writes are visible.
+    // above (shared memory, TMEM, tensor-map and L2 prefetch hints) may overlap that kernel's last
+    // CTAs, and no global memory is read or written before it has completed and its writes are
+    // visible (the TMA lane, in early mode, waited above before its first loads).
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // Likewise a grid launched after this one as a programmatic dependent (the merge of split key
     // ranges, or the next attention launch) may be scheduled once every CTA of this grid has
