@@ -561,7 +561,11 @@ fa_status launch_split(const void* Q, const void* K, const void* V, void* O, flo
     const fa::MergeMap map{static_cast<int>(split_begin),
                            static_cast<int>((Nq + fa::UNIT_ROWS - 1) / fa::UNIT_ROWS),
                            static_cast<int>(split_rows), static_cast<int>(Nq),
-                           static_cast<int>(B * H)};
+                           static_cast<int>(B * H),
+                           // signal the next launch early: 3.5 % less time per call on the ragged
+                           // workload, 1 % on the long-context chunk (same binary, switched at
+                           // run time, 30 rounds)
+                           1};
     const int64_t nrows = static_cast<int64_t>(rows);
     const int64_t sms = current_sms_or(152);
     const bool bf16 = dtype == FA_BF16;

@@ -24,6 +24,9 @@ namespace fa {
 struct MergeMap {
     int split_begin, num_units, split_rows, nq;
     int bh;  // slices of O (B * H)
+    // Nonzero: signal the stream's next programmatic-dependent launch as soon as every block has
+    // passed its wait (else at completion).
+    int trigger_dependents;
 };
 
 // One warp per R consecutive merged rows; lane i owns D/32 consecutive columns of each. The
@@ -40,6 +43,9 @@ __global__ void __launch_bounds__(256) fa_merge_kernel(const float* __restrict__
     // Launched as a programmatic dependent of the attention kernel: wait until that grid has
     // completed and its partial states are visible (a no-op for an ordinary launch).
     asm volatile("griddepcontrol.wait;" ::: "memory");
+    // The next launch (the next attention call) may then take SMs as this grid's blocks leave; it
+    // waits for this grid to complete before it reads or writes global memory.
+    if (map.trigger_dependents) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
     // 32-bit index arithmetic: rows, units and query rows all fit in int (checked on the host).
     const int row0 = static_cast<int>((blockIdx.x * blockDim.x + threadIdx.x) >> 5) * R;
     const int lane = threadIdx.x & 31;
