@@ -637,3 +637,38 @@ def test_tensor_map_cache_eviction_and_reuse(fa, orc):
         exact = orc.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"), w.scale)
         parity.assert_parity(parity.compare(results[Nq], exact, w.dtype), False, w.name, mean="auto")
     assert fa.last_device_error() == (0, 0)
+
+
+def test_splitkv_in_cuda_graph(fa):
+    """fa_fwd_splitkv (attention over key ranges, then the merge, which signals the next launch
+    early) followed by a forward that reads its output, captured in a CUDA graph: the replays give
+    the eager bits, replay after replay."""
+    w = inputs.Workload("graph_splitkv", 1, 4, 130, 2048, 128, "bf16", False, seed=17)
+    bits = inputs.draw(w)
+    q, k, v = (inputs.to_torch(bits[n], w.dtype).cuda() for n in "qkv")
+    ws = torch.empty(fa.lib().fa_splitkv_workspace_bytes(w.B, w.H, w.Nq, w.Nk, w.D, 6),
+                     dtype=torch.uint8, device="cuda")
+    o1, o2 = torch.empty_like(q), torch.empty_like(q)
+    try:
+        fa.set_tail_split(False)  # the second call as one launch, eager and captured alike
+        fa.forward_splitkv(q, k, v, num_splits=6, scale=w.scale, out=o1, workspace=ws)
+        fa.forward(o1, k, v, scale=w.scale, out=o2)
+        torch.cuda.synchronize()
+        eager1, eager2 = o1.clone(), o2.clone()
+        s = torch.cuda.Stream()
+        s.wait_stream(torch.cuda.current_stream())
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g, stream=s):
+            fa.forward_splitkv(q, k, v, num_splits=6, scale=w.scale, out=o1, workspace=ws,
+                               stream=s)
+            fa.forward(o1, k, v, scale=w.scale, out=o2, stream=s)
+        for _ in range(3):
+            o1.zero_()
+            o2.zero_()
+            g.replay()
+            torch.cuda.synchronize()
+            assert torch.equal(o1.view(torch.int16), eager1.view(torch.int16))
+            assert torch.equal(o2.view(torch.int16), eager2.view(torch.int16))
+    finally:
+        fa.set_tail_split(True)
+    assert fa.last_device_error() == (0, 0)
