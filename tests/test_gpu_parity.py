@@ -251,6 +251,28 @@ def test_rescale_threshold_choices_agree(fa, orc, dtype, taus):
         fa.set_rescale_threshold(old)
 
 
+@pytest.mark.parametrize("causal", [False, True])
+def test_rescale_on_every_rise_at_d64(fa, orc, causal):
+    """D = 64, where the S products of the two query tiles rotate through three TMEM buffers and a
+    tile's softmax runs ahead of the PV products: a rescale of O must first wait for the previous
+    PV product. Threshold 0 rescales on every rise of the maximum (on the large-magnitude
+    distribution, at most key steps), 15 lazily; both meet the bar, causal (one more key tile
+    for the second query tile) and not."""
+    w = inputs.WORKLOADS["rescale_stress"].with_(name="d64_rescale", B=1, H=2, Nq=1100, Nk=1100,
+                                                 D=64, dtype="f16", causal=causal, scale=0.125,
+                                                 seed=30 + causal)
+    bits = inputs.draw(w)
+    ref = orc.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"), w.scale, w.causal)
+    old = fa.get_rescale_threshold()
+    try:
+        for tau in (0.0, 15.0):
+            fa.set_rescale_threshold(tau)
+            o = inputs.from_torch(run_gpu(fa, bits, w))
+            parity.assert_parity(parity.compare(o, ref, w.dtype), True, f"d64 tau={tau}")
+    finally:
+        fa.set_rescale_threshold(old)
+
+
 def test_rescale_threshold_setter_validates(fa):
     old = fa.get_rescale_threshold()
     for bad in (-1.0, 64.5, float("inf"), float("nan")):

@@ -38,13 +38,20 @@
 // tiles before it, which move no data into the SM). The TMA lane initialises the barriers and
 // issues the first Q and K loads before the CTA-wide barrier; once its own loads are issued it
 // prefetches into L2 the first tiles of the CTA one wave later.
-// The MMA warp issues, per key tile j: PV_0(j) in two halves (keys 0-63 as soon as the softmax
-// releases them, then 64-127), S_0(j+1), PV_1(j) likewise, S_1(j+1). While one tile's softmax
-// runs, the tensor cores work on the other tile's products.
+// D = 128: the MMA warp issues, per key tile j: PV_0(j) in two halves (keys 0-63 as soon as the
+// softmax releases them, then 64-127), S_0(j+1), PV_1(j) likewise, S_1(j+1). While one tile's
+// softmax runs, the tensor cores work on the other tile's products; each tile's S_t(j+1) waits
+// for PV_t(j), because it overwrites P_t(j).
+// D = 64: the two O accumulators leave room for a third S/P buffer, and the S products of both
+// tiles rotate through the three (the k-th S product of the CTA, in issue order, goes to buffer
+// k mod 3). The MMA warp issues PV of product k - 3, which frees its buffer, then S product k. A
+// tile's next S then lands while its softmax still works on the current one, and each softmax
+// runs its key steps back to back.
 //
 // Tensor memory (512 columns x 128 lanes of 32 bit):
-//   [0,128) S_0 (fp32), its first 64 columns take P_0 (16-bit pairs) once S_0 is read
-//   [128,256) S_1 / P_1;  [256,256+D) O_0;  [384,384+D) O_1.
+//   D = 128: [0,128) S_0 (fp32), its first 64 columns take P_0 (16-bit pairs) once S_0 is read;
+//            [128,256) S_1 / P_1;  [256,384) O_0;  [384,512) O_1.
+//   D = 64:  [0,128), [128,256), [256,384) the three S / P buffers;  [384,448) O_0;  [448,512) O_1.
 //
 // Masking: a key j >= Nk (partial last tile, phobos "Attention", `attention`) or, under causal
 // masking, a key after the query (phobos "Causal attention") is left out of the row max and gets
@@ -75,8 +82,21 @@ constexpr int NUM_THREADS = 384;
 constexpr int MMA_WARP = 8;
 constexpr int LOAD_WARP = 9;
 constexpr uint32_t TMEM_COLS = 512;
-__host__ __device__ constexpr uint32_t tmem_s(int t) { return t ? 128u : 0u; }
-__host__ __device__ constexpr uint32_t tmem_o(int t) { return t ? 384u : 256u; }
+// Three S / P buffers rotating between the two tiles (D = 64), or one per tile (D = 128).
+template <int D>
+constexpr bool S_RING = (D == 64);
+template <int D>
+__host__ __device__ constexpr uint32_t tmem_o(int t) {
+    return S_RING<D> ? 384u + 64u * static_cast<uint32_t>(t) : (t ? 384u : 256u);
+}
+// Number of S_t(j) in the order the MMA warp issues a CTA's S products: the two tiles alternate
+// while both have key tiles left, then tile 1 alone (n0 = tile 0's key tiles <= tile 1's: its
+// rows come first). Its TMEM buffer: tmem_s_buf.
+__host__ __device__ constexpr int s_seq(int t, int j, int n0) { return j < n0 ? 2 * j + t : n0 + j; }
+template <int D>
+__host__ __device__ constexpr uint32_t tmem_s_buf(int t, int j, int n0) {
+    return S_RING<D> ? 128u * static_cast<uint32_t>(s_seq(t, j, n0) % 3) : (t ? 128u : 0u);
+}
 
 // Registers per thread after rebalancing. The launch gives each of the 384 threads 168 (the
 // most that fits 65536); the two softmax warpgroups then take 216 each, the MMA/TMA warpgroup
@@ -95,6 +115,7 @@ enum WaitSite : int {
     SITE_MMA_P_FULL = 5,
     SITE_MMA_V_FULL = 6,
     SITE_SOFTMAX_S_FULL = 7,
+    SITE_SOFTMAX_O_DONE = 8,
     SITE_EPI_O_READY = 9,
     SITE_DRAIN = 10,
     SITE_EPI_O_STAGED = 14,
@@ -166,10 +187,16 @@ struct Smem {
     static constexpr int B_K_EMPTY = B_K_FULL + STAGES;
     static constexpr int B_V_FULL = B_K_EMPTY + STAGES;
     static constexpr int B_V_EMPTY = B_V_FULL + STAGES;
-    static constexpr int B_S_FULL = B_V_EMPTY + STAGES;         // [2] MMA -> softmax
-    static constexpr int B_P_HALF = B_S_FULL + Q_TILES;         // [2] softmax -> MMA (keys 0-63)
-    static constexpr int B_P_FULL = B_P_HALF + Q_TILES;         // [2] softmax -> MMA (keys 64-127)
-    static constexpr int B_O_READY = B_P_FULL + Q_TILES;        // [2] MMA -> epilogue
+    // The per-step hand-offs use one barrier per tile, or with the S ring one per buffer: a
+    // tile's softmax may then run up to two steps ahead of the PV product that consumes its P,
+    // but a buffer is reused only after the PV of its previous product has been issued, so each
+    // barrier completes at most one phase ahead of its waiter.
+    static constexpr int HAND = S_RING<D> ? 3 : Q_TILES;
+    static constexpr int B_S_FULL = B_V_EMPTY + STAGES;         // [HAND] MMA -> softmax
+    static constexpr int B_P_HALF = B_S_FULL + HAND;            // [HAND] softmax -> MMA (keys 0-63)
+    static constexpr int B_P_FULL = B_P_HALF + HAND;            // [HAND] softmax -> MMA (keys 64-127)
+    static constexpr int B_O_DONE = B_P_FULL + HAND;            // [2] (S ring) PV_t(j) complete
+    static constexpr int B_O_READY = B_O_DONE + (S_RING<D> ? Q_TILES : 0);  // [2] MMA -> epilogue
     static constexpr int B_O_STAGED = B_O_READY + Q_TILES;      // [2] O_t in smem (4 warps)
     static constexpr int B_Q_ROT = B_O_STAGED + Q_TILES;        // [2] Q_t rotated (8 warps)
     static constexpr int B_DRAIN = B_Q_ROT + Q_TILES;
@@ -182,6 +209,14 @@ struct Smem {
     // More than half an SM's shared memory, so two CTAs never share an SM: each holds all 512
     // TMEM columns, and a second one would stall in tcgen05.alloc.
     static_assert(ALLOC_BYTES > 116 * 1024, "one CTA per SM");
+    // Hand-off barrier of tile t's key step j (base: B_S_FULL, B_P_HALF or B_P_FULL; n0: tile
+    // 0's key tiles), and the phase parity that step completes on it.
+    __device__ static constexpr int hand(int base, int t, int j, int n0) {
+        return base + (S_RING<D> ? s_seq(t, j, n0) % 3 : t);
+    }
+    __device__ static constexpr uint32_t hand_parity(int t, int j, int n0) {
+        return static_cast<uint32_t>(S_RING<D> ? (s_seq(t, j, n0) / 3) & 1 : j & 1);
+    }
 };
 
 // ---------------------------------------------------------------------------------------------
@@ -271,7 +306,7 @@ __device__ __forceinline__ void epilogue(int t, uint32_t tmem, uint32_t sbase, c
     const int r = threadIdx.x & 127;
     const int warp = threadIdx.x >> 5;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t o_cols = tmem + lane_base + tmem_o(t);
+    const uint32_t o_cols = tmem + lane_base + tmem_o<D>(t);
     const int row = q0 + t * BM + r;
     if (!wait_bar_warp(bar(L::B_O_READY + t), 0, ctl, SITE_EPI_O_READY)) return;
     ptx::tc_fence_after();
@@ -463,7 +498,7 @@ __device__ __forceinline__ bool rotate_q(uint32_t sbase, const Params& p, const 
 template <int D, bool BF16, bool CAUSAL>
 __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbase,
                                              const Params& p, const Ctl& ctl, int bh, int q0,
-                                             int split, int kv0, int n_tiles,
+                                             int split, int kv0, int n_tiles, int n_first,
                                              const CUtensorMap* tm_o) {
     using L = Smem<D>;
     auto bar = [&](int i) { return sbase + L::BAR_OFF + 8u * static_cast<uint32_t>(i); };
@@ -472,8 +507,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
     const int q_tile0 = q0 + t * BM;
     const int row = q_tile0 + r;
     const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
-    const uint32_t s_cols = tmem + lane_base + tmem_s(t);
-    const uint32_t o_cols = tmem + lane_base + tmem_o(t);
+    const uint32_t o_cols = tmem + lane_base + tmem_o<D>(t);
     // A zero scale would turn the -inf of a hidden score into 0 * inf = NaN; a tiny positive
     // scale gives the same weights (every visible score maps to 2^0 = 1) and keeps -inf -> 0.
     const float c_signed = (p.scale_log2 == 0.f) ? 1e-30f : p.scale_log2;
@@ -486,7 +520,11 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
     float l = 0.f;            // running denominator relative to m_ref
 
     for (int j = 0; j < n_tiles; ++j) {
-        if (!wait_bar_warp(bar(L::B_S_FULL + t), j & 1, ctl, SITE_SOFTMAX_S_FULL)) return;
+        // S_t(j), then P_t(j), in the TMEM buffer of this step (n_first: tile 0's key tiles).
+        const uint32_t s_cols = tmem + lane_base + tmem_s_buf<D>(t, j, n_first);
+        if (!wait_bar_warp(bar(L::hand(L::B_S_FULL, t, j, n_first)), L::hand_parity(t, j, n_first),
+                           ctl, SITE_SOFTMAX_S_FULL))
+            return;
         ptx::tc_fence_after();
         uint32_t sr[4][32];
         ptx::tmem_ld128(s_cols, sr);
@@ -567,9 +605,15 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
             }
             ptx::tmem_st32(s_cols + h * 32, pk);
             if (h == 0 && j > 0 && __any_sync(0xffffffffu, corr != 1.f)) {
-                // Rescale this warp's O rows when any of them moved its reference. No wait is
-                // needed: the S_t(j) commit this warp waited on was issued after PV_t(j-1), so
-                // O_t holds every key < k0, and PV_t(j) starts only after this warp's release.
+                // Rescale this warp's O rows when any of them moved its reference. O_t must hold
+                // every key < k0, and PV_t(j) starts only after this warp's release. With one
+                // buffer per tile no wait is needed: the S_t(j) commit this warp waited on was
+                // issued after PV_t(j-1). With the S ring, PV_t(j-1) may still run: wait for it.
+                if constexpr (S_RING<D>) {
+                    if (!wait_bar_warp(bar(L::B_O_DONE + t), (j - 1) & 1, ctl, SITE_SOFTMAX_O_DONE))
+                        return;
+                    ptx::tc_fence_after();
+                }
 #pragma unroll
                 for (int q = 0; q < D / 32; ++q) {
                     uint32_t o[32];
@@ -584,7 +628,7 @@ __device__ __forceinline__ void softmax_role(int t, uint32_t tmem, uint32_t sbas
             }
             ptx::tmem_wait_st();
             ptx::tc_fence_before();
-            ptx::mbar_arrive(bar(h == 0 ? L::B_P_HALF + t : L::B_P_FULL + t));
+            ptx::mbar_arrive(bar(L::hand(h == 0 ? L::B_P_HALF : L::B_P_FULL, t, j, n_first)));
         }
         const float rowsum =
             ((acc[0] + acc[1]) + (acc[2] + acc[3])) + ((acc[4] + acc[5]) + (acc[6] + acc[7]));
@@ -669,11 +713,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     };
     if (threadIdx.x == (early ? LOAD_WARP * 32 : 0)) {
         *abort_flag = 0;
+        for (int h = 0; h < L::HAND; ++h) {
+            ptx::mbar_init(bar(L::B_S_FULL + h), 1);
+            ptx::mbar_init(bar(L::B_P_HALF + h), BM);
+            ptx::mbar_init(bar(L::B_P_FULL + h), BM);
+        }
         for (int t = 0; t < Q_TILES; ++t) {
             ptx::mbar_init(bar(L::B_Q_FULL + t), 1);
-            ptx::mbar_init(bar(L::B_S_FULL + t), 1);
-            ptx::mbar_init(bar(L::B_P_HALF + t), BM);
-            ptx::mbar_init(bar(L::B_P_FULL + t), BM);
+            if (S_RING<D>) ptx::mbar_init(bar(L::B_O_DONE + t), 1);
             ptx::mbar_init(bar(L::B_O_READY + t), 1);
             ptx::mbar_init(bar(L::B_O_STAGED + t), 4);
             ptx::mbar_init(bar(L::B_Q_ROT + t), 8);
@@ -828,13 +875,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // swizzle row); Q and K tiles are K-major, 8-row swizzle atoms 1024 bytes apart, the
             // second 64 columns of D one column block further. Descriptors are built once per
             // operand tile; a step of k adds its byte offset (>> 4) to the start-address field.
+            const int n0 = n_tiles[0], n1 = n_tiles[Q_TILES - 1];
             auto issue_s = [&](int t, int j) {
                 const uint64_t a0 = ptx::sdesc_sw128(sq + t * L::Q_TILE_BYTES, 16, 1024);
                 const uint64_t b0 = ptx::sdesc_sw128(sk + (j % STAGES) * L::KV_BYTES, 16, 1024);
+                const uint32_t d = tmem + tmem_s_buf<D>(t, j, n0);
 #pragma unroll
                 for (int kk = 0; kk < D / 16; ++kk) {
                     const uint32_t off = ((kk / 4) * (BM * 128) + (kk % 4) * 32) >> 4;
-                    ptx::mma_ss_if(leader, tmem + tmem_s(t), a0 + off, b0 + off, IDESC_S, kk > 0 ? 1u : 0u);
+                    ptx::mma_ss_if(leader, d, a0 + off, b0 + off, IDESC_S, kk > 0 ? 1u : 0u);
                 }
             };
             // O_t += P_t V_j over keys [64 half, 64 half + 64): P_t is the A operand from TMEM
@@ -842,58 +891,115 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // 16 keys = 16 rows of 128 bytes, the next 64 columns of D one column block away.
             auto issue_pv = [&](int t, int j, int half) {
                 const uint64_t b0 = ptx::sdesc_sw128(sv + (j % STAGES) * L::KV_BYTES, BN * 128, 1024);
+                const uint32_t a = tmem + tmem_s_buf<D>(t, j, n0);
 #pragma unroll
                 for (int kk = half * (BN / 32); kk < (half + 1) * (BN / 32); ++kk)
-                    ptx::mma_ts_if(leader, tmem + tmem_o(t), tmem + tmem_s(t) + kk * 8,
+                    ptx::mma_ts_if(leader, tmem + tmem_o<D>(t), a + kk * 8,
                                    b0 + ((kk * 16 * 128) >> 4), IDESC_O, (j > 0 || kk > 0) ? 1u : 0u);
             };
             auto commit = [&](int b) { ptx::mma_commit_if(leader, bar(b)); };
-            // Per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1). S_t(j+1) overwrites the TMEM
-            // columns P_t(j) occupies, so it follows PV_t(j) (MMAs of one thread run in order).
-            const int n0 = n_tiles[0], n1 = n_tiles[Q_TILES - 1];
             // Q_t is ready once loaded, or once rotated when the kernel applies the rotary
             // embedding to it.
             const int q_ready = p.rope_cos != nullptr ? L::B_Q_ROT : L::B_Q_FULL;
-            bool ok = wait_bar_warp(bar(q_ready + 0), 0, ctl, SITE_MMA_Q_FULL) &&
-                      wait_bar_warp(bar(L::B_K_FULL + 0), 0, ctl, SITE_MMA_K_FULL);
-            if (ok) {
-                ptx::tc_fence_after();
-                issue_s(0, 0);
-                commit(L::B_S_FULL + 0);
-                ok = wait_bar_warp(bar(q_ready + 1), 0, ctl, SITE_MMA_Q_FULL);
-            }
-            if (ok) {
-                ptx::tc_fence_after();
-                issue_s(1, 0);
-                commit(L::B_S_FULL + 1);
-                commit(L::B_K_EMPTY + 0);
-            }
-            for (int j = 0; ok && j < n1; ++j) {
-                const int st = j % STAGES, st1 = (j + 1) % STAGES;
-                const uint32_t ph1 = ((j + 1) / STAGES) & 1;
-                if (!(ok = wait_bar_warp(bar(L::B_V_FULL + st), (j / STAGES) & 1, ctl, SITE_MMA_V_FULL)))
-                    break;
-                for (int t = 0; t < Q_TILES; ++t) {
-                    if (j >= n_tiles[t]) continue;
-                    if (!(ok = wait_bar_warp(bar(L::B_P_HALF + t), j & 1, ctl, SITE_MMA_P_FULL))) break;
-                    ptx::tc_fence_after();
-                    issue_pv(t, j, 0);
-                    if (!(ok = wait_bar_warp(bar(L::B_P_FULL + t), j & 1, ctl, SITE_MMA_P_FULL))) break;
-                    ptx::tc_fence_after();
-                    issue_pv(t, j, 1);
-                    if (j + 1 == n_tiles[t]) commit(L::B_O_READY + t);
-                    if (t == Q_TILES - 1) commit(L::B_V_EMPTY + st);
-                    if (j + 1 < n_tiles[t]) {
-                        if (!(ok = wait_bar_warp(bar(L::B_K_FULL + st1), ph1, ctl, SITE_MMA_K_FULL)))
+            bool ok = true;
+            if constexpr (S_RING<D>) {
+                // S product k (issue order of s_seq) goes to buffer k mod 3, whose previous
+                // product, k - 3, has had its PV issued just before (MMAs of one thread run in
+                // order, so S product k overwrites P only after that PV has read it). Tile 1
+                // (n1 >= n0) is the last user of every K and V tile.
+                auto seq_at = [&](int k, int& t, int& j) {
+                    if (k < 2 * n0) {
+                        t = k & 1;
+                        j = k >> 1;
+                    } else {
+                        t = 1;
+                        j = k - n0;
+                    }
+                };
+                const int total = n0 + n1;
+                for (int k = 0; ok && k < total + 3; ++k) {
+                    if (k >= 3) {
+                        int t, j;
+                        seq_at(k - 3, t, j);
+                        const int st = j % STAGES;
+                        if (!(ok = wait_bar_warp(bar(L::B_V_FULL + st), (j / STAGES) & 1, ctl,
+                                                 SITE_MMA_V_FULL) &&
+                                   wait_bar_warp(bar(L::hand(L::B_P_HALF, t, j, n0)),
+                                                 L::hand_parity(t, j, n0), ctl, SITE_MMA_P_FULL)))
                             break;
                         ptx::tc_fence_after();
-                        issue_s(t, j + 1);
-                        commit(L::B_S_FULL + t);
-                        if (t == Q_TILES - 1) commit(L::B_K_EMPTY + st1);
+                        issue_pv(t, j, 0);
+                        if (!(ok = wait_bar_warp(bar(L::hand(L::B_P_FULL, t, j, n0)),
+                                                 L::hand_parity(t, j, n0), ctl, SITE_MMA_P_FULL)))
+                            break;
+                        ptx::tc_fence_after();
+                        issue_pv(t, j, 1);
+                        commit(L::B_O_DONE + t);
+                        if (j + 1 == n_tiles[t]) commit(L::B_O_READY + t);
+                        if (t == Q_TILES - 1) commit(L::B_V_EMPTY + st);
+                    }
+                    if (k < total) {
+                        int t, j;
+                        seq_at(k, t, j);
+                        const int st = j % STAGES;
+                        if (!(ok = (j > 0 ||
+                                    wait_bar_warp(bar(q_ready + t), 0, ctl, SITE_MMA_Q_FULL)) &&
+                                   wait_bar_warp(bar(L::B_K_FULL + st), (j / STAGES) & 1, ctl,
+                                                 SITE_MMA_K_FULL)))
+                            break;
+                        ptx::tc_fence_after();
+                        issue_s(t, j);
+                        commit(L::hand(L::B_S_FULL, t, j, n0));
+                        if (t == Q_TILES - 1) commit(L::B_K_EMPTY + st);
+                    }
+                }
+            } else {
+                // Per key tile j: PV_0(j), S_0(j+1), PV_1(j), S_1(j+1). S_t(j+1) overwrites the TMEM
+                // columns P_t(j) occupies, so it follows PV_t(j) (MMAs of one thread run in order).
+                ok = wait_bar_warp(bar(q_ready + 0), 0, ctl, SITE_MMA_Q_FULL) &&
+                     wait_bar_warp(bar(L::B_K_FULL + 0), 0, ctl, SITE_MMA_K_FULL);
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_s(0, 0);
+                    commit(L::B_S_FULL + 0);
+                    ok = wait_bar_warp(bar(q_ready + 1), 0, ctl, SITE_MMA_Q_FULL);
+                }
+                if (ok) {
+                    ptx::tc_fence_after();
+                    issue_s(1, 0);
+                    commit(L::B_S_FULL + 1);
+                    commit(L::B_K_EMPTY + 0);
+                }
+                for (int j = 0; ok && j < n1; ++j) {
+                    const int st = j % STAGES, st1 = (j + 1) % STAGES;
+                    const uint32_t ph1 = ((j + 1) / STAGES) & 1;
+                    if (!(ok = wait_bar_warp(bar(L::B_V_FULL + st), (j / STAGES) & 1, ctl,
+                                             SITE_MMA_V_FULL)))
+                        break;
+                    for (int t = 0; t < Q_TILES; ++t) {
+                        if (j >= n_tiles[t]) continue;
+                        if (!(ok = wait_bar_warp(bar(L::B_P_HALF + t), j & 1, ctl, SITE_MMA_P_FULL)))
+                            break;
+                        ptx::tc_fence_after();
+                        issue_pv(t, j, 0);
+                        if (!(ok = wait_bar_warp(bar(L::B_P_FULL + t), j & 1, ctl, SITE_MMA_P_FULL)))
+                            break;
+                        ptx::tc_fence_after();
+                        issue_pv(t, j, 1);
+                        if (j + 1 == n_tiles[t]) commit(L::B_O_READY + t);
+                        if (t == Q_TILES - 1) commit(L::B_V_EMPTY + st);
+                        if (j + 1 < n_tiles[t]) {
+                            if (!(ok = wait_bar_warp(bar(L::B_K_FULL + st1), ph1, ctl,
+                                                     SITE_MMA_K_FULL)))
+                                break;
+                            ptx::tc_fence_after();
+                            issue_s(t, j + 1);
+                            commit(L::B_S_FULL + t);
+                            if (t == Q_TILES - 1) commit(L::B_K_EMPTY + st1);
+                        }
                     }
                 }
             }
-            (void)n0;
             if (*abort_flag) {
                 // Drain: wait until every MMA this warp issued has finished.
                 commit(L::B_DRAIN);
@@ -905,7 +1011,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::regs_inc<REG_SOFTMAX>();
         if (p.rope_cos == nullptr || rotate_q<D, BF16>(sbase, p, ctl, q0))
             softmax_role<D, BF16, CAUSAL>(wg, tmem, sbase, p, ctl, bh, q0, split, kv0, n_tiles[wg],
-                                          &tm_o);
+                                          n_tiles[0], &tm_o);
         ptx::tmem_wait_st();  // no TMEM store of this warp may be pending at dealloc
     }
 
