@@ -45,15 +45,20 @@ def main(path: str) -> None:
             print(f"\n{r['what']} ({r['shape']}, every element, O written in fp32 before rounding): "
                   f"max abs err {r['max_err']:.3e}, mean {r['mean_err']:.3e}, against the literal "
                   f"1e-2 and 1e-3.")
-    others = [r for r in recs if r.get("shape") and "rel_norm_err" not in r
+    others = [r for r in recs if "rel_norm_err" not in r
               and fwd.get(r.get("what")) is not r and not str(r.get("what", "")).endswith("fp32 output")]
     if others:
         worst = max(others, key=lambda r: r["mean_err"] / r["mean_bound"])
-        print(f"\nOther comparisons: {len(others)} (edge shapes, negative and zero scale, split over "
-              f"keys, rotary inputs, LSE cases). Largest mean |err| relative to its bound: "
-              f"{worst['what']} ({worst['shape']}), mean {worst['mean_err']:.3e} against "
-              f"{worst['mean_bound']:.2e} ({worst['mean_reading']}); largest max |err| of them: "
-              f"{max(r['max_err'] for r in others):.3e}.")
+        unshaped = sum(1 for r in others if not r.get("shape"))
+        within = all(r["worst_excess"] <= 0 and r["mean_err"] <= r["mean_bound"] for r in others)
+        print(f"\nOther comparisons: {len(others)} (edge shapes, negative and zero scale, rising "
+              f"maxima, lazy-rescale thresholds, split over keys, rotary inputs, LSE cases, "
+              f"streams and graphs; {unshaped} recorded without their shape). Largest mean |err| "
+              f"relative to its bound: {worst['what']} ({worst.get('shape') or 'shape not recorded'}), "
+              f"mean {worst['mean_err']:.3e} against {worst['mean_bound']:.2e} "
+              f"({worst['mean_reading']}); largest max |err| of them: "
+              f"{max(r['max_err'] for r in others):.3e}; "
+              f"{'every one within its bar' if within else 'NOT all within their bars'}.")
     bwd = [r for r in recs if "rel_norm_err" in r]
     if bwd:
         print("\n| backward gradient | shape | elements | norm error / norm | max error / largest magnitude |")

@@ -133,6 +133,7 @@ def test_late_maximum(fa, orc):
             "v": inputs.round_to_bits(v, "f16")}
     o = run_gpu(fa, bits, w)
     ref = orc.attention(*(inputs.bits_to_f64(bits[x], "f16") for x in "qkv"), 1.0)
+    parity.describe(w)
     parity.assert_parity(parity.compare(inputs.from_torch(o), ref, "f16"), True, "late max")
 
 
@@ -173,6 +174,7 @@ def test_zero_scale_gives_mean(fa, orc, causal):
     bits = inputs.draw(w)
     o = inputs.from_torch(run_gpu(fa, bits, w))
     ref = orc.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"), 0.0, causal)
+    parity.describe(w)
     parity.assert_parity(parity.compare(o, ref, w.dtype), True, "scale 0")
     v = inputs.bits_to_f64(bits["v"], w.dtype)
     if causal:
@@ -236,6 +238,7 @@ def test_rescale_threshold_choices_agree(fa, orc, dtype, taus):
     w = inputs.WORKLOADS["rescale_stress"].with_(B=1, H=2, Nq=2048, Nk=2048, dtype=dtype)
     bits = inputs.draw(w)
     ref = orc.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"), w.scale, w.causal)
+    parity.describe(w)
     old = fa.get_rescale_threshold()
     try:
         outs = {}
@@ -263,6 +266,7 @@ def test_rescale_on_every_rise_at_d64(fa, orc, causal):
                                                  seed=30 + causal)
     bits = inputs.draw(w)
     ref = orc.attention(*(inputs.bits_to_f64(bits[n], w.dtype) for n in "qkv"), w.scale, w.causal)
+    parity.describe(w)
     old = fa.get_rescale_threshold()
     try:
         for tau in (0.0, 15.0):
@@ -352,6 +356,7 @@ def test_long_context_chunk_full_size(fa, orc):
     torch.cuda.synchronize()
     assert fa.last_device_error() == (0, 0)
     rows = np.array([0, 1, 63, 64, 127])
+    parity.describe(w)
     for h in (0, w.H - 1):
         ref = orc.attention_rows(inputs.bits_to_f64(bits["q"][0, h, rows], w.dtype), rows,
                                  inputs.bits_to_f64(bits["k"][0, h], w.dtype),
@@ -368,6 +373,7 @@ def test_many_slices_with_split_last_wave(fa, orc):
     w = inputs.Workload("many_slices", 64, 32, 128, 1024, 64, "bf16", False, seed=14)
     bits = inputs.draw(w)
     o = inputs.from_torch(run_gpu(fa, bits, w))
+    parity.describe(w)
     for b, h in ((0, 0), (31, 7), (62, 31), (63, 30), (63, 31)):
         ref = orc.attention(*(inputs.bits_to_f64(bits[n][b, h], w.dtype) for n in "qkv"),
                             w.scale, False)
