@@ -45,8 +45,8 @@
 // D = 64: the two O accumulators leave room for a third S/P buffer, and the S products of both
 // tiles rotate through the three (the k-th S product of the CTA, in issue order, goes to buffer
 // k mod 3). The MMA warp issues PV of product k - 3, which frees its buffer, then S product k. A
-// tile's next S then lands while its softmax still works on the current one, and each softmax
-// runs its key steps back to back.
+// tile's next S product no longer waits for the PV product of its current one, so it can be
+// computed while the tile's softmax still works on the current step.
 //
 // Tensor memory (512 columns x 128 lanes of 32 bit):
 //   D = 128: [0,128) S_0 (fp32), its first 64 columns take P_0 (16-bit pairs) once S_0 is read;
